@@ -1,0 +1,45 @@
+"""Second, loop-based oracle for tiny shapes.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring).
+
+Pure Python: every dot product and sum is a ``math.fsum`` (exactly rounded
+sum), and the softmax is written with no maximum subtraction,
+p_j = e^(s_j) / sum_k e^(s_k), so it checks the vectorised oracle's max-shift
+arithmetic instead of repeating it.  Valid only while every |s_j| is small
+enough for e^(s_j) to stay finite (the tests keep |s| < 50).
+"""
+
+from __future__ import annotations
+
+import math
+
+
+def attention_bruteforce(q, k, v, seqlens, scale):
+    """Exact single-query attention by definition.
+
+    q: nested lists [B][Hq][D]; k, v: [B][Lcap][Hkv][D]; seqlens: list or None.
+    Query head h reads kv head h // (Hq // Hkv).  Returns (O, LSE) as nested
+    lists; an empty history gives O = 0 and LSE = -inf.
+    """
+    B = len(q)
+    Hq = len(q[0])
+    D = len(q[0][0])
+    Lcap = len(k[0])
+    Hkv = len(k[0][0])
+    G = Hq // Hkv
+    O = [[[0.0] * D for _ in range(Hq)] for _ in range(B)]
+    LSE = [[-math.inf] * Hq for _ in range(B)]
+    for b in range(B):
+        n = Lcap if seqlens is None else int(seqlens[b])
+        for h in range(Hq):
+            g = h // G
+            if n == 0:
+                continue
+            s = [scale * math.fsum(q[b][h][d] * k[b][j][g][d] for d in range(D))
+                 for j in range(n)]
+            e = [math.exp(x) for x in s]
+            z = math.fsum(e)
+            LSE[b][h] = math.log(z)
+            for d in range(D):
+                O[b][h][d] = math.fsum(e[j] * v[b][j][g][d] for j in range(n)) / z
+    return O, LSE
