@@ -1,0 +1,685 @@
+// C ABI of the decode-attention library: argument validation, kernel
+// selection, stream-ordered workspace, TMA descriptors, error state and
+// kernel timing hooks.  Host code only; kernels live in fd_kernels.cu.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <initializer_list>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/fd_decode.h"
+#include "fd_internal.h"
+
+namespace fd {
+cudaError_t read_and_clear_device_error(unsigned int* bits, cudaStream_t st);
+}
+
+using namespace fd;
+
+namespace {
+
+// ------------------------------------------------------------------ errors
+
+thread_local std::string g_last_error;
+
+fd_status fail(fd_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+fd_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ------------------------------------------------------------------ device info
+
+struct DeviceInfo {
+  bool ok = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+  cudaMemPool_t pool = nullptr;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+fd_status current_device(int* dev_out, DeviceInfo** info_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(FD_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ok) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(cc major)");
+    e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(cc minor)");
+    if (!(d.major == 10 && d.minor == 3))
+      return fail(FD_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                  d.major, d.minor);
+    // A library-private stream-ordered pool that keeps freed workspace cached.
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    e = cudaMemPoolCreate(&d.pool, &props);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+    uint64_t thresh = ~0ull;
+    e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &thresh);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
+    d.ok = true;
+  }
+  *dev_out = dev;
+  *info_out = &d;
+  return FD_OK;
+}
+
+// ------------------------------------------------------------------ profiling
+
+struct ProfRecord {
+  cudaEvent_t start, stop;
+};
+struct ProfState {
+  bool on = false;
+  std::vector<ProfRecord> rec[FD_KERNEL_KINDS];
+  std::vector<ProfRecord> pool;
+} g_prof;
+std::mutex g_prof_mu;
+
+bool prof_begin(int kind, cudaStream_t st, ProfRecord* r) {
+  if (!g_prof.on) return false;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof.pool.empty()) {
+    *r = g_prof.pool.back();
+    g_prof.pool.pop_back();
+  } else {
+    if (cudaEventCreate(&r->start) != cudaSuccess) return false;
+    if (cudaEventCreate(&r->stop) != cudaSuccess) return false;
+  }
+  cudaEventRecord(r->start, st);
+  (void)kind;
+  return true;
+}
+
+void prof_end(int kind, cudaStream_t st, bool active, const ProfRecord& r) {
+  if (!active) return;
+  cudaEventRecord(r.stop, st);
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof.rec[kind].push_back(r);
+}
+
+// ------------------------------------------------------------------ TMA maps
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+fd_status get_encoder() {
+  if (g_encode) return FD_OK;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return fail(FD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return FD_OK;
+}
+
+// 4-D bf16 map over a [B, L, Hkv, D] cache with box {D, 1, tile, 1}.
+bool make_kv_map(CUtensorMap* map, const void* base, int64_t B, int64_t L, int64_t Hkv,
+                 int64_t D, int64_t sb, int64_t sl, int64_t sh, int tile) {
+  const int64_t esz = 2;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)L, (cuuint64_t)B};
+  // A unit batch extent never steps along its stride; give it a legal one.
+  const int64_t sb_eff = (B == 1) ? sl * L : sb;
+  cuuint64_t strides[3] = {(cuuint64_t)(sh * esz), (cuuint64_t)(sl * esz),
+                           (cuuint64_t)(sb_eff * esz)};
+  cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)tile, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ validation
+
+int64_t esize(int32_t dt) { return dt == FD_BF16 ? 2 : 4; }
+
+fd_status check_tensor(const fd_tensor* t, const char* name, int ndim) {
+  if (t == nullptr) return fail(FD_ERR_NULL, "%s descriptor is NULL", name);
+  if (t->ndim != ndim) return fail(FD_ERR_SHAPE, "%s must have %d dims, got %d", name, ndim, t->ndim);
+  int64_t numel = 1;
+  for (int i = 0; i < ndim; ++i) {
+    if (t->shape[i] < 0) return fail(FD_ERR_SHAPE, "%s has a negative extent", name);
+    numel *= t->shape[i];
+  }
+  if (numel > 0 && t->data == nullptr) return fail(FD_ERR_NULL, "%s data pointer is NULL", name);
+  if (t->dtype != FD_F32 && t->dtype != FD_BF16 && t->dtype != FD_I32)
+    return fail(FD_ERR_DTYPE, "%s has unknown dtype %d", name, t->dtype);
+  if (t->stride[ndim - 1] != 1 && t->shape[ndim - 1] > 1)
+    return fail(FD_ERR_LAYOUT, "%s innermost stride must be 1", name);
+  for (int i = 0; i < ndim; ++i)
+    if (t->stride[i] < 0) return fail(FD_ERR_LAYOUT, "%s has a negative stride", name);
+  if (reinterpret_cast<uintptr_t>(t->data) % esize(t->dtype) != 0)
+    return fail(FD_ERR_LAYOUT, "%s data pointer is not element-aligned", name);
+  return FD_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DecodeDesc {
+  int64_t B, Hq, Hkv, D, Lcap, G;
+  int32_t q_dt, kv_dt;
+};
+
+// Validates q / k / v / seqlens / out / lse of a decode call.  `out_dims`
+// 3: out [B,Hq,D], lse [B,Hq];  4: partials out [B,Hq,ns,D], lse [B,Hq,ns].
+fd_status validate_decode(const fd_tensor* q, const fd_tensor* k, const fd_tensor* v,
+                          const fd_tensor* seqlens, const fd_tensor* out, const fd_tensor* lse,
+                          int out_dims, int ns, DecodeDesc* d) {
+  fd_status st;
+  if ((st = check_tensor(q, "q", 3))) return st;
+  if ((st = check_tensor(k, "k_cache", 4))) return st;
+  if ((st = check_tensor(v, "v_cache", 4))) return st;
+  if ((st = check_tensor(out, "out", out_dims))) return st;
+  if (lse && (st = check_tensor(lse, "lse", out_dims - 1))) return st;
+  if (seqlens && (st = check_tensor(seqlens, "seqlens", 1))) return st;
+  d->B = q->shape[0];
+  d->Hq = q->shape[1];
+  d->D = q->shape[2];
+  d->Lcap = k->shape[1];
+  d->Hkv = k->shape[2];
+  for (int i = 0; i < 4; ++i)
+    if (k->shape[i] != v->shape[i]) return fail(FD_ERR_SHAPE, "k_cache and v_cache shapes differ");
+  if (k->shape[0] != d->B) return fail(FD_ERR_SHAPE, "k_cache batch %lld != q batch %lld",
+                                       (long long)k->shape[0], (long long)d->B);
+  if (k->shape[3] != d->D) return fail(FD_ERR_SHAPE, "k_cache head dim != q head dim");
+  if (q->dtype != FD_BF16 && q->dtype != FD_F32) return fail(FD_ERR_DTYPE, "q must be bf16 or f32");
+  if (k->dtype != v->dtype) return fail(FD_ERR_DTYPE, "k_cache and v_cache dtypes differ");
+  if (k->dtype != FD_BF16 && k->dtype != FD_F32)
+    return fail(FD_ERR_DTYPE, "k_cache/v_cache must be bf16 or f32");
+  if (out->dtype != FD_F32) return fail(FD_ERR_DTYPE, "out must be f32");
+  if (lse && lse->dtype != FD_F32) return fail(FD_ERR_DTYPE, "lse must be f32");
+  if (seqlens) {
+    if (seqlens->dtype != FD_I32) return fail(FD_ERR_DTYPE, "seqlens must be int32");
+    if (seqlens->shape[0] != d->B) return fail(FD_ERR_SHAPE, "seqlens must have B entries");
+    if (seqlens->stride[0] != 1 && d->B > 1) return fail(FD_ERR_LAYOUT, "seqlens must be contiguous");
+  }
+  if (out_dims == 3) {
+    if (out->shape[0] != d->B || out->shape[1] != d->Hq || out->shape[2] != d->D)
+      return fail(FD_ERR_SHAPE, "out must be [B, Hq, D]");
+    if (lse && (lse->shape[0] != d->B || lse->shape[1] != d->Hq))
+      return fail(FD_ERR_SHAPE, "lse must be [B, Hq]");
+  } else {
+    if (out->shape[0] != d->B || out->shape[1] != d->Hq || out->shape[2] != ns || out->shape[3] != d->D)
+      return fail(FD_ERR_SHAPE, "part_o must be [B, Hq, num_splits, D]");
+    if (lse && (lse->shape[0] != d->B || lse->shape[1] != d->Hq || lse->shape[2] != ns))
+      return fail(FD_ERR_SHAPE, "part_lse must be [B, Hq, num_splits]");
+  }
+  if (d->Hkv < 1 || d->Hq < 1 || d->Hq % d->Hkv != 0)
+    return fail(FD_ERR_UNSUPPORTED, "Hq (%lld) must be a positive multiple of Hkv (%lld)",
+                (long long)d->Hq, (long long)d->Hkv);
+  if (d->D != 64 && d->D != 128) return fail(FD_ERR_UNSUPPORTED, "head dim %lld not in {64, 128}", (long long)d->D);
+  if (d->B > 65535 || d->Hq > 65535) return fail(FD_ERR_UNSUPPORTED, "batch and query heads must be <= 65535");
+  if (d->Lcap > (int64_t)INT32_MAX - 2 * kSplitAlign) return fail(FD_ERR_UNSUPPORTED, "cache length too large");
+  d->G = d->Hq / d->Hkv;
+  d->q_dt = q->dtype;
+  d->kv_dt = k->dtype;
+  return FD_OK;
+}
+
+// Whether the TMA kernel can stream this cache: bf16, head dim 128, 16-byte
+// aligned base and strides (token, kv head, batch), a group size it is
+// instantiated for.
+bool tma_ok(const DecodeDesc& d, const void* kd, const void* vd, const int64_t (&strides)[6],
+            int64_t batch_extent) {
+  if (d.kv_dt != FD_BF16 || d.D != 128 || d.Lcap < kSplitTileTokens) return false;
+  if (!(d.G == 1 || d.G == 2 || d.G == 4 || d.G == 8 || d.G == 16 || d.G == 32 || d.G == 64)) return false;
+  if (!aligned16(kd) || !aligned16(vd)) return false;
+  for (int i = 0; i < 6; ++i) {
+    if (i >= 4 && batch_extent == 1) continue;   // batch strides unused
+    if (strides[i] <= 0 || (strides[i] * 2) % 16 != 0 || strides[i] * 2 >= (1ll << 40)) return false;
+  }
+  return true;
+}
+
+int32_t choose_splits_host(int64_t batch, int64_t kv_heads, int64_t max_len, int32_t num_sms) {
+  const int64_t units = batch * kv_heads;
+  if (batch <= 0 || kv_heads <= 0 || max_len <= 0 || num_sms <= 0) return 1;
+  int64_t ns = (2 * (int64_t)num_sms) / units;
+  const int64_t cap = (max_len + 255) / 256;
+  if (ns > cap) ns = cap;
+  if (ns > kMaxSplits) ns = kMaxSplits;
+  if (ns < 1) ns = 1;
+  return (int32_t)ns;
+}
+
+// Enqueue the split stage for one cache.
+fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor* k,
+                        const fd_tensor* v, const int32_t* seqlens, int ns, float scale,
+                        float* o, int64_t o_sb, int64_t o_sh, int64_t o_ss, float* lse,
+                        int64_t l_sb, int64_t l_sh, int64_t l_ss, bool kv_broadcast,
+                        cudaStream_t st) {
+  SplitParams p = {};
+  p.q = q->data;
+  p.q_sb = q->stride[0];
+  p.q_sh = q->stride[1];
+  p.q_bf16 = d.q_dt == FD_BF16;
+  p.k = k->data;
+  p.v = v->data;
+  // kv tensors are [B, L, Hkv, D] or, when broadcast, [L, Hkv, D]
+  const int dim0 = kv_broadcast ? 1 : 0;
+  p.k_sb = kv_broadcast ? 0 : k->stride[0];
+  p.k_sl = k->stride[1 - dim0];
+  p.k_sh = k->stride[2 - dim0];
+  p.v_sb = kv_broadcast ? 0 : v->stride[0];
+  p.v_sl = v->stride[1 - dim0];
+  p.v_sh = v->stride[2 - dim0];
+  p.seqlens = seqlens;
+  p.B = (int)d.B;
+  p.Hq = (int)d.Hq;
+  p.Hkv = (int)d.Hkv;
+  p.G = (int)d.G;
+  p.Lcap = (int)d.Lcap;
+  p.ns = ns;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.o = o;
+  p.o_sb = o_sb;
+  p.o_sh = o_sh;
+  p.o_ss = o_ss;
+  p.lse = lse;
+  p.l_sb = l_sb;
+  p.l_sh = l_sh;
+  p.l_ss = l_ss;
+  p.kv_batch_broadcast = kv_broadcast ? 1 : 0;
+
+  ProfRecord rec;
+  bool launched = false;
+  cudaError_t e = cudaSuccess;
+  const int64_t kv_batch = kv_broadcast ? 1 : d.B;
+  const int64_t strides[6] = {p.k_sl, p.k_sh, p.v_sl, p.v_sh, p.k_sb, p.v_sb};
+  if (tma_ok(d, k->data, v->data, strides, kv_batch)) {
+    fd_status gs = get_encoder();
+    if (gs) return gs;
+    CUtensorMap tmK, tmV;
+    const bool okk = make_kv_map(&tmK, k->data, kv_batch, d.Lcap, d.Hkv, d.D, p.k_sb, p.k_sl,
+                                 p.k_sh, kSplitTileTokens);
+    const bool okv = make_kv_map(&tmV, v->data, kv_batch, d.Lcap, d.Hkv, d.D, p.v_sb, p.v_sl,
+                                 p.v_sh, kSplitTileTokens);
+    if (okk && okv) {
+      const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
+      e = launch_split_tma(p, tmK, tmV, (int)d.D, (int)d.G, st, &launched);
+      prof_end(FD_KERNEL_SPLIT, st, prof && launched, rec);
+      if (prof && !launched) {
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        g_prof.pool.push_back(rec);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
+    }
+  }
+  if (!launched) {
+    const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
+    e = launch_split_generic(p, (int)d.D, d.kv_dt == FD_BF16, st);
+    prof_end(FD_KERNEL_SPLIT, st, prof, rec);
+    if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
+  }
+  return FD_OK;
+}
+
+fd_status enqueue_combine(const CombineParams& cp, cudaStream_t st, bool pdl) {
+  ProfRecord rec;
+  const bool prof = prof_begin(FD_KERNEL_COMBINE, st, &rec);
+  // Event records between the kernels would defeat the programmatic
+  // overlap, so timing runs launch the combine without it.
+  cudaError_t e = launch_combine(cp, st, pdl && !prof);
+  prof_end(FD_KERNEL_COMBINE, st, prof, rec);
+  if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+  return FD_OK;
+}
+
+int64_t workspace_bytes(int64_t B, int64_t Hq, int64_t D, int64_t ns) {
+  const int64_t o_bytes = B * Hq * ns * D * 4;
+  const int64_t l_bytes = B * Hq * ns * 4;
+  return ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* fd_version(void) { return "fd_decode 0.1 (sm_103a)"; }
+
+const char* fd_last_error(void) { return g_last_error.c_str(); }
+
+const char* fd_status_string(fd_status s) {
+  switch (s) {
+    case FD_OK: return "ok";
+    case FD_ERR_NULL: return "null pointer or descriptor";
+    case FD_ERR_SHAPE: return "shape mismatch";
+    case FD_ERR_DTYPE: return "unsupported dtype";
+    case FD_ERR_LAYOUT: return "unsupported layout or alignment";
+    case FD_ERR_ARG: return "invalid argument";
+    case FD_ERR_UNSUPPORTED: return "unsupported problem";
+    case FD_ERR_ARCH: return "unsupported GPU architecture";
+    case FD_ERR_CUDA: return "CUDA error";
+    case FD_ERR_DEVICE_BOUNDS: return "device saw a length outside [0, capacity]";
+    case FD_ERR_DEVICE_TIMEOUT: return "a bounded device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int32_t fd_choose_num_splits(int64_t batch, int64_t kv_heads, int64_t max_len, int32_t num_sms) {
+  return choose_splits_host(batch, kv_heads, max_len, num_sms);
+}
+
+fd_status fd_split_bounds(int64_t len, int32_t ns, int32_t i, int64_t* begin, int64_t* end) {
+  if (begin == nullptr || end == nullptr) return fail(FD_ERR_NULL, "begin/end is NULL");
+  if (ns < 1 || i < 0 || i >= ns || len < 0) return fail(FD_ERR_ARG, "bad split arguments");
+  const int64_t per = (len + ns - 1) / ns;
+  const int64_t chunk = ((per + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
+  const int64_t b0 = (int64_t)i * chunk;
+  *begin = b0 < len ? b0 : len;
+  *end = b0 + chunk < len ? b0 + chunk : len;
+  return FD_OK;
+}
+
+int64_t fd_workspace_bytes(int64_t batch, int64_t q_heads, int64_t head_dim, int32_t num_splits) {
+  if (batch < 0 || q_heads < 0 || head_dim < 0 || num_splits <= 1) return 0;
+  return workspace_bytes(batch, q_heads, head_dim, num_splits);
+}
+
+fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
+                              const fd_tensor* v_cache, const fd_tensor* seqlens,
+                              int32_t num_splits, float scale, fd_tensor* out, fd_tensor* lse,
+                              fd_stream stream) {
+  DecodeDesc d;
+  fd_status st = validate_decode(q, k_cache, v_cache, seqlens, out, lse, 3, 0, &d);
+  if (st) return st;
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
+  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  int dev;
+  DeviceInfo* info;
+  if ((st = current_device(&dev, &info))) return st;
+  if (d.B == 0 || d.Hq == 0) return FD_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int ns = num_splits > 0 ? num_splits : choose_splits_host(d.B, d.Hkv, d.Lcap, info->sms);
+  const int32_t* sl = seqlens ? reinterpret_cast<const int32_t*>(seqlens->data) : nullptr;
+  float* o = reinterpret_cast<float*>(out->data);
+  float* l = lse ? reinterpret_cast<float*>(lse->data) : nullptr;
+  if (ns == 1) {
+    return enqueue_split(d, q, k_cache, v_cache, sl, 1, scale, o, out->stride[0], out->stride[1],
+                         0, l, lse ? lse->stride[0] : 0, lse ? lse->stride[1] : 0, 0, false, cs);
+  }
+  const int64_t bytes = workspace_bytes(d.B, d.Hq, d.D, ns);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)bytes, info->pool, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  float* po = reinterpret_cast<float*>(ws);
+  float* pl = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
+                                       ((d.B * d.Hq * ns * d.D * 4 + 255) / 256) * 256);
+  st = enqueue_split(d, q, k_cache, v_cache, sl, ns, scale, po, d.Hq * ns * d.D, ns * d.D, d.D,
+                     pl, d.Hq * ns, ns, 1, false, cs);
+  if (st == FD_OK) {
+    CombineParams cp = {};
+    cp.part_o = po;
+    cp.po_r1 = d.Hq * ns * d.D;
+    cp.po_r2 = ns * d.D;
+    cp.po_s = d.D;
+    cp.part_lse = pl;
+    cp.pl_r1 = d.Hq * ns;
+    cp.pl_r2 = ns;
+    cp.pl_s = 1;
+    cp.out = o;
+    cp.out_r1 = out->stride[0];
+    cp.out_r2 = out->stride[1];
+    cp.lse = l;
+    cp.lse_r1 = lse ? lse->stride[0] : 0;
+    cp.lse_r2 = lse ? lse->stride[1] : 0;
+    cp.R1 = (int)d.B;
+    cp.R2 = (int)d.Hq;
+    cp.S = ns;
+    cp.D = (int)d.D;
+    st = enqueue_combine(cp, cs, true);
+  }
+  e = cudaFreeAsync(ws, cs);
+  if (st) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return FD_OK;
+}
+
+fd_status fd_decode_attention_partials(const fd_tensor* q, const fd_tensor* k_cache,
+                                       const fd_tensor* v_cache, const fd_tensor* seqlens,
+                                       int32_t num_splits, float scale, fd_tensor* part_o,
+                                       fd_tensor* part_lse, fd_stream stream) {
+  if (num_splits < 1 || num_splits > kMaxSplits)
+    return fail(FD_ERR_ARG, "num_splits %d outside [1, %d]", num_splits, kMaxSplits);
+  DecodeDesc d;
+  fd_status st =
+      validate_decode(q, k_cache, v_cache, seqlens, part_o, part_lse, 4, num_splits, &d);
+  if (st) return st;
+  if (!part_lse) return fail(FD_ERR_NULL, "part_lse is required");
+  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  int dev;
+  DeviceInfo* info;
+  if ((st = current_device(&dev, &info))) return st;
+  if (d.B == 0 || d.Hq == 0) return FD_OK;
+  const int32_t* sl = seqlens ? reinterpret_cast<const int32_t*>(seqlens->data) : nullptr;
+  return enqueue_split(d, q, k_cache, v_cache, sl, num_splits, scale,
+                       reinterpret_cast<float*>(part_o->data), part_o->stride[0],
+                       part_o->stride[1], part_o->stride[2],
+                       reinterpret_cast<float*>(part_lse->data), part_lse->stride[0],
+                       part_lse->stride[1], part_lse->stride[2], false,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+fd_status fd_lse_combine(const fd_tensor* part_o, const fd_tensor* part_lse, fd_tensor* out,
+                         fd_tensor* lse, fd_stream stream) {
+  fd_status st;
+  if ((st = check_tensor(part_o, "part_o", 3))) return st;
+  if ((st = check_tensor(part_lse, "part_lse", 2))) return st;
+  if ((st = check_tensor(out, "out", 2))) return st;
+  if (lse && (st = check_tensor(lse, "lse", 1))) return st;
+  const int64_t R = part_o->shape[0], S = part_o->shape[1], D = part_o->shape[2];
+  if (part_o->dtype != FD_F32 || part_lse->dtype != FD_F32 || out->dtype != FD_F32)
+    return fail(FD_ERR_DTYPE, "combine tensors must be f32");
+  if (lse && lse->dtype != FD_F32) return fail(FD_ERR_DTYPE, "lse must be f32");
+  if (part_lse->shape[0] != R || part_lse->shape[1] != S)
+    return fail(FD_ERR_SHAPE, "part_lse must be [R, S]");
+  if (out->shape[0] != R || out->shape[1] != D) return fail(FD_ERR_SHAPE, "out must be [R, D]");
+  if (lse && lse->shape[0] != R) return fail(FD_ERR_SHAPE, "lse must be [R]");
+  if (D % 4 != 0 || D > 512 || D < 4) return fail(FD_ERR_UNSUPPORTED, "D must be a multiple of 4 in [4, 512]");
+  if (S < 1 || S > 4096) return fail(FD_ERR_UNSUPPORTED, "S must be in [1, 4096]");
+  if (R > INT32_MAX) return fail(FD_ERR_UNSUPPORTED, "too many rows");
+  if (!aligned16(part_o->data) || part_o->stride[0] % 4 != 0 || part_o->stride[1] % 4 != 0)
+    return fail(FD_ERR_LAYOUT, "part_o must be 16-byte aligned with strides multiple of 4");
+  int dev;
+  DeviceInfo* info;
+  if ((st = current_device(&dev, &info))) return st;
+  if (R == 0) return FD_OK;
+  CombineParams cp = {};
+  cp.part_o = reinterpret_cast<const float*>(part_o->data);
+  cp.po_r1 = 0;
+  cp.po_r2 = part_o->stride[0];
+  cp.po_s = part_o->stride[1];
+  cp.part_lse = reinterpret_cast<const float*>(part_lse->data);
+  cp.pl_r1 = 0;
+  cp.pl_r2 = part_lse->stride[0];
+  cp.pl_s = part_lse->stride[1];
+  cp.out = reinterpret_cast<float*>(out->data);
+  cp.out_r1 = 0;
+  cp.out_r2 = out->stride[0];
+  cp.lse = lse ? reinterpret_cast<float*>(lse->data) : nullptr;
+  cp.lse_r1 = 0;
+  cp.lse_r2 = lse ? lse->stride[0] : 0;
+  cp.R1 = 1;
+  cp.R2 = (int)R;
+  cp.S = (int)S;
+  cp.D = (int)D;
+  return enqueue_combine(cp, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx,
+                                      const fd_tensor* v_ctx, const fd_tensor* k_dec,
+                                      const fd_tensor* v_dec, const fd_tensor* dec_lens,
+                                      float scale, int32_t ctx_splits, fd_tensor* out,
+                                      fd_tensor* lse, fd_stream stream) {
+  fd_status st;
+  if ((st = check_tensor(q, "q", 3))) return st;
+  if ((st = check_tensor(k_ctx, "k_ctx", 3))) return st;
+  if ((st = check_tensor(v_ctx, "v_ctx", 3))) return st;
+  if ((st = check_tensor(k_dec, "k_dec", 4))) return st;
+  if ((st = check_tensor(v_dec, "v_dec", 4))) return st;
+  if ((st = check_tensor(out, "out", 3))) return st;
+  if (lse && (st = check_tensor(lse, "lse", 2))) return st;
+  if (dec_lens && (st = check_tensor(dec_lens, "dec_lens", 1))) return st;
+  const int64_t n = q->shape[0], Hq = q->shape[1], D = q->shape[2];
+  const int64_t Lc = k_ctx->shape[0], Hkv = k_ctx->shape[1], Ld = k_dec->shape[1];
+  for (int i = 0; i < 3; ++i)
+    if (k_ctx->shape[i] != v_ctx->shape[i]) return fail(FD_ERR_SHAPE, "k_ctx and v_ctx shapes differ");
+  for (int i = 0; i < 4; ++i)
+    if (k_dec->shape[i] != v_dec->shape[i]) return fail(FD_ERR_SHAPE, "k_dec and v_dec shapes differ");
+  if (k_ctx->shape[2] != D || k_dec->shape[3] != D) return fail(FD_ERR_SHAPE, "head dims differ");
+  if (k_dec->shape[0] != n) return fail(FD_ERR_SHAPE, "k_dec must have n samples");
+  if (k_dec->shape[2] != Hkv) return fail(FD_ERR_SHAPE, "k_dec and k_ctx kv heads differ");
+  if (out->shape[0] != n || out->shape[1] != Hq || out->shape[2] != D)
+    return fail(FD_ERR_SHAPE, "out must be [n, Hq, D]");
+  if (lse && (lse->shape[0] != n || lse->shape[1] != Hq)) return fail(FD_ERR_SHAPE, "lse must be [n, Hq]");
+  if (dec_lens) {
+    if (dec_lens->dtype != FD_I32) return fail(FD_ERR_DTYPE, "dec_lens must be int32");
+    if (dec_lens->shape[0] != n) return fail(FD_ERR_SHAPE, "dec_lens must have n entries");
+    if (dec_lens->stride[0] != 1 && n > 1) return fail(FD_ERR_LAYOUT, "dec_lens must be contiguous");
+  }
+  for (const fd_tensor* t : {q, k_ctx, v_ctx, k_dec, v_dec})
+    if (t->dtype != FD_BF16) return fail(FD_ERR_DTYPE, "bifurcated q/k/v must be bf16");
+  if (out->dtype != FD_F32 || (lse && lse->dtype != FD_F32)) return fail(FD_ERR_DTYPE, "out/lse must be f32");
+  if (Lc < 1) return fail(FD_ERR_SHAPE, "the shared context must hold at least one token");
+  if (Hkv < 1 || Hq % Hkv != 0) return fail(FD_ERR_UNSUPPORTED, "Hq must be a multiple of Hkv");
+  if (D != 64 && D != 128) return fail(FD_ERR_UNSUPPORTED, "head dim not in {64, 128}");
+  if (n > 65535 || Hq > 65535) return fail(FD_ERR_UNSUPPORTED, "n and Hq must be <= 65535");
+  if (Lc > (int64_t)INT32_MAX - 2 * kSplitAlign || Ld > (int64_t)INT32_MAX - 2 * kSplitAlign)
+    return fail(FD_ERR_UNSUPPORTED, "lengths too large");
+  if (ctx_splits < 0 || ctx_splits > kMaxSplits) return fail(FD_ERR_ARG, "ctx_splits out of range");
+  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  int dev;
+  DeviceInfo* info;
+  if ((st = current_device(&dev, &info))) return st;
+  if (n == 0 || Hq == 0) return FD_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+
+  const int ns_ctx = ctx_splits > 0 ? ctx_splits : choose_splits_host(n, Hkv, Lc, info->sms);
+  const int ns_dec = Ld > 0 ? 1 : 0;
+  const int S = ns_ctx + ns_dec;
+  const int64_t bytes = workspace_bytes(n, Hq, D, S);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)bytes, info->pool, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  float* po = reinterpret_cast<float*>(ws);
+  float* pl = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + ((n * Hq * S * D * 4 + 255) / 256) * 256);
+
+  // Context part: every sample reads the one shared context (batch stride 0).
+  DecodeDesc dc = {n, Hq, Hkv, D, Lc, Hq / Hkv, FD_BF16, FD_BF16};
+  st = enqueue_split(dc, q, k_ctx, v_ctx, nullptr, ns_ctx, scale, po, Hq * S * D, S * D, D, pl,
+                     Hq * S, S, 1, true, cs);
+  // Decode part: each sample's own tokens, one split, written after the
+  // context splits.
+  if (st == FD_OK && ns_dec) {
+    DecodeDesc dd = {n, Hq, Hkv, D, Ld, Hq / Hkv, FD_BF16, FD_BF16};
+    st = enqueue_split(dd, q, k_dec, v_dec,
+                       dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr, 1,
+                       scale, po + (int64_t)ns_ctx * D, Hq * S * D, S * D, 0, pl + ns_ctx, Hq * S,
+                       S, 0, false, cs);
+  }
+  if (st == FD_OK) {
+    CombineParams cp = {};
+    cp.part_o = po;
+    cp.po_r1 = Hq * S * D;
+    cp.po_r2 = S * D;
+    cp.po_s = D;
+    cp.part_lse = pl;
+    cp.pl_r1 = Hq * S;
+    cp.pl_r2 = S;
+    cp.pl_s = 1;
+    cp.out = reinterpret_cast<float*>(out->data);
+    cp.out_r1 = out->stride[0];
+    cp.out_r2 = out->stride[1];
+    cp.lse = lse ? reinterpret_cast<float*>(lse->data) : nullptr;
+    cp.lse_r1 = lse ? lse->stride[0] : 0;
+    cp.lse_r2 = lse ? lse->stride[1] : 0;
+    cp.R1 = (int)n;
+    cp.R2 = (int)Hq;
+    cp.S = S;
+    cp.D = (int)D;
+    st = enqueue_combine(cp, cs, true);
+  }
+  e = cudaFreeAsync(ws, cs);
+  if (st) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return FD_OK;
+}
+
+fd_status fd_bifurcated_attention(const fd_tensor* q, const fd_tensor* k_ctx,
+                                  const fd_tensor* v_ctx, const fd_tensor* k_dec,
+                                  const fd_tensor* v_dec, const fd_tensor* dec_lens, float scale,
+                                  fd_tensor* out, fd_stream stream) {
+  return fd_bifurcated_attention_lse(q, k_ctx, v_ctx, k_dec, v_dec, dec_lens, scale, 0, out,
+                                     nullptr, stream);
+}
+
+fd_status fd_check_device_error(fd_stream stream) {
+  unsigned int bits = 0;
+  cudaError_t e = read_and_clear_device_error(&bits, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (bits & FD_DEVERR_TIMEOUT) return fail(FD_ERR_DEVICE_TIMEOUT, "a bounded device wait timed out");
+  if (bits & FD_DEVERR_BOUNDS) return fail(FD_ERR_DEVICE_BOUNDS, "a length outside [0, capacity] was clamped");
+  return FD_OK;
+}
+
+fd_status fd_profile_enable(int32_t on) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (int k = 0; k < FD_KERNEL_KINDS; ++k) {
+    for (auto& r : g_prof.rec[k]) g_prof.pool.push_back(r);
+    g_prof.rec[k].clear();
+  }
+  g_prof.on = on != 0;
+  return FD_OK;
+}
+
+fd_status fd_profile_read(int32_t kind, int64_t* launches, double* total_ms) {
+  if (kind < 0 || kind >= FD_KERNEL_KINDS) return fail(FD_ERR_ARG, "unknown kernel kind");
+  if (!launches || !total_ms) return fail(FD_ERR_NULL, "output pointer is NULL");
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  double tot = 0.0;
+  for (auto& r : g_prof.rec[kind]) {
+    cudaError_t e = cudaEventSynchronize(r.stop);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    tot += ms;
+  }
+  *launches = (int64_t)g_prof.rec[kind].size();
+  *total_ms = tot;
+  return FD_OK;
+}
+
+}  // extern "C"

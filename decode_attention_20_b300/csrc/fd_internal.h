@@ -1,0 +1,66 @@
+// Internal host/device declarations of the decode-attention library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fd {
+
+// Device error word bits.
+constexpr unsigned int FD_DEVERR_BOUNDS = 1u;   // a length outside [0, capacity]
+constexpr unsigned int FD_DEVERR_TIMEOUT = 2u;  // a bounded wait gave up
+
+// Longest any on-device wait may spin before giving up (1 s).
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+
+constexpr int kSplitAlign = 64;   // FD_SPLIT_ALIGN
+constexpr int kMaxSplits = 256;   // FD_MAX_SPLITS
+
+// Arguments of the split-partial kernels (one CTA per (split, kv head, b)).
+struct SplitParams {
+  const void* q;              // [B, Hq, D]
+  int64_t q_sb, q_sh;         // element strides
+  int q_bf16;                 // 1: bf16, 0: fp32
+  const void* k;              // [B, Lcap, Hkv, D] (generic kernel only; the TMA
+  const void* v;              //  kernel reads through tensor maps)
+  int64_t k_sb, k_sl, k_sh;
+  int64_t v_sb, v_sl, v_sh;
+  const int32_t* seqlens;     // [B] or nullptr (= Lcap)
+  int B, Hq, Hkv, G, Lcap, ns;
+  float scale_log2;           // scale * log2(e): scores are kept in base 2
+  float* o;                   // partial (or final, ns == 1) output, fp32
+  int64_t o_sb, o_sh, o_ss;   // strides over (b, q head, split)
+  float* lse;                 // natural-log lse, or nullptr
+  int64_t l_sb, l_sh, l_ss;
+  int kv_batch_broadcast;     // 1: every sequence reads kv batch row 0
+};
+
+// Arguments of the log-sum-exp combine kernel.
+struct CombineParams {
+  const float* part_o;        // rows x splits x D
+  int64_t po_r1, po_r2, po_s; // row index r = r1 * R2 + r2 (two row dims) ; split stride
+  const float* part_lse;
+  int64_t pl_r1, pl_r2, pl_s;
+  float* out;
+  int64_t out_r1, out_r2;
+  float* lse;                 // may be nullptr
+  int64_t lse_r1, lse_r2;
+  int R1, R2, S, D;
+};
+
+// Host launchers (return a cudaError_t from the launch).
+cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, int D, int G, cudaStream_t st,
+                             bool* launched);
+cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16,
+                                 cudaStream_t st);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
+
+// Tile height (tokens) of the TMA split kernel; the tensor-map box uses it.
+constexpr int kSplitTileTokens = 64;
+
+// Host-side helpers (fd_api.cu).
+int split_chunk(int64_t len, int ns);
+
+}  // namespace fd

@@ -1,0 +1,94 @@
+// Device code of the decode-attention library and its host launchers.
+// (All device code lives in this translation unit, so the device error word
+// needs no relocatable device code.)
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fd_combine.cuh"
+#include "fd_internal.h"
+#include "fd_split.cuh"
+
+namespace fd {
+
+cudaError_t read_and_clear_device_error(unsigned int* bits, cudaStream_t st) {
+  unsigned int zero = 0u;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(bits, g_device_error, sizeof(unsigned int), 0,
+                                            cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(unsigned int), 0,
+                              cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(st);
+}
+
+template <int GH, int HC>
+static cudaError_t launch_tma_variant(const SplitParams& p, const CUtensorMap& tmK,
+                                      const CUtensorMap& tmV, cudaStream_t st) {
+  using C = TmaCfg<GH, HC>;
+  auto kern = split_tma_kernel<GH, HC>;
+  // The shared-memory opt-in is per (function, device): remember it per device.
+  static unsigned long long attr_set = 0ull;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set |= bit;
+  }
+  dim3 grid(p.ns, p.Hkv, p.B);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, int D, int G, cudaStream_t st,
+                             bool* launched) {
+  *launched = false;
+  if (D != 128) return cudaSuccess;
+  *launched = true;
+  switch (G) {
+    case 1: return launch_tma_variant<1, 1>(p, tmK, tmV, st);
+    case 2: return launch_tma_variant<2, 1>(p, tmK, tmV, st);
+    case 4: return launch_tma_variant<4, 1>(p, tmK, tmV, st);
+    case 8: return launch_tma_variant<8, 1>(p, tmK, tmV, st);
+    case 16: return launch_tma_variant<8, 2>(p, tmK, tmV, st);
+    case 32: return launch_tma_variant<8, 4>(p, tmK, tmV, st);
+    case 64: return launch_tma_variant<8, 8>(p, tmK, tmV, st);
+    default: *launched = false; return cudaSuccess;
+  }
+}
+
+cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaStream_t st) {
+  dim3 grid(p.ns, p.Hq, p.B);
+  if (D == 128) {
+    if (kv_bf16) split_generic_kernel<128, true><<<grid, 128, 0, st>>>(p);
+    else split_generic_kernel<128, false><<<grid, 128, 0, st>>>(p);
+  } else if (D == 64) {
+    if (kv_bf16) split_generic_kernel<64, true><<<grid, 128, 0, st>>>(p);
+    else split_generic_kernel<64, false><<<grid, 128, 0, st>>>(p);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
+  const int rows = p.R1 * p.R2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + kCombineWarps - 1) / kCombineWarps);
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, lse_combine_kernel, p);
+}
+
+}  // namespace fd

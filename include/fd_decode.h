@@ -1,0 +1,240 @@
+/*
+ * fd_decode.h — C ABI of the B300 (sm_103a) decode-attention library
+ * (libfd_decode.so).
+ *
+ * Exact single-query decode attention over a long KV cache, computed two ways:
+ *
+ *  1. Split-KV ("Flash-Decoding"): the cached history of every (sequence,
+ *     kv head) is cut into splits; independent CTAs each produce a partial
+ *     output and its log-sum-exp; a separate log-sum-exp reduction merges the
+ *     partials into the exact full-history result.
+ *     Source: "What is Flash-Decoding and when does it speed up LLMs?"
+ *     (slavadubrov.com), section "Why decoding needs different scheduling".
+ *
+ *  2. Bifurcated attention for single-context batch sampling: one context KV
+ *     shared by n samples is read once for all of them as a GEMM, a second
+ *     part covers each sample's own decode KV, and the two are merged exactly.
+ *     Source: summary of "Bifurcated Attention for Single-Context Large-Batch
+ *     Sampling" (linnk.ai), sections "Tiivistelmä" and "Tilastot".
+ *
+ * Definition computed (both entry points), for batch row b and query head h,
+ * with G = Hq / Hkv and kv head g = h / G (contiguous GQA groups):
+ *     s_j = scale * <q[b,h,:], K[b,j,g,:]>      for j < len_b
+ *     O[b,h,:] = sum_j softmax(s)_j * V[b,j,g,:]
+ *     LSE[b,h] = ln sum_j exp(s_j)              (natural log, scaled scores)
+ * len_b == 0 gives O = 0 and LSE = -inf.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors travel as fd_tensor descriptors: a data pointer, a dtype, a rank
+ *    and per-dimension shape and stride.  Strides are in ELEMENTS; the
+ *    innermost stride must be 1.  All data pointers given to compute entry
+ *    points are DEVICE pointers on the current CUDA device.
+ *  - Ownership: the caller owns every tensor and the stream.  The library
+ *    keeps no pointer after the call returns beyond the work it enqueued.
+ *  - Asynchrony: compute calls only enqueue work on `stream` (a cudaStream_t,
+ *    NULL = the legacy default stream) and return; outputs are valid once the
+ *    stream reaches that point.
+ *  - Errors: every call returns an fd_status.  Argument errors are detected on
+ *    the host before anything is enqueued (nothing is launched, outputs are
+ *    untouched).  fd_last_error() returns a thread-local message for the most
+ *    recent failure on the calling thread.  Data errors that only the device
+ *    can see (a seqlens entry outside [0, Lcap]) are clamped on the device and
+ *    recorded in a device error word that fd_check_device_error() reports.
+ *  - Workspace: calls that need scratch memory for partial results allocate
+ *    it stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`), so
+ *    calls on different streams or threads never share scratch.
+ */
+#ifndef FD_DECODE_H
+#define FD_DECODE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FD_API __attribute__((visibility("default")))
+#else
+#define FD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FD_MAX_DIMS 4
+/* Largest accepted num_splits. */
+#define FD_MAX_SPLITS 256
+/* Split partition granule in tokens (see fd_split_bounds). */
+#define FD_SPLIT_ALIGN 64
+
+typedef int32_t fd_status;
+enum {
+  FD_OK = 0,
+  FD_ERR_NULL = 1,          /* a required pointer or descriptor is NULL            */
+  FD_ERR_SHAPE = 2,         /* ranks or extents disagree                           */
+  FD_ERR_DTYPE = 3,         /* unsupported dtype combination                       */
+  FD_ERR_LAYOUT = 4,        /* inner stride != 1, or 16-byte alignment violated    */
+  FD_ERR_ARG = 5,           /* num_splits out of range, non-finite scale, ...      */
+  FD_ERR_UNSUPPORTED = 6,   /* head dim not in {64,128}, Hq % Hkv != 0, ...        */
+  FD_ERR_ARCH = 7,          /* current device is not sm_103 / sm_100 family       */
+  FD_ERR_CUDA = 8,          /* a CUDA runtime call failed                          */
+  FD_ERR_DEVICE_BOUNDS = 9, /* device saw a length outside [0, capacity]           */
+  FD_ERR_DEVICE_TIMEOUT = 10/* a bounded on-device wait gave up                    */
+};
+
+/* Element types. */
+enum { FD_F32 = 0, FD_BF16 = 1, FD_I32 = 2 };
+
+typedef struct fd_tensor {
+  void* data;                    /* device pointer (host pointer only where stated) */
+  int32_t dtype;                 /* FD_F32, FD_BF16 or FD_I32                      */
+  int32_t ndim;                  /* 1..4                                           */
+  int64_t shape[FD_MAX_DIMS];    /* extents, outermost first                        */
+  int64_t stride[FD_MAX_DIMS];   /* strides in elements, outermost first            */
+} fd_tensor;
+
+/* A cudaStream_t passed as an opaque pointer. */
+typedef void* fd_stream;
+
+/*
+ * fd_decode_attention — split-KV decode attention.
+ *   q        [B, Hq, D]            FD_BF16 or FD_F32
+ *   k_cache  [B, Lcap, Hkv, D]     FD_BF16 or FD_F32 (same dtype as v_cache)
+ *   v_cache  [B, Lcap, Hkv, D]
+ *   seqlens  [B] FD_I32 device tensor, or NULL meaning every len_b = Lcap.
+ *            Entries outside [0, Lcap] are clamped on the device and flagged
+ *            (FD_ERR_DEVICE_BOUNDS from fd_check_device_error).
+ *   num_splits  0 = choose with fd_choose_num_splits(B, Hkv, Lcap, #SMs);
+ *               1..FD_MAX_SPLITS = use that many splits per (b, kv head).
+ *   scale    finite multiplier of the dot product (typically 1/sqrt(D)).
+ *   out      [B, Hq, D] FD_F32 (written).
+ *   lse      [B, Hq] FD_F32 (written), or NULL.
+ * D must be 64 or 128 and Hq a multiple of Hkv.  Base pointers and the
+ * strides of k_cache / v_cache must be 16-byte aligned.
+ * Source: Flash-Decoding page, section "Why decoding needs different
+ * scheduling" (split the history, per-split partial + log-sum-exp, reduce).
+ */
+FD_API fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
+                              const fd_tensor* v_cache, const fd_tensor* seqlens,
+                              int32_t num_splits, float scale, fd_tensor* out,
+                              fd_tensor* lse, fd_stream stream);
+
+/*
+ * fd_decode_attention_partials — the split stage alone (diagnostics and
+ * partial-level tests).  Same inputs as fd_decode_attention with an explicit
+ * num_splits (1..FD_MAX_SPLITS); writes, instead of the merged result,
+ *   part_o   [B, Hq, num_splits, D] FD_F32: the NORMALISED partial output of
+ *            split i (attention restricted to fd_split_bounds(len_b, ns, i));
+ *   part_lse [B, Hq, num_splits] FD_F32: that split's log-sum-exp (natural
+ *            log); an empty split writes part_o = 0 and part_lse = -inf.
+ * Allocates nothing.
+ */
+FD_API fd_status fd_decode_attention_partials(const fd_tensor* q, const fd_tensor* k_cache,
+                                       const fd_tensor* v_cache, const fd_tensor* seqlens,
+                                       int32_t num_splits, float scale, fd_tensor* part_o,
+                                       fd_tensor* part_lse, fd_stream stream);
+
+/*
+ * fd_lse_combine — the log-sum-exp reduction alone.
+ *   part_o [R, S, D] FD_F32, part_lse [R, S] FD_F32 (S splits per row)
+ *   out    [R, D] FD_F32, lse [R] FD_F32 or NULL.
+ *   LSE = ln sum_i exp(lse_i);  O = sum_i exp(lse_i - LSE) * O_i;
+ *   rows whose lse_i are all -inf give O = 0, LSE = -inf.
+ * D must be a multiple of 4 and at most 512; S at most 4096.
+ * Source: Flash-Decoding page, section "Why decoding needs different
+ * scheduling" (the final reduction over partial results).
+ */
+FD_API fd_status fd_lse_combine(const fd_tensor* part_o, const fd_tensor* part_lse,
+                         fd_tensor* out, fd_tensor* lse, fd_stream stream);
+
+/*
+ * fd_bifurcated_attention — attention of n samples that share one context.
+ *   q        [n, Hq, D]            FD_BF16
+ *   k_ctx    [Lc, Hkv, D]          FD_BF16 (shared by every sample; Lc >= 1)
+ *   v_ctx    [Lc, Hkv, D]
+ *   k_dec    [n, Ld, Hkv, D]       FD_BF16 (sample i's own decode tokens)
+ *   v_dec    [n, Ld, Hkv, D]
+ *   dec_lens [n] FD_I32 device tensor, or NULL meaning all Ld.
+ *   out      [n, Hq, D] FD_F32.
+ * Sample i attends over concat(context, its first dec_lens[i] decode tokens).
+ * The context part runs as a tensor-core contraction whose rows are all
+ * (sample, query head) pairs of a kv-head group, so the context KV is read
+ * once for all samples; the decode part runs on the split kernel; partials
+ * are merged by the log-sum-exp reduction.
+ * Source: bifurcated-attention summary, section "Tiivistelmä" (two GEMMs,
+ * one over the prefill KV and one over the decode KV; exact result).
+ */
+FD_API fd_status fd_bifurcated_attention(const fd_tensor* q, const fd_tensor* k_ctx,
+                                  const fd_tensor* v_ctx, const fd_tensor* k_dec,
+                                  const fd_tensor* v_dec, const fd_tensor* dec_lens,
+                                  float scale, fd_tensor* out, fd_stream stream);
+
+/*
+ * fd_bifurcated_attention_lse — fd_bifurcated_attention that also writes
+ * lse [n, Hq] FD_F32 (may be NULL) and takes an explicit context split count
+ * (0 = library choice).
+ */
+FD_API fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx,
+                                      const fd_tensor* v_ctx, const fd_tensor* k_dec,
+                                      const fd_tensor* v_dec, const fd_tensor* dec_lens,
+                                      float scale, int32_t ctx_splits, fd_tensor* out,
+                                      fd_tensor* lse, fd_stream stream);
+
+/*
+ * fd_choose_num_splits — split-count heuristic (pure host function).
+ * Fill about two waves of CTAs: ns = floor(2 * num_sms / (batch * kv_heads)),
+ * at most ceil(max_len / 256), clamped to [1, FD_MAX_SPLITS].  Returns 1 for
+ * any non-positive argument.  The Flash-Decoding page ("Why decoding needs
+ * different scheduling") fixes only the direction: split when the batch
+ * leaves too few blocks, not when the history is short or the batch large.
+ */
+FD_API int32_t fd_choose_num_splits(int64_t batch, int64_t kv_heads, int64_t max_len,
+                             int32_t num_sms);
+
+/*
+ * fd_split_bounds — token range [*begin, *end) of split i (pure host function).
+ *   chunk = ceil(ceil(len / ns) / FD_SPLIT_ALIGN) * FD_SPLIT_ALIGN
+ *   begin = min(i * chunk, len), end = min((i + 1) * chunk, len).
+ * Returns FD_ERR_ARG (outputs untouched) unless 1 <= ns, 0 <= i < ns,
+ * len >= 0; FD_ERR_NULL if begin or end is NULL.
+ */
+FD_API fd_status fd_split_bounds(int64_t len, int32_t ns, int32_t i, int64_t* begin,
+                          int64_t* end);
+
+/* Bytes of scratch fd_decode_attention allocates for (B, Hq, D, ns). */
+FD_API int64_t fd_workspace_bytes(int64_t batch, int64_t q_heads, int64_t head_dim,
+                           int32_t num_splits);
+
+/*
+ * fd_check_device_error — SYNCHRONISES `stream`, then reads and clears the
+ * device error word of the current device.  Returns FD_OK, FD_ERR_DEVICE_BOUNDS
+ * (a length was clamped), FD_ERR_DEVICE_TIMEOUT (a bounded wait gave up; the
+ * affected outputs are undefined) or FD_ERR_CUDA.
+ */
+FD_API fd_status fd_check_device_error(fd_stream stream);
+
+/* Static English text for a status code. */
+FD_API const char* fd_status_string(fd_status status);
+
+/* Message of the last failing call on this thread ("" if none). */
+FD_API const char* fd_last_error(void);
+
+/*
+ * Kernel timing hooks.  While enabled, every kernel the library launches is
+ * bracketed by CUDA events recorded on its launch stream; fd_profile_read
+ * synchronises those events and returns, for one kernel kind, the number of
+ * launches and their summed duration in milliseconds since the last enable.
+ * Kernel kinds: 0 split partial, 1 log-sum-exp combine, 2 bifurcated context.
+ * Not thread-safe; meant for benchmarks.
+ */
+enum { FD_KERNEL_SPLIT = 0, FD_KERNEL_COMBINE = 1, FD_KERNEL_BIF_CTX = 2, FD_KERNEL_KINDS = 3 };
+FD_API fd_status fd_profile_enable(int32_t on);
+FD_API fd_status fd_profile_read(int32_t kernel_kind, int64_t* launches, double* total_ms);
+
+/* Library version string. */
+FD_API const char* fd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FD_DECODE_H */
