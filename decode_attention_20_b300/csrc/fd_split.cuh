@@ -104,10 +104,10 @@ struct TmaCfg {
   static constexpr int TILE_BYTES = T * D * 2;             // one K or V tile
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
-  static constexpr int P_FLOATS = NSLOT * NB * GH;
+  static constexpr int P_PAIRS = NSLOT * NB * GH;           // probabilities as (p, p)
   static constexpr int A_FLOATS = NSLOT * GH;
   static constexpr int SMEM_BYTES =
-      1024 /*align slack*/ + RING_BYTES + (P_FLOATS + A_FLOATS) * 4 + 2 * NSTAGE * 8 + 16;
+      1024 /*align slack*/ + RING_BYTES + P_PAIRS * 8 + A_FLOATS * 4 + 2 * NSTAGE * 8 + 16;
   static_assert(TS * TOK_PER_SLOT == T, "tile must split evenly over slots");
   static_assert(NBATCH >= 1 && NBATCH * NB == TOK_PER_SLOT, "whole batches per slot");
   static_assert(GH <= 8 && (GH & (GH - 1)) == 0, "GH must be 1, 2, 4 or 8");
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* P_s = reinterpret_cast<float*>(smem + C::RING_BYTES);
-  float* A_s = P_s + C::P_FLOATS;
+  float2* P_s = reinterpret_cast<float2*>(smem + C::RING_BYTES);   // (p, p) pairs
+  float* A_s = reinterpret_cast<float*>(P_s + C::P_PAIRS);
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(A_s + C::A_FLOATS);
   uint64_t* empty_bar = full_bar + C::NSTAGE;
   int* abort_s = reinterpret_cast<int*>(empty_bar + C::NSTAGE);
@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
   }
   __syncthreads();
 
-  // Consumer state (meaningful in consumer warps only).
   const int hc = warp % C::HC;
   const int slot = (warp / C::HC) * 2 + (lane >> 4);
   const int L = lane & 15;
@@ -163,7 +162,8 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
   const bool head_writer = (L & ((1 << (C::SH + C::NTB)) - 1)) == 0;
   const bool p_writer = (L & ((1 << C::SH) - 1)) == 0;
 
-  float acc[GH][C::EPL];
+  // Accumulators as (even, odd) head-dim pairs for the paired fp32 FMA.
+  float2 acc[GH][C::EPL / 2];
   float m_run = kNegInf, l_run = 0.f;
 
   // Tile issue (thread 0 only): tiles 0..NSTAGE-1 up front, then tile
@@ -184,26 +184,30 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
     }
   }
   {
-    // ------------------------------------------------------------ consumers
-    float qr[GH][C::EPL];
+    // Query registers, pre-scaled into base 2, as (even, odd) pairs, in the
+    // lane's physical head order.
+    float2 qr[GH][C::EPL / 2];
 #pragma unroll
     for (int ph = 0; ph < GH; ++ph) {
       const int h = g * C::G + hc * GH + (ph ^ mh);
+      float qv[C::EPL];
       if (p.q_bf16) {
         const uint16_t* qp =
             reinterpret_cast<const uint16_t*>(p.q) + b * p.q_sb + h * p.q_sh + L * C::EPL;
 #pragma unroll
-        for (int e = 0; e < C::EPL; ++e)
-          qr[ph][e] = __uint_as_float(uint32_t(qp[e]) << 16) * p.scale_log2;
+        for (int e = 0; e < C::EPL; ++e) qv[e] = __uint_as_float(uint32_t(qp[e]) << 16);
       } else {
         const float* qp = reinterpret_cast<const float*>(p.q) + b * p.q_sb + h * p.q_sh + L * C::EPL;
 #pragma unroll
-        for (int e = 0; e < C::EPL; ++e) qr[ph][e] = qp[e] * p.scale_log2;
+        for (int e = 0; e < C::EPL; ++e) qv[e] = qp[e];
       }
 #pragma unroll
-      for (int e = 0; e < C::EPL; ++e) acc[ph][e] = 0.f;
+      for (int e = 0; e < C::EPL / 2; ++e) {
+        qr[ph][e] = make_float2(qv[2 * e] * p.scale_log2, qv[2 * e + 1] * p.scale_log2);
+        acc[ph][e] = make_float2(0.f, 0.f);
+      }
     }
-    float* P_slot = P_s + (hc * C::TS + slot) * C::NB * GH;
+    float2* P_slot = P_s + (hc * C::TS + slot) * C::NB * GH;
     float* A_slot = A_s + (hc * C::TS + slot) * GH;
 
     for (int t = 0; t < ntiles; ++t) {
@@ -222,20 +226,17 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
         for (int pt = 0; pt < C::NB; ++pt) {
           const int row = (bi * C::NB + (pt ^ mt)) * C::TS + slot;
           const uint4 kr = lds128(Ks + row * C::D + L * C::EPL);
-          const float kf[8] = {bf16lo_to_f32(kr.x), bf16hi_to_f32(kr.x), bf16lo_to_f32(kr.y),
-                               bf16hi_to_f32(kr.y), bf16lo_to_f32(kr.z), bf16hi_to_f32(kr.z),
-                               bf16lo_to_f32(kr.w), bf16hi_to_f32(kr.w)};
+          const float2 k2[4] = {make_float2(bf16lo_to_f32(kr.x), bf16hi_to_f32(kr.x)),
+                                make_float2(bf16lo_to_f32(kr.y), bf16hi_to_f32(kr.y)),
+                                make_float2(bf16lo_to_f32(kr.z), bf16hi_to_f32(kr.z)),
+                                make_float2(bf16lo_to_f32(kr.w), bf16hi_to_f32(kr.w))};
 #pragma unroll
           for (int ph = 0; ph < GH; ++ph) {
-            float a0 = qr[ph][0] * kf[0];
-            float a1 = qr[ph][1] * kf[1];
-            a0 = fmaf(qr[ph][2], kf[2], a0);
-            a1 = fmaf(qr[ph][3], kf[3], a1);
-            a0 = fmaf(qr[ph][4], kf[4], a0);
-            a1 = fmaf(qr[ph][5], kf[5], a1);
-            a0 = fmaf(qr[ph][6], kf[6], a0);
-            a1 = fmaf(qr[ph][7], kf[7], a1);
-            sp[ph * C::NB + pt] = a0 + a1;
+            float2 a = __fmul2_rn(qr[ph][0], k2[0]);
+            a = __ffma2_rn(qr[ph][1], k2[1], a);
+            a = __ffma2_rn(qr[ph][2], k2[2], a);
+            a = __ffma2_rn(qr[ph][3], k2[3], a);
+            sp[ph * C::NB + pt] = a.x + a.y;
           }
         }
         // ---- reduce-scatter over the 16 lanes of the token group
@@ -281,50 +282,61 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
         m_run = m_new;
         if (p_writer) {
 #pragma unroll
-          for (int c = 0; c < C::C; ++c) P_slot[(c ^ mt) * GH + mh] = sp[c];
+          for (int c = 0; c < C::C; ++c) P_slot[(c ^ mt) * GH + mh] = make_float2(sp[c], sp[c]);
         }
         if (head_writer) A_slot[mh] = alpha;
         __syncwarp();
         // ---- rescale accumulators when some head's max moved
         float al[GH];
+        if constexpr (GH >= 4) {
 #pragma unroll
-        for (int h = 0; h < GH; ++h) al[h] = A_slot[h];
+          for (int h4 = 0; h4 < GH / 4; ++h4) {
+            const float4 a4 = lds128f(A_slot + h4 * 4);
+            al[h4 * 4 + 0] = a4.x;
+            al[h4 * 4 + 1] = a4.y;
+            al[h4 * 4 + 2] = a4.z;
+            al[h4 * 4 + 3] = a4.w;
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < GH; ++h) al[h] = A_slot[h];
+        }
         bool moved = false;
 #pragma unroll
         for (int h = 0; h < GH; ++h) moved |= (al[h] != 1.f);
         if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
-          for (int h = 0; h < GH; ++h)
+          for (int h = 0; h < GH; ++h) {
+            const float2 a2 = make_float2(al[h], al[h]);
 #pragma unroll
-            for (int e = 0; e < C::EPL; ++e) acc[h][e] *= al[h];
+            for (int e = 0; e < C::EPL / 2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], a2);
+          }
         }
         // ---- PV
 #pragma unroll
         for (int tk = 0; tk < C::NB; ++tk) {
-          float pr[GH];
-          if constexpr (GH >= 4) {
+          float2 pr[GH];
+          if constexpr (GH >= 2) {
 #pragma unroll
-            for (int h4 = 0; h4 < GH / 4; ++h4) {
-              const float4 p4 = lds128f(P_slot + tk * GH + h4 * 4);
-              pr[h4 * 4 + 0] = p4.x;
-              pr[h4 * 4 + 1] = p4.y;
-              pr[h4 * 4 + 2] = p4.z;
-              pr[h4 * 4 + 3] = p4.w;
+            for (int h2 = 0; h2 < GH / 2; ++h2) {
+              const float4 p4 = lds128f(P_slot + tk * GH + h2 * 2);
+              pr[h2 * 2 + 0] = make_float2(p4.x, p4.y);
+              pr[h2 * 2 + 1] = make_float2(p4.z, p4.w);
             }
           } else {
-#pragma unroll
-            for (int h = 0; h < GH; ++h) pr[h] = P_slot[tk * GH + h];
+            pr[0] = P_slot[tk * GH];
           }
           const int row = (bi * C::NB + tk) * C::TS + slot;
           uint4 vr = lds128(Vs + row * C::D + L * C::EPL);
           if (!full_tile && row >= nvalid) vr = make_uint4(0u, 0u, 0u, 0u);
-          const float vf[8] = {bf16lo_to_f32(vr.x), bf16hi_to_f32(vr.x), bf16lo_to_f32(vr.y),
-                               bf16hi_to_f32(vr.y), bf16lo_to_f32(vr.z), bf16hi_to_f32(vr.z),
-                               bf16lo_to_f32(vr.w), bf16hi_to_f32(vr.w)};
+          const float2 v2[4] = {make_float2(bf16lo_to_f32(vr.x), bf16hi_to_f32(vr.x)),
+                                make_float2(bf16lo_to_f32(vr.y), bf16hi_to_f32(vr.y)),
+                                make_float2(bf16lo_to_f32(vr.z), bf16hi_to_f32(vr.z)),
+                                make_float2(bf16lo_to_f32(vr.w), bf16hi_to_f32(vr.w))};
 #pragma unroll
           for (int h = 0; h < GH; ++h)
 #pragma unroll
-            for (int e = 0; e < C::EPL; ++e) acc[h][e] = fmaf(pr[h], vf[e], acc[h][e]);
+            for (int e = 0; e < C::EPL / 2; ++e) acc[h][e] = __ffma2_rn(pr[h], v2[e], acc[h][e]);
         }
         __syncwarp();
       }
@@ -368,8 +380,8 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
 #pragma unroll
     for (int h = 0; h < GH; ++h) {
       float* dst = ACC_s + (sidx * GH + h) * C::D + L * C::EPL;
-      *reinterpret_cast<float4*>(dst) = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[h][0].x, acc[h][0].y, acc[h][1].x, acc[h][1].y);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[h][2].x, acc[h][2].y, acc[h][3].x, acc[h][3].y);
     }
   }
   __syncthreads();
