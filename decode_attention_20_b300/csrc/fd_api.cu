@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
@@ -140,21 +141,25 @@ fd_status get_encoder() {
   return FD_OK;
 }
 
-// 4-D bf16 map over a [B, L, Hkv, D] cache with box {D, 1, tile, 1}.
+// 4-D bf16 map over a [B, L, Hkv, D] cache with box {box_d, 1, tile, 1};
+// box_d = 64 uses the 128-byte swizzle (one swizzle row per token), box_d =
+// D leaves the tile unswizzled.
 bool make_kv_map(CUtensorMap* map, const void* base, int64_t B, int64_t L, int64_t Hkv,
-                 int64_t D, int64_t sb, int64_t sl, int64_t sh, int tile) {
+                 int64_t D, int64_t sb, int64_t sl, int64_t sh, int tile, int box_d = 0) {
+  if (box_d == 0) box_d = (int)D;
   const int64_t esz = 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)L, (cuuint64_t)B};
   // A unit batch extent never steps along its stride; give it a legal one.
   const int64_t sb_eff = (B == 1) ? sl * L : sb;
   cuuint64_t strides[3] = {(cuuint64_t)(sh * esz), (cuuint64_t)(sl * esz),
                            (cuuint64_t)(sb_eff * esz)};
-  cuuint32_t box[4] = {(cuuint32_t)D, 1u, (cuuint32_t)tile, 1u};
+  cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)tile, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  const CUtensorMapSwizzle swz =
+      (box_d * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -260,6 +265,20 @@ bool tma_ok(const DecodeDesc& d, const void* kd, const void* vd, const int64_t (
   return true;
 }
 
+// Which split kernel variant to use.  Tuning and test knob, read on every
+// call: FD_SPLIT_VARIANT = "cuda" forces the CUDA-core kernel, "mma0" /
+// "mma1" / "mma2" pick a tensor-core tiling; unset = "mma0".
+int split_variant() {
+  const char* e = getenv("FD_SPLIT_VARIANT");
+  if (e == nullptr || e[0] == 0) return 0;
+  if (!strcmp(e, "cuda")) return -1;
+  if (!strcmp(e, "mma1")) return 1;
+  if (!strcmp(e, "mma2")) return 2;
+  return 0;
+}
+
+bool mma_group_ok(int64_t G) { return G == 4 || G == 8 || G == 16 || G == 32 || G == 64; }
+
 int32_t choose_splits_host(int64_t batch, int64_t kv_heads, int64_t max_len, int32_t num_sms) {
   const int64_t units = batch * kv_heads;
   if (batch <= 0 || kv_heads <= 0 || max_len <= 0 || num_sms <= 0) return 1;
@@ -315,7 +334,29 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   cudaError_t e = cudaSuccess;
   const int64_t kv_batch = kv_broadcast ? 1 : d.B;
   const int64_t strides[6] = {p.k_sl, p.k_sh, p.v_sl, p.v_sh, p.k_sb, p.v_sb};
-  if (tma_ok(d, k->data, v->data, strides, kv_batch)) {
+  const int variant = split_variant();
+  if (variant >= 0 && d.q_dt == FD_BF16 && mma_group_ok(d.G) &&
+      d.Lcap >= mma_tile_tokens(variant) && tma_ok(d, k->data, v->data, strides, kv_batch)) {
+    fd_status gs = get_encoder();
+    if (gs) return gs;
+    CUtensorMap tmK, tmV;
+    const int tile = mma_tile_tokens(variant);
+    const bool okk = make_kv_map(&tmK, k->data, kv_batch, d.Lcap, d.Hkv, d.D, p.k_sb, p.k_sl,
+                                 p.k_sh, tile, 64);
+    const bool okv = make_kv_map(&tmV, v->data, kv_batch, d.Lcap, d.Hkv, d.D, p.v_sb, p.v_sl,
+                                 p.v_sh, tile, 64);
+    if (okk && okv) {
+      const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
+      e = launch_split_mma(p, tmK, tmV, (int)d.G, variant, st, &launched);
+      prof_end(FD_KERNEL_SPLIT, st, prof && launched, rec);
+      if (prof && !launched) {
+        std::lock_guard<std::mutex> lock(g_prof_mu);
+        g_prof.pool.push_back(rec);
+      }
+      if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
+    }
+  }
+  if (!launched && tma_ok(d, k->data, v->data, strides, kv_batch)) {
     fd_status gs = get_encoder();
     if (gs) return gs;
     CUtensorMap tmK, tmV;

@@ -53,6 +53,9 @@ struct CombineParams {
 cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
                              const CUtensorMap& tmV, int D, int G, cudaStream_t st,
                              bool* launched);
+cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             int G, int variant, cudaStream_t st, bool* launched);
+int mma_tile_tokens(int variant);
 cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16,
                                  cudaStream_t st);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);

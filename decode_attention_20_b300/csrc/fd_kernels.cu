@@ -7,6 +7,7 @@
 #include "fd_combine.cuh"
 #include "fd_internal.h"
 #include "fd_split.cuh"
+#include "fd_split_mma.cuh"
 
 namespace fd {
 
@@ -60,6 +61,60 @@ cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
     case 64: return launch_tma_variant<8, 8>(p, tmK, tmV, st);
     default: *launched = false; return cudaSuccess;
   }
+}
+
+template <int NT, int WN, int W, int T, int NSTAGE>
+static cudaError_t launch_mma_variant(const SplitParams& p, const CUtensorMap& tmK,
+                                      const CUtensorMap& tmV, cudaStream_t st) {
+  using C = MmaCfg<NT, WN, W, T, NSTAGE>;
+  auto kern = split_mma_kernel<NT, WN, W, T, NSTAGE>;
+  static unsigned long long attr_set = 0ull;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set |= bit;
+  }
+  dim3 grid(p.ns, p.Hkv, p.B);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
+  return cudaGetLastError();
+}
+
+int mma_tile_tokens(int variant) { return variant == 1 ? 128 : 64; }
+
+cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             int G, int variant, cudaStream_t st, bool* launched) {
+  *launched = true;
+  if (variant == 1) {            // 8 warps, 128-token tiles, 3 stages
+    switch (G) {
+      case 4: case 8: return launch_mma_variant<1, 1, 8, 128, 3>(p, tmK, tmV, st);
+      case 16: return launch_mma_variant<2, 1, 8, 128, 3>(p, tmK, tmV, st);
+      case 32: return launch_mma_variant<4, 2, 8, 128, 3>(p, tmK, tmV, st);
+      case 64: return launch_mma_variant<8, 4, 8, 128, 3>(p, tmK, tmV, st);
+      default: break;
+    }
+  } else if (variant == 2) {     // 4 warps, 64-token tiles, 3 stages (two CTAs per SM)
+    switch (G) {
+      case 4: case 8: return launch_mma_variant<1, 1, 4, 64, 3>(p, tmK, tmV, st);
+      case 16: return launch_mma_variant<2, 1, 4, 64, 3>(p, tmK, tmV, st);
+      case 32: return launch_mma_variant<4, 2, 4, 64, 3>(p, tmK, tmV, st);
+      case 64: return launch_mma_variant<8, 4, 4, 64, 3>(p, tmK, tmV, st);
+      default: break;
+    }
+  } else {                       // 4 warps, 64-token tiles, 6 stages
+    switch (G) {
+      case 4: case 8: return launch_mma_variant<1, 1, 4, 64, 6>(p, tmK, tmV, st);
+      case 16: return launch_mma_variant<2, 1, 4, 64, 6>(p, tmK, tmV, st);
+      case 32: return launch_mma_variant<4, 2, 4, 64, 6>(p, tmK, tmV, st);
+      case 64: return launch_mma_variant<8, 4, 4, 64, 6>(p, tmK, tmV, st);
+      default: break;
+    }
+  }
+  *launched = false;
+  return cudaSuccess;
 }
 
 cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaStream_t st) {

@@ -1,0 +1,400 @@
+// Split-KV partial kernel for grouped-query attention on the tensor cores.
+//
+// Same contract as split_tma_kernel (fd_split.cuh): one CTA per (split i,
+// kv head g, sequence b) writes the normalised partial output and the
+// natural-log log-sum-exp of its token range for every query head of the
+// group.  Source: Flash-Decoding page ("What is Flash-Decoding and when does
+// it speed up LLMs?"), section "Why decoding needs different scheduling";
+// online softmax after "How does Flash Attention reduce memory traffic during
+// local inference?", section on online softmax.
+//
+// Why tensor cores here: with G query heads sharing every K/V element, the
+// per-token work is a real contraction (G x D scores, G x D accumulations).
+// On CUDA cores at G = 8 the FMA pipe alone needs about as long as HBM takes
+// to deliver the cache (profiled: ~45% FMA-pipe activity over an 83 us
+// launch at 64K tokens), so the kernel cannot reach the memory roofline.
+// Warp-level mma.sync m16n8k16 (bf16 in, fp32 accumulate) does the same
+// arithmetic in ~1/16 of the instructions, leaving the kernel HBM-bound.
+//
+// Layout of the work (per warp, per 16-token block, per 8-head n-tile):
+//   S^T[16 tok x 8 heads]  = K[16 x 128] . Q^T[128 x 8]    8 mma (k = 16 dims)
+//   online softmax on the accumulator fragment (each lane: 2 tokens x 2
+//   heads; per-head block max over the 8 lanes sharing lane % 4)
+//   P^T -> bf16 hi + lo, transposed in registers (movmatrix) into B operands
+//   O^T[128 dims x 8 heads] += V^T[128 x 16 tok] . P^T[16 tok x 8 heads]
+//                                                   2 x 8 mma (k = 16 tokens)
+// K and V tiles arrive by TMA with the 128-byte swizzle (two 64-column boxes
+// per tile), so every ldmatrix is bank-conflict free.  The probabilities
+// enter the PV product as a hi + lo pair of bf16 values (two MMAs), which
+// keeps ~16 mantissa bits; the running sum l stays in fp32.
+#pragma once
+
+#include "fd_split.cuh"
+
+namespace fd {
+
+// --------------------------------------------------------- warp MMA helpers
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + C (fp32)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// (lo, hi) floats -> bf16x2 with round-to-nearest-even; lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Byte offset of (row, 16-byte chunk) inside a 128-byte-swizzled box whose
+// rows are 128 bytes (the TMA SWIZZLE_128B pattern on a 1024-byte aligned
+// base: chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz128(int row, int chunk) {
+  return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// ------------------------------------------------------------------ config
+
+template <int NT_, int WN_, int W_, int T_, int NSTAGE_>
+struct MmaCfg {
+  static constexpr int NT = NT_;               // 8-head n-tiles per kv head (ceil(G/8))
+  static constexpr int WN = WN_;               // warps sharing a token block (split n-tiles)
+  static constexpr int NPW = NT / WN;          // n-tiles per warp
+  static constexpr int W = W_;                 // warps per CTA
+  static constexpr int WT = W / WN;            // token groups
+  static constexpr int T = T_;                 // tokens per tile
+  static constexpr int NSTAGE = NSTAGE_;
+  static constexpr int D = 128;
+  static constexpr int THREADS = W * 32;
+  static constexpr int BLK = T / 16;           // 16-token blocks per tile
+  static constexpr int BPW = BLK / WT;         // blocks per warp per tile
+  static constexpr int HALF_BYTES = T * 128;   // [T][64] bf16, swizzled
+  static constexpr int STAGE_BYTES = 4 * HALF_BYTES;   // K lo, K hi, V lo, V hi
+  static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
+  static constexpr int GP = NT * 8;            // padded heads
+  static constexpr int SMEM_BYTES = 1024 + RING_BYTES + 2 * NSTAGE * 8 + 16;
+  static_assert(NT % WN == 0, "n-tiles split evenly over warps");
+  static_assert(W % WN == 0 && BLK % WT == 0 && BPW >= 1, "blocks split evenly over warps");
+  static_assert(WT * GP * (D + 2) * 4 <= RING_BYTES, "epilogue fits the ring");
+  static_assert(HALF_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
+};
+
+template <int NT, int WN, int W, int T, int NSTAGE>
+__global__ void __launch_bounds__(W * 32, 1)
+    split_mma_kernel(const __grid_constant__ SplitParams p,
+                     const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV) {
+  using C = MmaCfg<NT, WN, W, T, NSTAGE>;
+  constexpr int NPW = C::NPW;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::RING_BYTES);
+  uint64_t* empty_bar = full_bar + C::NSTAGE;
+  int* abort_s = reinterpret_cast<int*>(empty_bar + C::NSTAGE);
+
+  const int split = blockIdx.x;
+  const int g = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wn = warp % WN;                    // n-tile group
+  const int wt = warp / WN;                    // token group
+
+  const int len = resolve_len(p.seqlens, b, p.Lcap);
+  int begin, end;
+  split_range(len, p.ns, split, begin, end);
+  const int ntiles = (end - begin + C::T - 1) / C::T;
+  const int kvb = p.kv_batch_broadcast ? 0 : b;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], W);
+    }
+    *abort_s = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  uint64_t policy = 0;
+  int issued = 0;
+  auto issue = [&](int t) {
+    const int s = t % C::NSTAGE;
+    unsigned char* stage = smem + s * C::STAGE_BYTES;
+    mbar_arrive_expect_tx(&full_bar[s], C::STAGE_BYTES);
+    const int tok = begin + t * C::T;
+    tma_load_4d(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
+    tma_load_4d(stage + C::HALF_BYTES, &tmK, &full_bar[s], 64, g, tok, kvb, policy);
+    tma_load_4d(stage + 2 * C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
+    tma_load_4d(stage + 3 * C::HALF_BYTES, &tmV, &full_bar[s], 64, g, tok, kvb, policy);
+  };
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    policy = l2_policy_evict_first();
+    for (int t = 0; t < C::NSTAGE && t < ntiles; ++t) {
+      issue(t);
+      ++issued;
+    }
+  }
+
+  // ---- query fragments (B operand of S^T = K . Q^T): B[k = dim][n = head]
+  // lane holds dims 2(lane%4)+{0,1} and +8 of head (lane/4) of each n-tile.
+  const int G = p.G;
+  uint32_t qf[NPW][8][2];
+#pragma unroll
+  for (int j = 0; j < NPW; ++j) {
+    const int hl = (wn * NPW + j) * 8 + (lane >> 2);          // head within the group
+    const bool real = hl < G;
+    const int h = g * G + (real ? hl : 0);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int d0 = ks * 16 + 2 * (lane & 3);
+      uint32_t lo = 0u, hi = 0u;
+      if (real) {
+        const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) + b * p.q_sb + h * p.q_sh;
+        lo = uint32_t(qp[d0]) | (uint32_t(qp[d0 + 1]) << 16);
+        hi = uint32_t(qp[d0 + 8]) | (uint32_t(qp[d0 + 9]) << 16);
+      }
+      qf[j][ks][0] = lo;
+      qf[j][ks][1] = hi;
+    }
+  }
+
+  float acc[NPW][8][4];
+  float m_run[NPW][2], l_run[NPW][2];
+#pragma unroll
+  for (int j = 0; j < NPW; ++j) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][mt][e] = 0.f;
+    m_run[j][0] = m_run[j][1] = kNegInf;
+    l_run[j][0] = l_run[j][1] = 0.f;
+  }
+  const float sl2 = p.scale_log2;
+  const int r8 = lane & 7;
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % C::NSTAGE;
+    if (!mbar_wait_or_abort(&full_bar[s], (t / C::NSTAGE) & 1, abort_s)) break;
+    const uint32_t kbase = smem_u32(smem + s * C::STAGE_BYTES);
+    const uint32_t vbase = kbase + 2 * C::HALF_BYTES;
+    const int nvalid = min(C::T, end - (begin + t * C::T));
+#pragma unroll 1
+    for (int bb = 0; bb < C::BPW; ++bb) {
+      const int row0 = (bb * C::WT + wt) * 16;       // first token row of this block
+      // ---- S^T = K . Q^T
+      float sacc[NPW][4];
+#pragma unroll
+      for (int j = 0; j < NPW; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
+      {
+        const int arow = row0 + r8 + ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const int col = ks * 16 + (lane >> 4) * 8;           // 0..127
+          const uint32_t addr =
+              kbase + (col >> 6) * C::HALF_BYTES + swz128(arow, (col & 63) >> 3);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(addr, a0, a1, a2, a3);
+#pragma unroll
+          for (int j = 0; j < NPW; ++j) mma_bf16_16816(sacc[j], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
+        }
+      }
+      // ---- online softmax; lane holds tokens tA = lane/4, tB = tA + 8 and
+      // heads hA = 2(lane%4), hB = hA + 1 of each n-tile
+      const int tokA = row0 + (lane >> 2);
+      const bool vA = tokA < nvalid;
+      const bool vB = tokA + 8 < nvalid;
+      uint32_t pb[NPW][2], pbl[NPW][2];
+      bool moved = false;
+      float alpha[NPW][2];
+#pragma unroll
+      for (int j = 0; j < NPW; ++j) {
+        float sA0 = vA ? sacc[j][0] * sl2 : kNegInf;   // (tA, hA)
+        float sA1 = vA ? sacc[j][1] * sl2 : kNegInf;   // (tA, hB)
+        float sB0 = vB ? sacc[j][2] * sl2 : kNegInf;   // (tB, hA)
+        float sB1 = vB ? sacc[j][3] * sl2 : kNegInf;   // (tB, hB)
+        float mx0 = fmaxf(sA0, sB0), mx1 = fmaxf(sA1, sB1);
+#pragma unroll
+        for (int o = 4; o <= 16; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        // Lazy rescaling (threshold 8 in base 2): probabilities stay <= 256.
+        const float mn0 = (mx0 > m_run[j][0] + 8.f) ? mx0 : m_run[j][0];
+        const float mn1 = (mx1 > m_run[j][1] + 8.f) ? mx1 : m_run[j][1];
+        alpha[j][0] = (mn0 == m_run[j][0]) ? 1.f : fast_exp2(m_run[j][0] - mn0);
+        alpha[j][1] = (mn1 == m_run[j][1]) ? 1.f : fast_exp2(m_run[j][1] - mn1);
+        moved |= (alpha[j][0] != 1.f) | (alpha[j][1] != 1.f);
+        m_run[j][0] = mn0;
+        m_run[j][1] = mn1;
+        const float pA0 = (mn0 == kNegInf) ? 0.f : fast_exp2(sA0 - mn0);
+        const float pB0 = (mn0 == kNegInf) ? 0.f : fast_exp2(sB0 - mn0);
+        const float pA1 = (mn1 == kNegInf) ? 0.f : fast_exp2(sA1 - mn1);
+        const float pB1 = (mn1 == kNegInf) ? 0.f : fast_exp2(sB1 - mn1);
+        // Probabilities as hi + lo bf16 pairs (hi = RNE(p), lo = RNE(p - hi)):
+        // two PV products carry ~16 mantissa bits, so the bf16 operand adds
+        // no visible error; the running sum keeps the fp32 values.
+        const uint32_t XA = pack_bf16x2(pA0, pA1);      // token tA, heads hA hB
+        const uint32_t XB = pack_bf16x2(pB0, pB1);      // token tB
+        const uint32_t XAl = pack_bf16x2(pA0 - __uint_as_float(XA << 16),
+                                         pA1 - __uint_as_float(XA & 0xffff0000u));
+        const uint32_t XBl = pack_bf16x2(pB0 - __uint_as_float(XB << 16),
+                                         pB1 - __uint_as_float(XB & 0xffff0000u));
+        l_run[j][0] = l_run[j][0] * alpha[j][0] + (pA0 + pB0);
+        l_run[j][1] = l_run[j][1] * alpha[j][1] + (pA1 + pB1);
+        pb[j][0] = movmatrix_trans(XA);                 // B[k = tokens 0-7][n = head]
+        pb[j][1] = movmatrix_trans(XB);                 // B[k = tokens 8-15][n = head]
+        pbl[j][0] = movmatrix_trans(XAl);
+        pbl[j][1] = movmatrix_trans(XBl);
+      }
+      if (__any_sync(0xffffffffu, moved)) {
+#pragma unroll
+        for (int j = 0; j < NPW; ++j)
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            acc[j][mt][0] *= alpha[j][0];
+            acc[j][mt][1] *= alpha[j][1];
+            acc[j][mt][2] *= alpha[j][0];
+            acc[j][mt][3] *= alpha[j][1];
+          }
+      }
+      // ---- O^T += V^T . P^T   (A = V^T via transposing ldmatrix)
+      {
+        // In the last, partial tile, rows past the split may hold anything
+        // (even NaN padding): clear this lane's V elements of those tokens
+        // (low half = token 2(lane%4), high half = the next token), so
+        // zero-probability rows contribute exactly zero.
+        uint32_t keep01 = 0xffffffffu, keep23 = 0xffffffffu;
+        if (nvalid < C::T) {
+          const int tk = row0 + 2 * (lane & 3);
+          keep01 = (tk < nvalid ? 0x0000ffffu : 0u) | (tk + 1 < nvalid ? 0xffff0000u : 0u);
+          keep23 = (tk + 8 < nvalid ? 0x0000ffffu : 0u) | (tk + 9 < nvalid ? 0xffff0000u : 0u);
+        }
+        const int vrow = row0 + r8 + (lane >> 4) * 8;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          const int col = mt * 16 + ((lane >> 3) & 1) * 8;
+          const uint32_t addr =
+              vbase + (col >> 6) * C::HALF_BYTES + swz128(vrow, (col & 63) >> 3);
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(addr, a0, a1, a2, a3);
+          a0 &= keep01;
+          a1 &= keep01;
+          a2 &= keep23;
+          a3 &= keep23;
+#pragma unroll
+          for (int j = 0; j < NPW; ++j) {
+            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pbl[j][0], pbl[j][1]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[s]);
+    if (threadIdx.x == 0 && t >= 1 && issued < ntiles) {
+      const int tp = t - 1;
+      if (mbar_wait_or_abort(&empty_bar[tp % C::NSTAGE], (tp / C::NSTAGE) & 1, abort_s)) {
+        issue(issued);
+        ++issued;
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    const int first = issued > C::NSTAGE ? issued - C::NSTAGE : 0;
+    for (int t = first; t < issued; ++t)
+      mbar_wait_bounded(&full_bar[t % C::NSTAGE], (t / C::NSTAGE) & 1);
+  }
+
+  pdl_launch_dependents();
+  __syncthreads();
+
+  // ------------------------------------------------------------ epilogue
+  // Sum l over the 8 lanes that share each head, then merge the token
+  // groups' (m, l, acc) through shared memory (the ring is free now).
+  float* ML_s = reinterpret_cast<float*>(smem);              // [WT][GP][2]
+  float* ACC_s = ML_s + C::WT * C::GP * 2;                   // [WT][GP][D]
+#pragma unroll
+  for (int j = 0; j < NPW; ++j) {
+#pragma unroll
+    for (int o = 4; o <= 16; o <<= 1) {
+      l_run[j][0] += __shfl_xor_sync(0xffffffffu, l_run[j][0], o);
+      l_run[j][1] += __shfl_xor_sync(0xffffffffu, l_run[j][1], o);
+    }
+    const int hbase = (wn * NPW + j) * 8;
+    if (lane < 4) {
+      const int h0 = hbase + 2 * lane;
+      ML_s[(wt * C::GP + h0) * 2 + 0] = m_run[j][0];
+      ML_s[(wt * C::GP + h0) * 2 + 1] = l_run[j][0];
+      ML_s[(wt * C::GP + h0 + 1) * 2 + 0] = m_run[j][1];
+      ML_s[(wt * C::GP + h0 + 1) * 2 + 1] = l_run[j][1];
+    }
+    const int hA = hbase + 2 * (lane & 3);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      const int d = mt * 16 + (lane >> 2);
+      ACC_s[(wt * C::GP + hA) * C::D + d] = acc[j][mt][0];
+      ACC_s[(wt * C::GP + hA + 1) * C::D + d] = acc[j][mt][1];
+      ACC_s[(wt * C::GP + hA) * C::D + d + 8] = acc[j][mt][2];
+      ACC_s[(wt * C::GP + hA + 1) * C::D + d + 8] = acc[j][mt][3];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * C::D; idx += C::THREADS) {
+    const int h = idx / C::D;
+    const int d = idx - h * C::D;
+    float M = kNegInf;
+#pragma unroll
+    for (int w = 0; w < C::WT; ++w) M = fmaxf(M, ML_s[(w * C::GP + h) * 2]);
+    float lt = 0.f, o = 0.f;
+    if (M != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < C::WT; ++w) {
+        const float ms = ML_s[(w * C::GP + h) * 2];
+        const float f = (ms == kNegInf) ? 0.f : fast_exp2(ms - M);
+        lt += f * ML_s[(w * C::GP + h) * 2 + 1];
+        o += f * ACC_s[(w * C::GP + h) * C::D + d];
+      }
+    }
+    const int hq = g * G + h;
+    p.o[b * p.o_sb + hq * p.o_sh + split * p.o_ss + d] = lt > 0.f ? o / lt : 0.f;
+    if (d == 0 && p.lse != nullptr)
+      p.lse[b * p.l_sb + hq * p.l_sh + split * p.l_ss] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
+  }
+}
+
+}  // namespace fd

@@ -17,6 +17,15 @@ from _convert import assert_parity, to_f64
 
 pytestmark = pytest.mark.gpu
 
+VARIANTS = ["mma0", "mma1", "mma2", "cuda"]
+
+
+@pytest.fixture(params=VARIANTS)
+def variant(request, monkeypatch):
+    """Split-kernel variant (tensor-core tilings or the CUDA-core kernel)."""
+    monkeypatch.setenv("FD_SPLIT_VARIANT", request.param)
+    return request.param
+
 
 def _lens_np(case):
     return None if case.seqlens is None else case.seqlens.numpy()
@@ -48,15 +57,15 @@ def test_flash_decoding_b1_lengths(cuda_device, L):
 
 
 @pytest.mark.parametrize("ns", [1, 2, 5, 16, 37, 64, 128])
-def test_flash_decoding_b1_split_sweep(cuda_device, ns):
+def test_flash_decoding_b1_split_sweep(cuda_device, variant, ns):
     _check(inputs.flash_decoding_b1(8192, seed=3), ns, f"L8192 ns={ns}")
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("ns", [1, 3])
-def test_group_sizes_tma_path(cuda_device, G, ns):
+def test_group_sizes_tma_path(cuda_device, variant, G, ns):
     case = inputs.decode_case(2, 2 * G, 2, 128, 300, seed=G, seqlens=[300, 77])
-    _check(case, ns, f"G={G} ns={ns}")
+    _check(case, ns, f"{variant} G={G} ns={ns}")
 
 
 @pytest.mark.parametrize("dtype,D,G,Lcap", [
@@ -77,18 +86,18 @@ def test_q_fp32_with_bf16_cache(cuda_device):
     _check(case, 3)
 
 
-def test_seqlens_edges(cuda_device):
+def test_seqlens_edges(cuda_device, variant):
     case = inputs.decode_case(4, 16, 2, 128, 200, seed=11, seqlens=[0, 1, 200, 65])
     for ns in [1, 2, 7]:
         _check(case, ns, f"edges ns={ns}")
 
 
-def test_many_empty_splits(cuda_device):
+def test_many_empty_splits(cuda_device, variant):
     case = inputs.decode_case(1, 8, 1, 128, 512, seed=12)
     _check(case, 256, "ns=256 over 512 tokens")
 
 
-def test_partials_match_oracle_per_split(cuda_device):
+def test_partials_match_oracle_per_split(cuda_device, variant):
     """Each split's partial (O_i, lse_i) equals exact attention over exactly
     the oracle's [begin_i, end_i): pins the partition bounds on the device."""
     for case, nss in [
@@ -105,7 +114,7 @@ def test_partials_match_oracle_per_split(cuda_device):
             assert_parity(to_f64(po), to_f64(pl), Or, Lr, case.k.dtype, f"partials ns={ns}")
 
 
-def test_strided_cache_layout(cuda_device):
+def test_strided_cache_layout(cuda_device, variant):
     """Cache stored head-major [B, Hkv, L, D] and passed as a [B, L, Hkv, D]
     view: the tensor maps take the strides as given."""
     case = inputs.decode_case(2, 16, 2, 128, 700, seed=15, seqlens=[700, 123])
@@ -212,3 +221,21 @@ def test_kernel_timing_hooks(cuda_device):
     fd.profile_enable(False)
     assert n_split == 3 and n_comb == 3
     assert ms_split > 0 and ms_comb > 0
+
+
+def test_nan_padding_past_the_lengths_is_ignored(cuda_device, variant):
+    """Cache rows at or past each sequence's length may hold anything, NaN
+    included: they must not reach the output."""
+    case = inputs.decode_case(2, 16, 2, 128, 400, seed=22, seqlens=[333, 70])
+    k = case.k.clone()
+    v = case.v.clone()
+    k[0, 333:] = float("nan")
+    v[0, 333:] = float("nan")
+    k[1, 70:] = float("inf")
+    v[1, 70:] = float("nan")
+    for ns in [1, 3]:
+        O, L = fd.decode_attention(case.q.cuda(), k.cuda(), v.cuda(), case.seqlens.cuda(), ns,
+                                   case.scale)
+        O_ref, L_ref = oracle.decode_attention_ref(to_f64(case.q), to_f64(case.k), to_f64(case.v),
+                                                   _lens_np(case), case.scale)
+        assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16, f"{variant} nan pad ns={ns}")
