@@ -403,6 +403,59 @@ int64_t workspace_bytes(int64_t B, int64_t Hq, int64_t D, int64_t ns) {
 
 }  // namespace
 
+// ------------------------------------------------------- allocation-free scratch
+//
+// For callers that must not allocate device memory while they run (see
+// fd_decode_attention_noalloc in fd_decode.h): the partial-result workspace
+// of the split stage lives in this fixed array instead of the stream-ordered
+// pool.  Every GPU that loads the library holds it until the process exits.
+// Host code must never pass the array's name to a kernel (on the host it is
+// only a stand-in for the symbol); the device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FD_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+struct NoAllocDevice {
+  bool ok = false;
+  int sms = 0;
+  void* scratch = nullptr;   // device address of g_noalloc_scratch on this device
+};
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_dev[64];
+
+// One-time set-up for the current device: architecture check, SM count and
+// the scratch array's device address.  Allocates nothing.
+fd_status noalloc_setup(NoAllocDevice** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(FD_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ok) {
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(cc major)");
+    e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(cc minor)");
+    if (!(major == 10 && minor == 3))
+      return fail(FD_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a only", dev,
+                  major, minor);
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    d.scratch = ptr;
+    d.ok = true;
+  }
+  *out = &d;
+  return FD_OK;
+}
+
+}  // namespace
+
 // ====================================================================== C ABI
 
 extern "C" {
@@ -506,6 +559,65 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
   if (st) return st;
   if (e != cudaSuccess) return cuda_fail(e, "workspace release");
   return FD_OK;
+}
+
+fd_status fd_decode_attention_noalloc(const fd_tensor* q, const fd_tensor* k_cache,
+                                      const fd_tensor* v_cache, const fd_tensor* seqlens,
+                                      int32_t num_splits, float scale, fd_tensor* out,
+                                      fd_tensor* lse, fd_stream stream) {
+  DecodeDesc d;
+  fd_status st = validate_decode(q, k_cache, v_cache, seqlens, out, lse, 3, 0, &d);
+  if (st) return st;
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
+  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  NoAllocDevice* dev = nullptr;
+  if ((st = noalloc_setup(&dev))) return st;
+  if (d.B == 0 || d.Hq == 0) return FD_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int ns = num_splits > 0 ? num_splits : choose_splits_host(d.B, d.Hkv, d.Lcap, dev->sms);
+  const int32_t* sl = seqlens ? reinterpret_cast<const int32_t*>(seqlens->data) : nullptr;
+  float* o = reinterpret_cast<float*>(out->data);
+  float* l = lse ? reinterpret_cast<float*>(lse->data) : nullptr;
+  if (ns == 1) {
+    return enqueue_split(d, q, k_cache, v_cache, sl, 1, scale, o, out->stride[0], out->stride[1],
+                         0, l, lse ? lse->stride[0] : 0, lse ? lse->stride[1] : 0, 0, false, cs);
+  }
+  const int64_t bytes = workspace_bytes(d.B, d.Hq, d.D, ns);
+  if (bytes > (int64_t)FD_NOALLOC_SCRATCH_BYTES)
+    return fail(FD_ERR_UNSUPPORTED,
+                "partial results need %lld bytes (B=%lld, Hq=%lld, D=%lld, %d splits) but the "
+                "static scratch holds %lld; use fewer splits or fd_decode_attention",
+                (long long)bytes, (long long)d.B, (long long)d.Hq, (long long)d.D, ns,
+                (long long)FD_NOALLOC_SCRATCH_BYTES);
+  // Nothing in the scratch has to start at zero: the split kernel writes
+  // every partial (O_i, lse_i) that the combine kernel then reads.
+  float* po = reinterpret_cast<float*>(dev->scratch);
+  float* pl = reinterpret_cast<float*>(reinterpret_cast<char*>(dev->scratch) +
+                                       ((d.B * d.Hq * ns * d.D * 4 + 255) / 256) * 256);
+  st = enqueue_split(d, q, k_cache, v_cache, sl, ns, scale, po, d.Hq * ns * d.D, ns * d.D, d.D,
+                     pl, d.Hq * ns, ns, 1, false, cs);
+  if (st) return st;
+  CombineParams cp = {};
+  cp.part_o = po;
+  cp.po_r1 = d.Hq * ns * d.D;
+  cp.po_r2 = ns * d.D;
+  cp.po_s = d.D;
+  cp.part_lse = pl;
+  cp.pl_r1 = d.Hq * ns;
+  cp.pl_r2 = ns;
+  cp.pl_s = 1;
+  cp.out = o;
+  cp.out_r1 = out->stride[0];
+  cp.out_r2 = out->stride[1];
+  cp.lse = l;
+  cp.lse_r1 = lse ? lse->stride[0] : 0;
+  cp.lse_r2 = lse ? lse->stride[1] : 0;
+  cp.R1 = (int)d.B;
+  cp.R2 = (int)d.Hq;
+  cp.S = ns;
+  cp.D = (int)d.D;
+  return enqueue_combine(cp, cs, true);
 }
 
 fd_status fd_decode_attention_partials(const fd_tensor* q, const fd_tensor* k_cache,

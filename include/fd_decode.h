@@ -119,6 +119,39 @@ FD_API fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cach
                               fd_tensor* lse, fd_stream stream);
 
 /*
+ * fd_decode_attention_noalloc — fd_decode_attention without any device
+ * allocation.  (The pages have no counterpart: this is a library service.)
+ *
+ * For callers that cannot allocate GPU memory while they run: code inside a
+ * region where a memory pool must not grow, a runtime that owns all device
+ * memory itself, or a deadline-bound loop that cannot risk an allocation
+ * stall.  Same arguments, results and errors as fd_decode_attention, but the
+ * partial results of the split stage go to a fixed, library-owned device
+ * array of FD_NOALLOC_SCRATCH_BYTES bytes instead of stream-ordered
+ * workspace.  That array exists on every GPU that loads the library, for the
+ * life of the process.
+ *   - Calls whose partial results would not fit (fd_workspace_bytes(B, Hq,
+ *     D, ns) > FD_NOALLOC_SCRATCH_BYTES, ns being num_splits or the
+ *     heuristic's choice) return FD_ERR_UNSUPPORTED and enqueue nothing; pass
+ *     a smaller num_splits or use fd_decode_attention.
+ *   - All calls on a device share the one array: two calls whose work
+ *     overlaps on the GPU (different streams, no ordering between them) race
+ *     and may return wrong results.  Order them on one stream or with events.
+ *   - The first call on each device looks up the array's device address
+ *     (once, with that device current); make that first call before any
+ *     stream capture.
+ *   - Nothing in the array has to start at zero; each call writes every
+ *     partial result before reading it.
+ */
+FD_API fd_status fd_decode_attention_noalloc(const fd_tensor* q, const fd_tensor* k_cache,
+                                             const fd_tensor* v_cache, const fd_tensor* seqlens,
+                                             int32_t num_splits, float scale, fd_tensor* out,
+                                             fd_tensor* lse, fd_stream stream);
+
+/* Size of the fixed scratch used by fd_decode_attention_noalloc (8 MiB). */
+#define FD_NOALLOC_SCRATCH_BYTES (8 * 1024 * 1024)
+
+/*
  * fd_decode_attention_partials — the split stage alone (diagnostics and
  * partial-level tests).  Same inputs as fd_decode_attention with an explicit
  * num_splits (1..FD_MAX_SPLITS); writes, instead of the merged result,
