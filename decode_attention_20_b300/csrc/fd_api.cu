@@ -163,6 +163,24 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t B, int64_t L, int64
   return r == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map {D, dim1, dim2} with byte strides {s1, s2} and box
+// {64, box1, box2}, 128-byte swizzle (one swizzle row per 64-element box row).
+bool make_3d_map(CUtensorMap* map, const void* base, int64_t D, int64_t n1, int64_t n2,
+                 int64_t s1_elems, int64_t s2_elems, int box1, int box2) {
+  const int64_t esz = 2;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)n1, (cuuint64_t)n2};
+  // A unit outer extent never steps along its stride; give it a legal one.
+  const int64_t s2_eff = (n2 == 1) ? s1_elems * n1 : s2_elems;
+  cuuint64_t strides[2] = {(cuuint64_t)(s1_elems * esz), (cuuint64_t)(s2_eff * esz)};
+  cuuint32_t box[3] = {64u, (cuuint32_t)box1, (cuuint32_t)box2};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ validation
 
 int64_t esize(int32_t dt) { return dt == FD_BF16 ? 2 : 4; }
@@ -279,15 +297,32 @@ int split_variant() {
 
 bool mma_group_ok(int64_t G) { return G == 4 || G == 8 || G == 16 || G == 32 || G == 64; }
 
+// Split-count heuristic: the smallest ns with the lowest makespan
+// waves(ns) * (chunk(ns) + kSplitOverheadTokens), where chunk is the
+// fd_split_bounds chunk of a max_len history and waves counts rounds of one
+// CTA per SM over batch * kv_heads * (non-empty splits) CTAs; ns is capped at
+// ceil(max_len / 256) and FD_MAX_SPLITS.
 int32_t choose_splits_host(int64_t batch, int64_t kv_heads, int64_t max_len, int32_t num_sms) {
-  const int64_t units = batch * kv_heads;
+  constexpr int64_t kMinChunk = 256;
+  constexpr int64_t kSplitOverheadTokens = 256;
   if (batch <= 0 || kv_heads <= 0 || max_len <= 0 || num_sms <= 0) return 1;
-  int64_t ns = (2 * (int64_t)num_sms) / units;
-  const int64_t cap = (max_len + 255) / 256;
-  if (ns > cap) ns = cap;
-  if (ns > kMaxSplits) ns = kMaxSplits;
-  if (ns < 1) ns = 1;
-  return (int32_t)ns;
+  const int64_t units = batch * kv_heads;
+  int64_t cap = (max_len + kMinChunk - 1) / kMinChunk;
+  if (cap > kMaxSplits) cap = kMaxSplits;
+  if (cap < 1) cap = 1;
+  int64_t best_ns = 1, best_cost = -1;
+  for (int64_t ns = 1; ns <= cap; ++ns) {
+    const int64_t per = (max_len + ns - 1) / ns;
+    const int64_t chunk = ((per + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
+    const int64_t used = (max_len + chunk - 1) / chunk;
+    const int64_t waves = (units * used + num_sms - 1) / num_sms;
+    const int64_t cost = waves * (chunk + kSplitOverheadTokens);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_ns = ns;
+    }
+  }
+  return (int32_t)best_ns;
 }
 
 // Enqueue the split stage for one cache.
@@ -393,6 +428,37 @@ fd_status enqueue_combine(const CombineParams& cp, cudaStream_t st, bool pdl) {
   prof_end(FD_KERNEL_COMBINE, st, prof, rec);
   if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
   return FD_OK;
+}
+
+// Context split count of the bifurcated tensor-core kernel: the fewest
+// splits that reach the smallest makespan (waves x tiles per split) when
+// `units` CTAs (M-tiles x kv heads) run per split on `num_sms` SMs, one CTA
+// per SM.
+int choose_ctx_splits(int64_t Lc, int64_t units, int num_sms) {
+  const int64_t tiles = (Lc + kBifTileTokens - 1) / kBifTileTokens;
+  int best_ns = 1;
+  int64_t best_cost = -1;
+  for (int ns = 1; ns <= kMaxSplits && ns <= tiles; ++ns) {
+    const int64_t per = (tiles + ns - 1) / ns;          // tiles per split
+    const int64_t used = (tiles + per - 1) / per;        // non-empty splits
+    const int64_t ctas = used * units;
+    const int64_t waves = (ctas + num_sms - 1) / num_sms;
+    const int64_t cost = waves * per;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best_ns = (int)used;
+    }
+  }
+  return best_ns;
+}
+
+// Which context path the bifurcated call takes.  Tuning and test knob, read
+// on every call: FD_BIF_CTX = "split" forces the split kernel over a
+// batch-broadcast view of the context; unset = the tensor-core kernel where
+// it applies.
+bool bif_ctx_tensor_core_allowed() {
+  const char* e = getenv("FD_BIF_CTX");
+  return !(e && !strcmp(e, "split"));
 }
 
 int64_t workspace_bytes(int64_t B, int64_t Hq, int64_t D, int64_t ns) {
@@ -739,7 +805,21 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   if (n == 0 || Hq == 0) return FD_OK;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
-  const int ns_ctx = ctx_splits > 0 ? ctx_splits : choose_splits_host(n, Hkv, Lc, info->sms);
+  // Tensor-core context path: head dim 128, group size dividing 128,
+  // 16-byte aligned bases and strides.
+  const int64_t G = Hq / Hkv;
+  const bool tc_ok = bif_ctx_tensor_core_allowed() && D == 128 && G <= 128 && 128 % G == 0 &&
+                     aligned16(q->data) && aligned16(k_ctx->data) && aligned16(v_ctx->data) &&
+                     (q->stride[1] * 2) % 16 == 0 && (q->stride[0] * 2) % 16 == 0 &&
+                     q->stride[1] > 0 && (q->stride[0] > 0 || n == 1) &&
+                     (k_ctx->stride[1] * 2) % 16 == 0 && (k_ctx->stride[0] * 2) % 16 == 0 &&
+                     (v_ctx->stride[1] * 2) % 16 == 0 && (v_ctx->stride[0] * 2) % 16 == 0 &&
+                     k_ctx->stride[1] > 0 && v_ctx->stride[1] > 0 && k_ctx->stride[0] > 0 &&
+                     v_ctx->stride[0] > 0;
+  const int64_t mtiles = (n * G + 127) / 128;
+  const int ns_ctx = ctx_splits > 0 ? ctx_splits
+                     : tc_ok ? choose_ctx_splits(Lc, mtiles * Hkv, info->sms)
+                             : choose_splits_host(n, Hkv, Lc, info->sms);
   const int ns_dec = Ld > 0 ? 1 : 0;
   const int S = ns_ctx + ns_dec;
   const int64_t bytes = workspace_bytes(n, Hq, D, S);
@@ -749,10 +829,52 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   float* po = reinterpret_cast<float*>(ws);
   float* pl = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + ((n * Hq * S * D * 4 + 255) / 256) * 256);
 
-  // Context part: every sample reads the one shared context (batch stride 0).
-  DecodeDesc dc = {n, Hq, Hkv, D, Lc, Hq / Hkv, FD_BF16, FD_BF16};
-  st = enqueue_split(dc, q, k_ctx, v_ctx, nullptr, ns_ctx, scale, po, Hq * S * D, S * D, D, pl,
-                     Hq * S, S, 1, true, cs);
+  st = FD_OK;
+  bool ctx_done = false;
+  if (tc_ok) {
+    // Context part on the tensor cores: rows (sample, head of the group).
+    if ((st = get_encoder()) == FD_OK) {
+      CUtensorMap tmQ, tmK, tmV;
+      const bool okq = make_3d_map(&tmQ, q->data, D, Hq, n, q->stride[1], q->stride[0], (int)G,
+                                   (int)(128 / G));
+      const bool okk = make_3d_map(&tmK, k_ctx->data, D, Hkv, Lc, k_ctx->stride[1],
+                                   k_ctx->stride[0], 1, kBifTileTokens);
+      const bool okv = make_3d_map(&tmV, v_ctx->data, D, Hkv, Lc, v_ctx->stride[1],
+                                   v_ctx->stride[0], 1, kBifTileTokens);
+      if (okq && okk && okv) {
+        BifCtxParams bp = {};
+        bp.n = (int)n;
+        bp.Hq = (int)Hq;
+        bp.Hkv = (int)Hkv;
+        bp.G = (int)G;
+        bp.Lc = (int)Lc;
+        bp.ns = ns_ctx;
+        bp.rows = (int)(n * G);
+        bp.scale_log2 = scale * 1.4426950408889634f;
+        bp.o = po;
+        bp.o_sb = Hq * S * D;
+        bp.o_sh = S * D;
+        bp.o_ss = D;
+        bp.lse = pl;
+        bp.l_sb = Hq * S;
+        bp.l_sh = S;
+        bp.l_ss = 1;
+        ProfRecord rec;
+        const bool prof = prof_begin(FD_KERNEL_BIF_CTX, cs, &rec);
+        e = launch_bif_ctx(bp, tmQ, tmK, tmV, (int)mtiles, cs);
+        prof_end(FD_KERNEL_BIF_CTX, cs, prof, rec);
+        if (e != cudaSuccess) st = cuda_fail(e, "bifurcated context kernel launch");
+        ctx_done = true;
+      }
+    }
+  }
+  if (st == FD_OK && !ctx_done) {
+    // Context part on the split kernel: every sample reads the one shared
+    // context through a batch-broadcast view (batch stride 0).
+    DecodeDesc dc = {n, Hq, Hkv, D, Lc, Hq / Hkv, FD_BF16, FD_BF16};
+    st = enqueue_split(dc, q, k_ctx, v_ctx, nullptr, ns_ctx, scale, po, Hq * S * D, S * D, D, pl,
+                       Hq * S, S, 1, true, cs);
+  }
   // Decode part: each sample's own tokens, one split, written after the
   // context splits.
   if (st == FD_OK && ns_dec) {

@@ -5,92 +5,113 @@
 //   LSE = ln sum_i e^(lse_i)   (evaluated as M + ln sum_i e^(lse_i - M))
 //   O   = sum_i e^(lse_i - LSE) * O_i
 // Rows whose partials are all empty (every lse_i = -inf) give O = 0 and
-// LSE = -inf.  Source: Flash-Decoding page ("What is Flash-Decoding and when
-// does it speed up LLMs?"), section "Why decoding needs different
-// scheduling": a final reduction merges the per-split results exactly.
+// LSE = -inf; an empty split's O_i is never used (its weight selects 0, so
+// whatever it holds, even NaN, does not reach the result).  Source:
+// Flash-Decoding page ("What is Flash-Decoding and when does it speed up
+// LLMs?"), section "Why decoding needs different scheduling": a final
+// reduction merges the per-split results exactly.
 //
-// One warp per row; each lane owns 4 consecutive head-dim elements (16-byte
-// loads, coalesced across the warp).  Launched with programmatic stream
-// serialisation behind the split kernel: the prologue overlaps its tail, and
-// griddepcontrol.wait orders the reads after the partial writes.
+// One CTA of 128 threads per row.  The work is a few KB per row, so the
+// kernel is latency-bound: every load of the row is independent of every
+// other one and issued up front.
+//   pass 1: threads stride over the splits for the max M and sum e^(lse-M)
+//           (block reduction through shared memory);
+//   pass 2: thread t owns 4 consecutive head-dim elements c = t % (D/4) of
+//           the split group t / (D/4) (splits s = group, group + SG, ...);
+//           each thread recomputes its splits' weights from lse directly,
+//           so its O_i loads depend on nothing but the addresses;
+//           the SG group sums are added through shared memory.
+// Launched with programmatic stream serialisation behind the split kernel:
+// the launch overlaps its tail, and griddepcontrol.wait orders the reads
+// after the partial writes.
 #pragma once
 
 #include "fd_device.cuh"
 
 namespace fd {
 
-constexpr int kCombineWarps = 4;
+constexpr int kCombineThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
-__global__ void __launch_bounds__(kCombineWarps * 32)
+__global__ void __launch_bounds__(kCombineThreads)
     lse_combine_kernel(const __grid_constant__ CombineParams p) {
   constexpr float kNegInfC = -__builtin_huge_valf();
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kCombineWarps + warp;
-  const int rows = p.R1 * p.R2;
+  __shared__ float red_s[kCombineThreads / 32];
+  __shared__ float4 acc_s[kCombineThreads];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int row = blockIdx.x;
   pdl_wait_prerequisites();
-  if (row >= rows) return;
+  if (row >= p.R1 * p.R2) return;
   const int r1 = row / p.R2;
   const int r2 = row - r1 * p.R2;
   const float* pl = p.part_lse + r1 * p.pl_r1 + r2 * p.pl_r2;
   const float* po = p.part_o + r1 * p.po_r1 + r2 * p.po_r2;
 
-  // Pass 1 (lanes over splits, all loads in parallel): M and sum e^(lse-M).
+  // ---- pass 1: M = max_i lse_i, tot = sum_i e^(lse_i - M)
   float M = kNegInfC;
-  for (int s0 = 0; s0 < p.S; s0 += 32) {
-    const int s = s0 + lane;
-    M = fmaxf(M, s < p.S ? pl[s * p.pl_s] : kNegInfC);
-  }
+  for (int s = tid; s < p.S; s += kCombineThreads) M = fmaxf(M, pl[s * p.pl_s]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red_s[warp] = M;
+  __syncthreads();
+  M = red_s[0];
+#pragma unroll
+  for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red_s[w]);
   const bool empty = (M == kNegInfC);
   float tot = 0.f;
-  if (!empty) {
-    for (int s0 = 0; s0 < p.S; s0 += 32) {
-      const int s = s0 + lane;
-      if (s < p.S) tot += fast_exp2((pl[s * p.pl_s] - M) * kLog2e);
-    }
-  }
+  if (!empty)
+    for (int s = tid; s < p.S; s += kCombineThreads) tot += fast_exp2((pl[s * p.pl_s] - M) * kLog2e);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  __syncthreads();                       // everyone has read red_s (max)
+  if (lane == 0) red_s[warp] = tot;
+  __syncthreads();
+  tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) tot += red_s[w];
   const float inv_tot = empty ? 0.f : 1.f / tot;
 
-  // Pass 2: each lane owns 4 consecutive head-dim elements; the weight of
-  // split s is broadcast from lane s of the chunk; loads are batched.
-  // (Every lane runs every iteration so the full-warp shuffles stay
-  // converged; lanes past the head dimension only skip their loads/stores.)
-  for (int c0 = 0; c0 * 4 < p.D; c0 += 32) {
-    const int c = c0 + lane;
-    const bool active = c * 4 < p.D;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (!empty) {
-      for (int s0 = 0; s0 < p.S; s0 += 32) {
-        const int sl = s0 + lane;
-        const float w_lane = sl < p.S ? fast_exp2((pl[sl * p.pl_s] - M) * kLog2e) * inv_tot : 0.f;
-        const int nchunk = min(32, p.S - s0);
-#pragma unroll 8
-        for (int j = 0; j < nchunk; ++j) {
-          const float w = __shfl_sync(0xffffffffu, w_lane, j);
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (active && w != 0.f)                       // empty split: ignore its O
-            v = *reinterpret_cast<const float4*>(po + (s0 + j) * p.po_s + c * 4);
-          acc.x = fmaf(w, v.x, acc.x);
-          acc.y = fmaf(w, v.y, acc.y);
-          acc.z = fmaf(w, v.z, acc.z);
-          acc.w = fmaf(w, v.w, acc.w);
-        }
+  // ---- pass 2: O = sum_i w_i O_i, split groups in parallel
+  const int CD = p.D >> 2;                            // float4 chunks per row (<= 128)
+  const int SG = kCombineThreads / CD;                // split groups (>= 1)
+  const int c = tid % CD;
+  const int sg = tid / CD;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (!empty && sg < SG) {
+    const float* pc = po + c * 4;
+#pragma unroll 4
+    for (int s = sg; s < p.S; s += SG) {
+      const float ls = pl[s * p.pl_s];
+      const float4 v = *reinterpret_cast<const float4*>(pc + s * p.po_s);
+      const float w = fast_exp2((ls - M) * kLog2e) * inv_tot;   // -inf -> 0
+      if (w != 0.f) {
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
       }
     }
-    if (active) {
-      float* out = p.out + r1 * p.out_r1 + r2 * p.out_r2 + c * 4;
-      out[0] = acc.x;
-      out[1] = acc.y;
-      out[2] = acc.z;
-      out[3] = acc.w;
-    }
   }
-  if (lane == 0 && p.lse != nullptr)
+  acc_s[tid] = acc;
+  __syncthreads();
+  if (tid < CD) {
+    float4 o = acc_s[tid];
+    for (int gI = 1; gI < SG; ++gI) {
+      const float4 a = acc_s[gI * CD + tid];
+      o.x += a.x;
+      o.y += a.y;
+      o.z += a.z;
+      o.w += a.w;
+    }
+    float* out = p.out + r1 * p.out_r1 + r2 * p.out_r2 + tid * 4;
+    out[0] = o.x;
+    out[1] = o.y;
+    out[2] = o.z;
+    out[3] = o.w;
+  }
+  if (tid == 0 && p.lse != nullptr)
     p.lse[r1 * p.lse_r1 + r2 * p.lse_r2] = empty ? M : M + __logf(tot);
 }
 

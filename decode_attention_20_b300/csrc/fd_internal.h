@@ -49,6 +49,22 @@ struct CombineParams {
   int R1, R2, S, D;
 };
 
+// Arguments of the bifurcated context kernel (one CTA per (128-row M-tile,
+// context split, kv head)); rows of kv head g are (sample, head-in-group)
+// pairs, row m = sample * G + r.
+struct BifCtxParams {
+  int n, Hq, Hkv, G, Lc, ns;
+  int rows;                   // n * G
+  float scale_log2;           // scale * log2(e)
+  float* o;                   // partial outputs, fp32
+  int64_t o_sb, o_sh, o_ss;   // strides over (sample, q head, split)
+  float* lse;                 // natural-log partial lse
+  int64_t l_sb, l_sh, l_ss;
+};
+
+// Tokens per tile of the bifurcated context kernel.
+constexpr int kBifTileTokens = 128;
+
 // Host launchers (return a cudaError_t from the launch).
 cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
                              const CUtensorMap& tmV, int D, int G, cudaStream_t st,
@@ -59,6 +75,8 @@ int mma_tile_tokens(int variant);
 cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16,
                                  cudaStream_t st);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmV, int mtiles, cudaStream_t st);
 
 // Tile height (tokens) of the TMA split kernel; the tensor-map box uses it.
 constexpr int kSplitTileTokens = 64;

@@ -8,6 +8,7 @@
 #include "fd_internal.h"
 #include "fd_split.cuh"
 #include "fd_split_mma.cuh"
+#include "fd_bif_ctx.cuh"
 
 namespace fd {
 
@@ -134,8 +135,8 @@ cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaS
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
   const int rows = p.R1 * p.R2;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((rows + kCombineWarps - 1) / kCombineWarps);
-  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(kCombineThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -144,6 +145,24 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, lse_combine_kernel, p);
+}
+
+cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                           const CUtensorMap& tmV, int mtiles, cudaStream_t st) {
+  static unsigned long long attr_set = 0ull;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_set & bit)) {
+    e = cudaFuncSetAttribute(bif_ctx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BifCfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set |= bit;
+  }
+  dim3 grid(mtiles, p.ns, p.Hkv);
+  bif_ctx_kernel<<<grid, BifCfg::THREADS, BifCfg::SMEM_BYTES, st>>>(p, tmQ, tmK, tmV);
+  return cudaGetLastError();
 }
 
 }  // namespace fd

@@ -214,11 +214,16 @@ FD_API fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor
 
 /*
  * fd_choose_num_splits — split-count heuristic (pure host function).
- * Fill about two waves of CTAs: ns = floor(2 * num_sms / (batch * kv_heads)),
- * at most ceil(max_len / 256), clamped to [1, FD_MAX_SPLITS].  Returns 1 for
- * any non-positive argument.  The Flash-Decoding page ("Why decoding needs
- * different scheduling") fixes only the direction: split when the batch
- * leaves too few blocks, not when the history is short or the batch large.
+ * Returns the smallest ns in [1, min(FD_MAX_SPLITS, ceil(max_len / 256))]
+ * that minimises the modelled makespan
+ *     waves(ns) * (chunk(ns) + 256)
+ * where chunk(ns) is the fd_split_bounds chunk of a max_len history and
+ * waves(ns) = ceil(batch * kv_heads * nonempty_splits / num_sms) rounds of
+ * one CTA per SM; the 256 tokens charge each wave its fixed start-up and
+ * epilogue time.  Returns 1 for any non-positive argument.  The
+ * Flash-Decoding page ("Why decoding needs different scheduling") fixes only
+ * the direction: split when the batch leaves SMs idle, not when the history
+ * is short or the batch already fills the GPU.
  */
 FD_API int32_t fd_choose_num_splits(int64_t batch, int64_t kv_heads, int64_t max_len,
                              int32_t num_sms);

@@ -43,5 +43,7 @@ from .attention import (  # noqa: F401
     required_bytes_ref,
     SPLIT_ALIGN,
     MAX_SPLITS,
+    MIN_CHUNK,
+    SPLIT_OVERHEAD_TOKENS,
 )
 from .bruteforce import attention_bruteforce  # noqa: F401

@@ -25,6 +25,9 @@ SPLIT_ALIGN = 64
 MAX_SPLITS = 256
 # Shortest chunk the split heuristic will create (tokens).
 MIN_CHUNK = 256
+# Fixed cost of one wave of split CTAs in the heuristic's makespan model, in
+# tokens of streaming (start-up latency of the first tiles plus the epilogue).
+SPLIT_OVERHEAD_TOKENS = 256
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:
@@ -166,17 +169,30 @@ def choose_num_splits_ref(batch: int, kv_heads: int, max_len: int, num_sms: int)
     The Flash-Decoding page ("Why decoding needs different scheduling") gives
     only the direction: a small batch leaves too few independent blocks, so
     split the history; a short history or a large batch makes more splitting
-    useless.  Reading adopted: fill about two waves of CTAs,
-        ns = floor(2 * num_sms / (batch * kv_heads)),
-    never more than ceil(max_len / MIN_CHUNK) splits, clamped to
-    [1, MAX_SPLITS].
+    useless, and more splits are no guaranteed gain.  Reading adopted: a
+    makespan model.  With ns splits of a max_len history, one CTA per
+    (sequence, kv head, split) and one CTA per SM at a time,
+        chunk  = the split chunk of split_bounds_ref(max_len, ns, .)
+        waves  = ceil(batch * kv_heads * nonempty_splits / num_sms)
+        cost   = waves * (chunk + SPLIT_OVERHEAD_TOKENS)
+    and the smallest ns in [1, min(MAX_SPLITS, ceil(max_len / MIN_CHUNK))]
+    with the lowest cost wins.  SPLIT_OVERHEAD_TOKENS charges each wave the
+    fixed start-up and epilogue time of a CTA, in tokens of streaming.
     """
     units = batch * kv_heads
     if units <= 0 or max_len <= 0 or num_sms <= 0:
         return 1
-    ns = (2 * num_sms) // units
-    cap = max(1, -(-max_len // MIN_CHUNK))
-    return int(max(1, min(ns, cap, MAX_SPLITS)))
+    cap = max(1, min(MAX_SPLITS, -(-max_len // MIN_CHUNK)))
+    best_ns, best_cost = 1, None
+    for ns in range(1, cap + 1):
+        per = -(-max_len // ns)
+        chunk = -(-per // SPLIT_ALIGN) * SPLIT_ALIGN
+        used = -(-max_len // chunk)
+        waves = -(-(units * used) // num_sms)
+        cost = waves * (chunk + SPLIT_OVERHEAD_TOKENS)
+        if best_cost is None or cost < best_cost:
+            best_ns, best_cost = ns, cost
+    return int(best_ns)
 
 
 def split_partials_ref(q, k, v, seqlens, scale, ns):

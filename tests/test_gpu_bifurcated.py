@@ -68,3 +68,47 @@ def test_bifurcated_mqa_sampling_workload(cuda_device):
     rep = inputs.replicate_context(case)
     O2, L2 = fd.decode_attention(rep.q, rep.k, rep.v, rep.seqlens.cuda(), 0, rep.scale)
     assert_parity(to_f64(O2), to_f64(L2), O_ref, L_ref, torch.bfloat16, "replicated")
+
+
+# ---------------------------------------------------------------------------
+# Context part on the tensor cores (default) and on the split kernel over a
+# batch-broadcast view of the context (FD_BIF_CTX=split): both against the
+# oracle, across M-tile tails, context tails, split counts and a peaked
+# softmax that makes the running max jump (accumulator rescaling).
+
+@pytest.fixture(params=["tc", "split"])
+def ctx_path(request, monkeypatch):
+    monkeypatch.setenv("FD_BIF_CTX", request.param)
+    return request.param
+
+
+@pytest.mark.parametrize("n,hkv,G,lc,ld,ctx_splits", [
+    (5, 1, 32, 300, 70, 0),        # rows 160: two M-tiles, second one ragged
+    (4, 1, 32, 256, 16, 1),        # rows 128: exactly one M-tile, whole tiles
+    (40, 4, 8, 1000, 33, 0),       # GQA, 3 M-tiles per kv head, context tail of 104
+    (3, 2, 64, 129, 5, 2),         # G = 64, second split holds one token
+    (16, 1, 8, 4173, 20, 1),       # one split streams 33 tiles (rings wrap many times)
+    (2, 1, 1, 700, 9, 0),          # G = 1
+])
+def test_bifurcated_ctx_paths(cuda_device, ctx_path, n, hkv, G, lc, ld, ctx_splits):
+    case = inputs.bifurcated_case(n, hkv * G, hkv, 128, lc, ld, seed=n * 7 + G,
+                                  ragged_dec=(0, ld))
+    O, L = _run(case, ctx_splits)
+    O_ref, L_ref = _ref(case)
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16,
+                  f"{ctx_path} n={n} hkv={hkv} G={G} lc={lc} ns={ctx_splits}")
+
+
+@pytest.mark.parametrize("ctx_splits", [0, 1])
+def test_bifurcated_peaked_context(cuda_device, ctx_path, ctx_splits):
+    """Context keys at a seeded 2% of positions scaled by 8 (exact in bf16):
+    scores jump late in a split, so the running max moves by far more than
+    the lazy-rescale threshold."""
+    case = inputs.bifurcated_case(8, 32, 1, 128, 2048, 40, seed=77, ragged_dec=(1, 40))
+    gen = torch.Generator().manual_seed(78)
+    pos = torch.randperm(2048, generator=gen)[:41]
+    case.k_ctx[pos] = case.k_ctx[pos] * 8
+    O, L = _run(case, ctx_splits)
+    O_ref, L_ref = _ref(case)
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16,
+                  f"{ctx_path} peaked ns={ctx_splits}")

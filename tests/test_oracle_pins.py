@@ -223,22 +223,40 @@ def test_heuristic_properties():
     sms = 148
     for B in [1, 2, 4, 8, 32, 64, 256]:
         for hkv in [1, 8]:
-            prev = None
             for L in [1, 64, 256, 512, 1024, 4096, 65536, 131072, 1 << 20]:
                 ns = oracle.choose_num_splits_ref(B, hkv, L, sms)
                 assert 1 <= ns <= oracle.MAX_SPLITS
-                if prev is not None:
-                    assert ns >= prev                      # longer history: never fewer
-                prev = ns
-                if ns > 1:
-                    assert ns * B * hkv <= 2 * sms         # at most ~two waves of CTAs
-    # short history -> no splitting; more batch -> never more splits
+                assert ns <= max(1, -(-L // oracle.MIN_CHUNK))   # chunks of >= 256 tokens
+    # short history -> no splitting
     assert oracle.choose_num_splits_ref(1, 8, 200, sms) == 1
-    for L in [4096, 65536]:
-        seq = [oracle.choose_num_splits_ref(B, 8, L, sms) for B in [1, 2, 4, 8, 16, 32]]
-        assert all(a >= b for a, b in zip(seq, seq[1:]))
-    assert oracle.choose_num_splits_ref(1, 8, 65536, 148) == 37
     assert oracle.choose_num_splits_ref(0, 8, 65536, 148) == 1
+
+
+def _makespan(units, L, ns, sms):
+    chunk = -(-(-(-L // ns)) // oracle.SPLIT_ALIGN) * oracle.SPLIT_ALIGN
+    used = -(-L // chunk)
+    return -(-(units * used) // sms) * (chunk + oracle.SPLIT_OVERHEAD_TOKENS)
+
+
+def test_heuristic_is_the_makespan_minimiser():
+    """Brute force over every admissible ns: the choice has the lowest
+    modelled makespan, and no smaller ns ties it."""
+    for sms in [148, 132]:
+        for units in [1, 8, 16, 32, 64, 256, 1000]:
+            for L in [300, 4096, 65536, 131072]:
+                ns = oracle.choose_num_splits_ref(units, 1, L, sms)
+                costs = {k: _makespan(units, L, k, sms)
+                         for k in range(1, min(oracle.MAX_SPLITS, -(-L // oracle.MIN_CHUNK)) + 1)}
+                assert costs[ns] == min(costs.values())
+                assert all(costs[k] > costs[ns] for k in costs if k < ns)
+
+
+def test_heuristic_workload_choices():
+    # one wave of 144 CTAs for the batch-1 64K layer; ~two waves at batch 4
+    # over 128K; about seven waves for the batch-32 cache of 32K
+    assert oracle.choose_num_splits_ref(1, 8, 65536, 148) == 18
+    assert oracle.choose_num_splits_ref(4, 8, 131072, 148) == 9
+    assert oracle.choose_num_splits_ref(32, 8, 32768, 148) == 4
 
 
 def test_required_bytes_config_flash_decoding_64k():
