@@ -1,24 +1,34 @@
-"""Benchmark: split-KV decode attention, batch 1, CodeLlama-34B-shaped layer
-(64 query heads, 8 kv heads, head dim 128, bf16), 65536 cached tokens.
+"""Benchmark of the decode-attention hot path on one B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
+                    [--workload b1_64k|ragged_b32|long_b4|bif_mqa] [--num-splits S]
 
-One step = one fd_decode_attention call (split kernel + log-sum-exp combine)
-over the whole 64K history.  Prints ONE JSON line (rank 0):
-  value        device-timed microseconds per call (CUDA events around K calls
-               replayed from a CUDA graph; inputs resident in HBM; the K/V
-               cache rotates over 4 copies of 268 MB, each larger than L2)
-  e2e          microseconds per step through the Python API with pinned host
-               buffers: H2D of the step's new query and new K/V row, the call,
-               D2H of out + lse, stream synchronised every step
-  roofline     the split kernel's algorithmic bytes / its mean CUDA-event
-               duration, against the measured HBM copy bandwidth
-  cpu_baseline the fp64 CPU oracle on the same workload (rank 0, N = 1)
+Default workload: split-KV decode attention at batch 1 over a 65536-token
+history of a CodeLlama-34B-shaped layer (64 query heads, 8 kv heads, head
+dim 128, bf16 K/V, fp32 out + LSE).  One step = one library call (split
+kernel + log-sum-exp combine) over the whole history.  Other workloads:
+  ragged_b32  batch 32, 32/8 heads, padded [32, 32768, 8, 128] cache, lengths
+              uniform in [1024, 32768]
+  long_b4     batch 4, 131072 tokens, 32/8 heads, 1% of keys scaled by 8
+  bif_mqa     bifurcated attention: 64 samples share an 8192-token context,
+              256 own decode tokens each, 32 query heads on 1 kv head; the
+              line also carries the replicated-context decode time
+Prints ONE JSON line (rank 0):
+  value        device-timed microseconds per call: CUDA events around K calls
+               replayed from a CUDA graph, inputs resident in HBM and rotated
+               over enough copies that every call reads past L2
+  e2e          microseconds per step through the Python API: H2D from pinned
+               host memory of the step's new inputs (query, one new K/V row per
+               sequence), the call, D2H of out (+ lse), synchronised per step
+  roofline     the dominant kernel's algorithmic bytes (or FLOPs) per launch /
+               its mean CUDA-event duration, against the measured peak
+  cpu_baseline the fp64 CPU oracle timed on a bounded sample of the same
+               workload on the host cores (rank 0, N = 1)
 With --gpus N > 1 (torchrun), every rank runs an independent replica (the
 method has no cross-GPU exchange); value is the max over ranks.
 
---impl reference times the fp64 CPU oracle on the host cores instead (each
-step a bounded sample of the same workload, extrapolated to one full call).
+--impl reference times the fp64 CPU oracle instead (each step a bounded
+sample of the same workload, extrapolated to one full call).
 """
 
 from __future__ import annotations
@@ -36,22 +46,11 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-L_TOKENS = 65536
-B, HQ, HKV, D = 1, 64, 8, 128
-WORKLOAD = "flash_decoding_b1_h64_kv8_d128_bf16_L65536"
 METRIC = "split-KV decode attention µs/call and achieved HBM GB/s vs ~8 TB/s peak"
-NBUF = 4
-
-
-def required_bytes(lens=(L_TOKENS,)):
-    kv = sum(lens) * HKV * D * 2 * 2
-    return kv + B * HQ * D * 2 + B * HQ * D * 4 + B * HQ * 4
-
-
-def split_kernel_bytes(lens=(L_TOKENS,)):
-    """Algorithmic bytes the split kernel must move: K and V over the history
-    plus the query (its partial outputs are scratch, not required traffic)."""
-    return sum(lens) * HKV * D * 2 * 2 + B * HQ * D * 2
+L2_BYTES = 126 << 20
+FD_KERNEL_SPLIT, FD_KERNEL_COMBINE, FD_KERNEL_BIF_CTX = 0, 1, 2
+KERNEL_NAMES = {FD_KERNEL_SPLIT: "split_mma_kernel (mma.sync bf16, TMA ring)",
+                FD_KERNEL_BIF_CTX: "bif_ctx_kernel (tcgen05.mma, TMEM accumulators)"}
 
 
 def load_peaks():
@@ -59,8 +58,9 @@ def load_peaks():
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return 6400.0, "fallback"
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "kind": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "kind": "fallback"}
 
 
 # ------------------------------------------------------------------ clocks
@@ -104,37 +104,18 @@ class ClockSampler:
                 if len(parts) >= 9:
                     rows.append(parts)
         os.unlink(self.path)
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        num = lambda x: x.replace(".", "", 1).isdigit()
+        sm = [float(r[1]) for r in rows if num(r[1])]
+        smax = [float(r[2]) for r in rows if num(r[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
         for r in rows:
             for i, n in enumerate(names):
                 if r[5 + i].lower().startswith("active"):
                     reasons.add(n)
-        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(rows),
-                "power_w_max": max(power) if power else None}
-
-
-# ------------------------------------------------------------------ oracle timing
-
-def oracle_time_per_call(tokens_per_step, steps, warmup, q, k, v, scale):
-    """Time the fp64 oracle on a sample: the first ``tokens_per_step`` tokens
-    of the history for every kv head.  Returns (seconds per full call
-    extrapolated linearly in tokens, seconds per step, threads)."""
-    import oracle
-    kk = k[:, :tokens_per_step]
-    vv = v[:, :tokens_per_step]
-    for _ in range(warmup):
-        oracle.decode_attention_ref(q, kk, vv, None, scale)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        oracle.decode_attention_ref(q, kk, vv, None, scale)
-    dt = (time.perf_counter() - t0) / max(1, steps)
-    return dt * (L_TOKENS / tokens_per_step), dt
+                "reasons": sorted(reasons), "samples": len(rows)}
 
 
 def blas_threads():
@@ -146,48 +127,334 @@ def blas_threads():
         return os.cpu_count() or 1
 
 
-def oracle_inputs(case):
+def f64(t):
     import numpy as np
     import torch
     import oracle
+    t = t.detach().to("cpu").contiguous()
+    if t.dtype == torch.bfloat16:
+        return oracle.bf16_bits_to_f64(t.view(torch.uint16).numpy())
+    return t.numpy().astype(np.float64)
 
-    def f64(t):
-        t = t.detach().to("cpu").contiguous()
-        if t.dtype == torch.bfloat16:
-            return oracle.bf16_bits_to_f64(t.view(torch.uint16).numpy())
-        return t.numpy().astype(np.float64)
-    return f64(case.q), f64(case.k), f64(case.v)
 
+# ------------------------------------------------------------------ workloads
+
+class Workload:
+    """One benchmark workload: device inputs, the timed call, its byte / FLOP
+    accounting, an end-to-end step and a bounded oracle sample."""
+
+    short = ""
+    name = ""
+    dominant = FD_KERNEL_SPLIT
+
+    def config(self):
+        raise NotImplementedError
+
+
+class DecodeWorkload(Workload):
+    dominant = FD_KERNEL_SPLIT
+
+    def __init__(self, short, builder, device):
+        import torch
+        from decode_attention_20_b300 import inputs
+        self.short = short
+        self.case = builder(device)
+        c = self.case
+        self.name = c.name
+        self.B, self.Hq, self.D = c.q.shape
+        self.Lcap, self.Hkv = c.k.shape[1], c.k.shape[2]
+        self.lens = c.lens
+        self.seqlens_dev = c.seqlens.to(device) if c.seqlens is not None else None
+        kv_bytes = c.k.numel() * c.k.element_size() * 2
+        self.nbuf = max(1, min(8, math.ceil(2 * L2_BYTES / kv_bytes) + (1 if kv_bytes < 4 * L2_BYTES else 0)))
+        self.ks = [c.k] + [c.k.clone() for _ in range(self.nbuf - 1)]
+        self.vs = [c.v] + [c.v.clone() for _ in range(self.nbuf - 1)]
+        self.out = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=device)
+        self.lse = torch.empty((self.B, self.Hq), dtype=torch.float32, device=device)
+        esz = c.k.element_size()
+        tokens = sum(self.lens)
+        self.kv_req = tokens * self.Hkv * self.D * esz * 2
+        self.required = (self.kv_req + c.q.numel() * c.q.element_size()
+                         + self.out.numel() * 4 + self.lse.numel() * 4)
+        self.dominant_units = self.kv_req + c.q.numel() * c.q.element_size()   # split kernel bytes
+        self.bound, self.unit = "hbm", "GB/s"
+
+    def config(self, ns):
+        return {"workload": self.name, "batch": self.B, "q_heads": self.Hq, "kv_heads": self.Hkv,
+                "head_dim": self.D, "kv_capacity": self.Lcap,
+                "kv_tokens": sum(self.lens), "num_splits": ns}
+
+    def prepare(self, L, stream, ns):
+        from decode_attention_20_b300.api import _desc
+        c = self.case
+        self.ns = ns
+        self.dq, self.do, self.dl = _desc(c.q, "q"), _desc(self.out, "out"), _desc(self.lse, "lse")
+        self.ds = _desc(self.seqlens_dev, "seqlens")
+        self.dks = [_desc(x, "k") for x in self.ks]
+        self.dvs = [_desc(x, "v") for x in self.vs]
+        self.L = L
+        self.sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def call(self, i):
+        r = ctypes.byref
+        st = self.L.fd_decode_attention(r(self.dq), r(self.dks[i % self.nbuf]), r(self.dvs[i % self.nbuf]),
+                                        r(self.ds) if self.ds is not None else None, self.ns,
+                                        ctypes.c_float(self.case.scale), r(self.do), r(self.dl), self.sptr)
+        if st:
+            raise RuntimeError(self.L.fd_last_error().decode())
+
+    def e2e(self, stream, steps):
+        """Per step: H2D of the new query and one new K/V row per sequence
+        (written at position len_b - 1), the call, D2H of out + lse."""
+        import torch
+        import decode_attention_20_b300 as fd
+        c = self.case
+        hq = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
+        hq.copy_(c.q.cpu())
+        hk = torch.empty((self.B, self.Hkv, self.D), dtype=c.k.dtype).pin_memory()
+        hv = torch.empty_like(hk).pin_memory()
+        pos = [max(0, n - 1) for n in self.lens]
+        for b in range(self.B):
+            hk[b].copy_(c.k[b, pos[b]].cpu())
+            hv[b].copy_(c.v[b, pos[b]].cpu())
+        hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        rows = torch.tensor([b * self.Lcap + pos[b] for b in range(self.B)], dtype=torch.int64,
+                            device=c.q.device)
+        dk = torch.empty((self.B, self.Hkv * self.D), dtype=c.k.dtype, device=c.q.device)
+        dv = torch.empty_like(dk)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
+                c.q.copy_(hq, non_blocking=True)
+                dk.copy_(hk.view(self.B, -1), non_blocking=True)
+                dv.copy_(hv.view(self.B, -1), non_blocking=True)
+                kb.view(self.B * self.Lcap, -1).index_copy_(0, rows, dk)
+                vb.view(self.B * self.Lcap, -1).index_copy_(0, rows, dv)
+                fd.decode_attention(c.q, kb, vb, self.seqlens_dev, self.ns, c.scale, out=self.out,
+                                    lse=self.lse, stream=stream)
+                hout.copy_(self.out, non_blocking=True)
+                hlse.copy_(self.lse, non_blocking=True)
+                stream.synchronize()
+        us = (time.perf_counter() - t0) * 1e6 / steps
+        h2d = hq.numel() * hq.element_size() + hk.numel() * hk.element_size() * 2
+        d2h = hout.numel() * 4 + hlse.numel() * 4
+        return us, h2d, d2h
+
+    def oracle_sample(self, target_s):
+        """Time the oracle on the first T tokens of sequence 0 (all kv
+        heads), T sized for about target_s seconds (at least 64 tokens);
+        returns (us per full call extrapolated by tokens, sample text,
+        seconds of the sample)."""
+        import oracle
+        c = self.case
+        if not hasattr(self, "_of"):
+            n0 = max(self.lens[0], 1)
+            self._of = (f64(c.q[0:1]), f64(c.k[0:1, :n0]), f64(c.v[0:1, :n0]))
+            q, k, v = self._of
+            T0 = min(n0, 2048)
+            t0 = time.perf_counter()
+            oracle.decode_attention_ref(q, k[:, :T0], v[:, :T0], None, c.scale)
+            self._per_tok = (time.perf_counter() - t0) / T0
+        q, k, v = self._of
+        T = int(max(min(64, self.lens[0]), min(self.lens[0], target_s / self._per_tok)))
+        t0 = time.perf_counter()
+        oracle.decode_attention_ref(q, k[:, :T], v[:, :T], None, c.scale)
+        dt = time.perf_counter() - t0
+        full = dt * (sum(self.lens) / T)
+        return full * 1e6, (f"sequence 0, first {T} tokens x all {self.Hkv} kv heads per call, "
+                            f"extrapolated linearly to {sum(self.lens)} tokens x {self.B} sequences"), dt
+
+
+class BifWorkload(Workload):
+    dominant = FD_KERNEL_BIF_CTX
+
+    def __init__(self, device):
+        import torch
+        from decode_attention_20_b300 import inputs
+        self.short = "bif_mqa"
+        c = self.case = inputs.bifurcated_mqa(device=device)
+        self.name = c.name
+        self.n, self.Hq, self.D = c.q.shape
+        self.Lc, self.Hkv = c.k_ctx.shape[0], c.k_ctx.shape[1]
+        self.Ld = c.k_dec.shape[1]
+        self.dec_dev = c.dec_lens.to(device) if c.dec_lens is not None else None
+        per_copy = sum(x.numel() * 2 for x in [c.k_ctx, c.v_ctx, c.k_dec, c.v_dec, c.q])
+        self.nbuf = max(1, math.ceil(2 * L2_BYTES / per_copy))
+        self.bufs = [(c.q, c.k_ctx, c.v_ctx, c.k_dec, c.v_dec)] + [
+            tuple(x.clone() for x in (c.q, c.k_ctx, c.v_ctx, c.k_dec, c.v_dec))
+            for _ in range(self.nbuf - 1)]
+        self.out = torch.empty((self.n, self.Hq, self.D), dtype=torch.float32, device=device)
+        self.lse = torch.empty((self.n, self.Hq), dtype=torch.float32, device=device)
+        kv_ctx = c.k_ctx.numel() * 2 * 2
+        kv_dec = sum(self.case.lens) * self.Hkv * self.D * 2 * 2
+        self.required = kv_ctx + kv_dec + c.q.numel() * 2 + self.out.numel() * 4 + self.lse.numel() * 4
+        self.dominant_units = 4.0 * self.n * self.Hq * self.Lc * self.D     # context FLOPs
+        self.bound, self.unit = "tensor", "TFLOP/s"
+
+    def config(self, ns):
+        return {"workload": self.name, "samples": self.n, "q_heads": self.Hq, "kv_heads": self.Hkv,
+                "head_dim": self.D, "context_len": self.Lc, "decode_len": self.Ld,
+                "ctx_splits": ns}
+
+    def prepare(self, L, stream, ns):
+        from decode_attention_20_b300.api import _desc
+        self.ns = ns
+        self.L = L
+        self.sptr = ctypes.c_void_p(stream.cuda_stream)
+        self.dbufs = [[_desc(x, "t") for x in b] for b in self.bufs]
+        self.ddl = _desc(self.dec_dev, "dec_lens")
+        self.do, self.dl = _desc(self.out, "out"), _desc(self.lse, "lse")
+
+    def call(self, i):
+        r = ctypes.byref
+        d = self.dbufs[i % self.nbuf]
+        st = self.L.fd_bifurcated_attention_lse(r(d[0]), r(d[1]), r(d[2]), r(d[3]), r(d[4]),
+                                                r(self.ddl) if self.ddl is not None else None,
+                                                ctypes.c_float(self.case.scale), self.ns, r(self.do),
+                                                r(self.dl), self.sptr)
+        if st:
+            raise RuntimeError(self.L.fd_last_error().decode())
+
+    def replicated_us(self, stream, steps, ns):
+        """The same inputs with the context materialised per sample, through
+        the split-KV decode path (the comparison the method is measured
+        against)."""
+        import torch
+        import decode_attention_20_b300 as fd
+        from decode_attention_20_b300 import inputs
+        rep = inputs.replicate_context(self.case)
+        reps = [rep.k, rep.v]
+        nb = max(1, math.ceil(2 * L2_BYTES / (rep.k.numel() * 4)))
+        ks = [rep.k] + [rep.k.clone() for _ in range(nb - 1)]
+        vs = [rep.v] + [rep.v.clone() for _ in range(nb - 1)]
+        sl = rep.seqlens.to(rep.k.device)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                fd.decode_attention(rep.q, ks[i % nb], vs[i % nb], sl, 0, rep.scale, out=self.out,
+                                    lse=self.lse, stream=stream)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for i in range(steps):
+                fd.decode_attention(rep.q, ks[i % nb], vs[i % nb], sl, 0, rep.scale, out=self.out,
+                                    lse=self.lse, stream=stream)
+            e1.record(stream)
+        stream.synchronize()
+        kv = sum(rep.lens) * self.Hkv * self.D * 2 * 2
+        del ks, vs, reps
+        return e0.elapsed_time(e1) * 1e3 / steps, kv
+
+    def e2e(self, stream, steps):
+        """Per step: H2D of the queries and one new decode K/V row per sample,
+        the call, D2H of out + lse."""
+        import torch
+        import decode_attention_20_b300 as fd
+        c = self.case
+        hq = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
+        hq.copy_(c.q.cpu())
+        hk = torch.empty((self.n, self.Hkv, self.D), dtype=c.k_dec.dtype).pin_memory()
+        hv = torch.empty_like(hk).pin_memory()
+        pos = [max(0, x - 1) for x in c.lens]
+        for b in range(self.n):
+            hk[b].copy_(c.k_dec[b, pos[b]].cpu())
+            hv[b].copy_(c.v_dec[b, pos[b]].cpu())
+        hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        rows = torch.tensor([b * self.Ld + pos[b] for b in range(self.n)], dtype=torch.int64,
+                            device=c.q.device)
+        dk = torch.empty((self.n, self.Hkv * self.D), dtype=c.k_dec.dtype, device=c.q.device)
+        dv = torch.empty_like(dk)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                q, kc, vc, kd, vd = self.bufs[i % self.nbuf]
+                q.copy_(hq, non_blocking=True)
+                dk.copy_(hk.view(self.n, -1), non_blocking=True)
+                dv.copy_(hv.view(self.n, -1), non_blocking=True)
+                kd.view(self.n * self.Ld, -1).index_copy_(0, rows, dk)
+                vd.view(self.n * self.Ld, -1).index_copy_(0, rows, dv)
+                fd.bifurcated_attention(q, kc, vc, kd, vd, self.dec_dev, c.scale, out=self.out,
+                                        lse=self.lse, ctx_splits=self.ns, return_lse=True,
+                                        stream=stream)
+                hout.copy_(self.out, non_blocking=True)
+                hlse.copy_(self.lse, non_blocking=True)
+                stream.synchronize()
+        us = (time.perf_counter() - t0) * 1e6 / steps
+        h2d = hq.numel() * 2 + hk.numel() * 2 * 2
+        d2h = hout.numel() * 4 + hlse.numel() * 4
+        return us, h2d, d2h
+
+    def oracle_sample(self, target_s):
+        """Time the oracle on sample 0 with the first T context tokens (and
+        its own decode tokens), T sized for about target_s seconds (at least
+        64); returns (us per full call extrapolated by tokens and samples,
+        sample text, seconds of the sample)."""
+        import oracle
+        c = self.case
+        lens = c.lens
+        if not hasattr(self, "_of"):
+            self._of = (f64(c.q[:1]), f64(c.k_ctx), f64(c.v_ctx), f64(c.k_dec[:1]), f64(c.v_dec[:1]))
+            q, kc, vc, kd, vd = self._of
+            T0 = min(self.Lc, 2048)
+            t0 = time.perf_counter()
+            oracle.bifurcated_attention_ref(q, kc[:T0], vc[:T0], kd, vd, [lens[0]], c.scale)
+            self._per_tok = (time.perf_counter() - t0) / (T0 + lens[0])
+        q, kc, vc, kd, vd = self._of
+        T = int(max(64, min(self.Lc, target_s / self._per_tok - lens[0])))
+        t0 = time.perf_counter()
+        oracle.bifurcated_attention_ref(q, kc[:T], vc[:T], kd, vd, [lens[0]], c.scale)
+        dt = time.perf_counter() - t0
+        full_tokens = sum(self.Lc + x for x in lens)
+        return dt * full_tokens / (T + lens[0]) * 1e6, (
+            f"sample 0 with the first {T} of {self.Lc} context tokens and its {lens[0]} decode "
+            f"tokens per call, extrapolated linearly to {self.n} samples"), dt
+
+
+def make_workload(short, device):
+    from decode_attention_20_b300 import inputs
+    if short == "b1_64k":
+        return DecodeWorkload(short, lambda d: inputs.flash_decoding_b1(65536, seed=0, device=d), device)
+    if short == "ragged_b32":
+        return DecodeWorkload(short, lambda d: inputs.ragged_batch(device=d), device)
+    if short == "long_b4":
+        return DecodeWorkload(short, lambda d: inputs.long_context_peaked(device=d), device)
+    if short == "bif_mqa":
+        return BifWorkload(device)
+    raise SystemExit(f"unknown workload {short}")
+
+
+# ------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank):
     """--impl reference: the fp64 oracle on host cores, same workload."""
     if rank != 0:
         return 0
-    import torch
-    from decode_attention_20_b300 import inputs
-    case = inputs.flash_decoding_b1(L_TOKENS, seed=0, device="cpu")
-    q, k, v = oracle_inputs(case)
-    # calibrate: pick the tokens per step so warmup + steps take ~60 s
-    _, t_small = oracle_time_per_call(4096, 2, 1, q, k, v, case.scale)
-    per_token = t_small / 4096
-    budget = 60.0 / max(1, args.steps + args.warmup)
-    tokens = int(max(256, min(L_TOKENS, budget / per_token)))
-    tokens = (tokens // 256) * 256
-    full_s, step_s = oracle_time_per_call(tokens, args.steps, args.warmup, q, k, v, case.scale)
-    us = full_s * 1e6
-    sample = (f"{tokens} of {L_TOKENS} tokens x all 8 kv heads per step, extrapolated "
-              f"linearly to the full history")
+    w = make_workload(args.workload, "cpu")
+    budget = 100.0 / max(1, args.steps + args.warmup)
+    us = []
+    sample = ""
+    step_s = []
+    for i in range(args.warmup + args.steps):
+        u, sample, dt = w.oracle_sample(budget)
+        if i >= args.warmup:
+            us.append(u)
+            step_s.append(dt)
+    value = statistics.median(us)
     line = {
-        "impl": "reference", "metric": METRIC, "value": us, "unit": "us/call",
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "us/call",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": step_s * 1e3, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": B, "q_heads": HQ, "kv_heads": HKV,
-                   "head_dim": D, "kv_len": L_TOKENS, "parallelism": "replicas"},
-        "cpu_baseline": {"value": us, "unit": "us/call", "cores": blas_threads(),
+        "ms_per_step": statistics.median(step_s) * 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": w.config(args.num_splits),
+        "cpu_baseline": {"value": round(value, 1), "unit": "us/call", "cores": blas_threads(),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": us, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "achieved_gbs": required_bytes() / (us * 1e-6) / 1e9,
+        "e2e": {"value": round(value, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "achieved_gbs": round(w.required / (value * 1e-6) / 1e9, 3),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -199,55 +466,42 @@ def run_fd(args, rank, world):
     import torch
     import torch.distributed as dist
     import decode_attention_20_b300 as fd
-    from decode_attention_20_b300 import _lib, inputs
+    from decode_attention_20_b300 import _lib
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     L = _lib.lib()
     props = torch.cuda.get_device_properties(dev)
-    case = inputs.flash_decoding_b1(L_TOKENS, seed=0, device="cuda")
-    ks = [case.k] + [case.k.clone() for _ in range(NBUF - 1)]
-    vs = [case.v] + [case.v.clone() for _ in range(NBUF - 1)]
-    q = case.q
-    out = torch.empty((B, HQ, D), dtype=torch.float32, device=dev)
-    lse = torch.empty((B, HQ), dtype=torch.float32, device=dev)
-    ns = args.num_splits if args.num_splits else fd.choose_num_splits(B, HKV, L_TOKENS, props.multi_processor_count)
-
+    w = make_workload(args.workload, dev)
+    if isinstance(w, DecodeWorkload):
+        ns = args.num_splits or fd.choose_num_splits(w.B, w.Hkv, w.Lcap, props.multi_processor_count)
+    else:
+        ns = args.num_splits     # 0: the library's context split choice
     stream = torch.cuda.Stream(device=dev)
-    sptr = ctypes.c_void_p(stream.cuda_stream)
-    from decode_attention_20_b300.api import _desc
-    dq, do, dl = _desc(q, "q"), _desc(out, "out"), _desc(lse, "lse")
-    dks = [_desc(x, "k") for x in ks]
-    dvs = [_desc(x, "v") for x in vs]
-    r = ctypes.byref
-
-    def call(i):
-        st = L.fd_decode_attention(r(dq), r(dks[i % NBUF]), r(dvs[i % NBUF]), None, ns,
-                                   ctypes.c_float(case.scale), r(do), r(dl), sptr)
-        if st:
-            raise RuntimeError(L.fd_last_error().decode())
+    w.prepare(L, stream, ns)
 
     def barrier():
         if world > 1:
             dist.barrier()
 
+    warm = max(3, args.warmup)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for i in range(max(3, args.warmup)):
-            call(i)
+        for i in range(warm):
+            w.call(i)
     stream.synchronize()
     fd.check_device_error(stream)
 
-    # CUDA graph of NBUF consecutive calls (one per rotating cache copy)
-    reps = max(1, math.ceil(args.steps / NBUF))
-    steps = reps * NBUF
+    # CUDA graph of nbuf consecutive calls (one per rotating input copy)
+    reps = max(1, math.ceil(args.steps / w.nbuf))
+    steps = reps * w.nbuf
     graph = None
-    timing = "CUDA graph of 4 calls, replayed"
+    timing = f"CUDA graph of {w.nbuf} calls, replayed"
     try:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(NBUF):
-                call(i)
+            for i in range(w.nbuf):
+                w.call(i)
         for _ in range(2):
             g.replay()
         torch.cuda.synchronize()
@@ -271,111 +525,160 @@ def run_fd(args, rank, world):
                 graph.replay()
         else:
             for i in range(steps):
-                call(i)
+                w.call(i)
         e1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms_total = e0.elapsed_time(e1)
-    us_per_call = ms_total * 1e3 / steps
+    us_per_call = e0.elapsed_time(e1) * 1e3 / steps
+    del graph
 
     # Direct API calls (no graph), same rotation: launch overhead included.
+    dsteps = min(steps, 2000)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         e0.record(stream)
-        for i in range(steps):
-            call(i)
+        for i in range(dsteps):
+            w.call(i)
         e1.record(stream)
     stream.synchronize()
-    us_direct = e0.elapsed_time(e1) * 1e3 / steps
+    us_direct = e0.elapsed_time(e1) * 1e3 / dsteps
 
     # Per-kernel durations (CUDA events around each launch on its stream).
     fd.profile_enable(True)
     with torch.cuda.stream(stream):
-        for i in range(steps):
-            call(i)
+        for i in range(dsteps):
+            w.call(i)
     stream.synchronize()
-    n_split, ms_split = fd.profile_read(fd.FD_KERNEL_SPLIT)
-    n_comb, ms_comb = fd.profile_read(fd.FD_KERNEL_COMBINE)
+    kern = {}
+    launches = 0
+    for kind, label in [(FD_KERNEL_SPLIT, "split"), (FD_KERNEL_COMBINE, "combine"),
+                        (FD_KERNEL_BIF_CTX, "bif_ctx")]:
+        n, ms = fd.profile_read(kind)
+        launches += n
+        if n:
+            kern[label + "_us"] = round(ms * 1e3 / n, 3)
+            kern[label + "_launches_per_call"] = n / dsteps
     fd.profile_enable(False)
-    launches_per_call = (n_split + n_comb) / steps
-    split_us = ms_split * 1e3 / max(1, n_split)
-    comb_us = ms_comb * 1e3 / max(1, n_comb)
+    launches_per_call = launches / dsteps
+    dom_label = {FD_KERNEL_SPLIT: "split", FD_KERNEL_BIF_CTX: "bif_ctx"}[w.dominant]
+    dom_us = kern[dom_label + "_us"]
 
-    # End to end through the Python API with pinned host buffers.
-    hq = torch.empty((B, HQ, D), dtype=torch.bfloat16).pin_memory()
-    hq.copy_(q.cpu())
-    hkv = torch.empty((2, B, HKV, D), dtype=torch.bfloat16).pin_memory()
-    hkv[0].copy_(case.k[:, L_TOKENS - 1].cpu())
-    hkv[1].copy_(case.v[:, L_TOKENS - 1].cpu())
-    hout = torch.empty((B, HQ, D), dtype=torch.float32).pin_memory()
-    hlse = torch.empty((B, HQ), dtype=torch.float32).pin_memory()
-    e2e_steps = max(1, min(steps, 2000))
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
-        for i in range(e2e_steps):
-            kb, vb = ks[i % NBUF], vs[i % NBUF]
-            q.copy_(hq, non_blocking=True)
-            kb[:, L_TOKENS - 1].copy_(hkv[0], non_blocking=True)
-            vb[:, L_TOKENS - 1].copy_(hkv[1], non_blocking=True)
-            fd.decode_attention(q, kb, vb, None, ns, case.scale, out=out, lse=lse, stream=stream)
-            hout.copy_(out, non_blocking=True)
-            hlse.copy_(lse, non_blocking=True)
-            stream.synchronize()
-    e2e_us = (time.perf_counter() - t0) * 1e6 / e2e_steps
-    h2d = hq.numel() * 2 + hkv.numel() * 2
-    d2h = hout.numel() * 4 + hlse.numel() * 4
+    extra = {}
+    if isinstance(w, BifWorkload):
+        rep_us, rep_kv = w.replicated_us(stream, min(steps, 400), 0)
+        extra["replicated_context_us"] = round(rep_us, 3)
+        extra["speedup_vs_replicated"] = round(rep_us / us_per_call, 3)
+        kv_bif = w.case.k_ctx.numel() * 4 + sum(w.case.lens) * w.Hkv * w.D * 4
+        extra["kv_byte_ratio_replicated_over_bifurcated"] = round(rep_kv / kv_bif, 3)
+        extra["h_over_g"] = w.Hq // w.Hkv
+
+    e2e_us, h2d, d2h = w.e2e(stream, max(1, min(steps, 1000)))
     fd.check_device_error(stream)
 
-    # max over ranks
-    vals = torch.tensor([us_per_call, e2e_us, split_us], dtype=torch.float64, device=dev)
+    vals = torch.tensor([us_per_call, e2e_us, dom_us], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    us_per_call, e2e_us, split_us = [float(x) for x in vals.tolist()]
+    us_per_call, e2e_us, dom_us = [float(x) for x in vals.tolist()]
     if rank != 0:
         return 0
 
-    peak, peak_kind = load_peaks()
-    req = required_bytes()
-    gbs = req / (us_per_call * 1e-6) / 1e9
-    split_bytes = split_kernel_bytes()
-    split_gbs = split_bytes / (split_us * 1e-6) / 1e9
+    peaks = load_peaks()
+    gbs = w.required / (us_per_call * 1e-6) / 1e9 * world
+    if w.bound == "hbm":
+        achieved = w.dominant_units / (dom_us * 1e-6) / 1e9
+        peak = peaks["hbm_gbs"]
+        per_launch = int(w.dominant_units)
+    else:
+        achieved = w.dominant_units / (dom_us * 1e-6) / 1e12
+        peak = peaks["bf16_tflops"]
+        per_launch = w.dominant_units
     line = {
         "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call",
-        "n_gpus": world, "steps": steps, "warmup": max(3, args.warmup),
+        "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": us_per_call / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": B, "q_heads": HQ, "kv_heads": HKV,
-                   "head_dim": D, "kv_len": L_TOKENS, "num_splits": ns,
-                   "parallelism": "replicas" if world > 1 else "single",
-                   "l2": f"inputs larger than L2: {NBUF} rotating K/V caches of "
-                         f"{req / 1e6:.0f} MB each", "timing": timing},
+        "config": dict(w.config(ns), parallelism="replicas" if world > 1 else "single",
+                       l2=f"inputs larger than L2: {w.nbuf} rotating input copies",
+                       timing=timing),
         "achieved_gbs": round(gbs, 1),
-        "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
-        "frac_of_measured_hbm": round(gbs / peak, 4),
+        "frac_of_nominal_8tbs": round(gbs / world / 8000.0, 4),
+        "frac_of_measured_hbm": round(gbs / world / peaks["hbm_gbs"], 4),
         "direct_call_us": round(us_direct, 3),
-        "kernels": {"split_us": round(split_us, 3), "combine_us": round(comb_us, 3)},
-        "roofline": {"bound": "hbm", "achieved": round(split_gbs, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(split_gbs / peak, 4),
-                     "traffic": None, "kernel": "split_tma_kernel<8,1>",
-                     "peak_kind": peak_kind,
-                     "bytes_per_launch": split_bytes},
+        "kernels": kern,
+        "roofline": {"bound": w.bound, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": w.unit, "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": KERNEL_NAMES[w.dominant], "peak_kind": peaks["kind"],
+                     "per_launch": per_launch, "launch_us": round(dom_us, 3)},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                    "reasons": clk["reasons"], "samples": clk["samples"]},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": int(round(launches_per_call * steps)),
     }
+    line.update(extra)
     if world == 1 and not args.no_cpu_baseline:
-        qf, kf, vf = oracle_inputs(case)
-        full_s, step_s = oracle_time_per_call(L_TOKENS, args.cpu_calls, 1, qf, kf, vf, case.scale)
-        line["cpu_baseline"] = {"value": round(full_s * 1e6, 1), "unit": "us/call",
-                                "cores": blas_threads(), "kind": "oracle",
-                                "sample": f"{args.cpu_calls} full calls of the same workload"}
+        import torch as _t
+        u, sample, dt = w.oracle_sample(args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(u, 1), "unit": "us/call", "cores": blas_threads(),
+                                "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sweep(args):
+    """--sweep-splits: per split count (and split-kernel variant, through
+    the library's FD_SPLIT_VARIANT knob), the device time per call of back-
+    to-back calls and the split kernel's event-timed launch; one JSON line
+    each.  A tuning aid, not the benchmark line."""
+    import torch
+    import decode_attention_20_b300 as fd
+    from decode_attention_20_b300 import _lib
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L = _lib.lib()
+    w = make_workload(args.workload, dev)
+    stream = torch.cuda.Stream(device=dev)
+    variants = args.sweep_variants.split(",") if args.sweep_variants else [""]
+    iters = max(10, min(args.steps, 200))
+    for var in variants:
+        if var:
+            os.environ["FD_SPLIT_VARIANT"] = var
+        else:
+            os.environ.pop("FD_SPLIT_VARIANT", None)
+        for ns in [int(x) for x in args.sweep_splits.split(",")]:
+            w.prepare(L, stream, ns)
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    w.call(i)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for i in range(iters):
+                    w.call(i)
+                e1.record(stream)
+            stream.synchronize()
+            call_us = e0.elapsed_time(e1) * 1e3 / iters
+            fd.profile_enable(True)
+            with torch.cuda.stream(stream):
+                for i in range(iters):
+                    w.call(i)
+            stream.synchronize()
+            kern = {}
+            for kind, label in [(FD_KERNEL_SPLIT, "split"), (FD_KERNEL_COMBINE, "combine"),
+                                (FD_KERNEL_BIF_CTX, "bif_ctx")]:
+                n, ms = fd.profile_read(kind)
+                if n:
+                    kern[label + "_us"] = round(ms * 1e3 / n, 3)
+            fd.profile_enable(False)
+            fd.check_device_error(stream)
+            row = {"workload": w.name, "variant": var or "default", "splits": ns,
+                   "call_us": round(call_us, 3), **kern}
+            if isinstance(w, DecodeWorkload):
+                row["split_gbs"] = round(w.dominant_units / (kern["split_us"] * 1e-6) / 1e9, 1)
+            print(json.dumps(row), flush=True)
     return 0
 
 
@@ -385,10 +688,18 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
+    ap.add_argument("--workload", default="b1_64k",
+                    choices=["b1_64k", "ragged_b32", "long_b4", "bif_mqa"])
     ap.add_argument("--num-splits", type=int, default=0)
-    ap.add_argument("--cpu-calls", type=int, default=60)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep-splits", default="",
+                    help="comma-separated split counts: print one timing line per count instead")
+    ap.add_argument("--sweep-variants", default="",
+                    help="with --sweep-splits: comma-separated FD_SPLIT_VARIANT values")
     args = ap.parse_args(argv)
+    if args.sweep_splits:
+        return run_sweep(args)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":

@@ -20,6 +20,14 @@
 
 namespace fd {
 cudaError_t read_and_clear_device_error(unsigned int* bits, cudaStream_t st);
+
+// Tokens per split of a len-token history cut into ns splits (the chunk of
+// fd_split_bounds).
+int split_chunk(int64_t len, int ns) {
+  if (ns < 1 || len <= 0) return 0;
+  const int64_t per = (len + ns - 1) / ns;
+  return (int)(((per + kSplitAlign - 1) / kSplitAlign) * kSplitAlign);
+}
 }
 
 using namespace fd;
@@ -285,10 +293,13 @@ bool tma_ok(const DecodeDesc& d, const void* kd, const void* vd, const int64_t (
 
 // Which split kernel variant to use.  Tuning and test knob, read on every
 // call: FD_SPLIT_VARIANT = "cuda" forces the CUDA-core kernel, "mma0" /
-// "mma1" / "mma2" pick a tensor-core tiling; unset = "mma0".
-int split_variant() {
+// "mma1" / "mma2" pick a tensor-core tiling.  Unset: "mma0" (6-stage ring,
+// one CTA per SM) for splits that stream more than three 64-token tiles,
+// "mma2" (3-stage ring, two CTAs per SM) for shorter ones, where a deep ring
+// cannot fill and a second resident CTA hides the start-up latency instead.
+int split_variant(int64_t chunk_tokens) {
   const char* e = getenv("FD_SPLIT_VARIANT");
-  if (e == nullptr || e[0] == 0) return 0;
+  if (e == nullptr || e[0] == 0) return chunk_tokens <= 3 * 64 ? 2 : 0;
   if (!strcmp(e, "cuda")) return -1;
   if (!strcmp(e, "mma1")) return 1;
   if (!strcmp(e, "mma2")) return 2;
@@ -369,7 +380,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   cudaError_t e = cudaSuccess;
   const int64_t kv_batch = kv_broadcast ? 1 : d.B;
   const int64_t strides[6] = {p.k_sl, p.k_sh, p.v_sl, p.v_sh, p.k_sb, p.v_sb};
-  const int variant = split_variant();
+  const int variant = split_variant(split_chunk(d.Lcap, ns));
   if (variant >= 0 && d.q_dt == FD_BF16 && mma_group_ok(d.G) &&
       d.Lcap >= mma_tile_tokens(variant) && tma_ok(d, k->data, v->data, strides, kv_batch)) {
     fd_status gs = get_encoder();
@@ -431,10 +442,12 @@ fd_status enqueue_combine(const CombineParams& cp, cudaStream_t st, bool pdl) {
 }
 
 // Context split count of the bifurcated tensor-core kernel: the fewest
-// splits that reach the smallest makespan (waves x tiles per split) when
-// `units` CTAs (M-tiles x kv heads) run per split on `num_sms` SMs, one CTA
-// per SM.
+// splits that reach the smallest makespan waves x (tiles per split + 2) when
+// `units` CTAs (query-tile pairs x kv heads) run per split on `num_sms` SMs,
+// one CTA per SM; the 2 tiles (256 tokens) charge each CTA its start-up
+// (query load, pipeline fill) and epilogue.
 int choose_ctx_splits(int64_t Lc, int64_t units, int num_sms) {
+  constexpr int64_t kCtaOverheadTiles = 2;
   const int64_t tiles = (Lc + kBifTileTokens - 1) / kBifTileTokens;
   int best_ns = 1;
   int64_t best_cost = -1;
@@ -443,7 +456,7 @@ int choose_ctx_splits(int64_t Lc, int64_t units, int num_sms) {
     const int64_t used = (tiles + per - 1) / per;        // non-empty splits
     const int64_t ctas = used * units;
     const int64_t waves = (ctas + num_sms - 1) / num_sms;
-    const int64_t cost = waves * per;
+    const int64_t cost = waves * (per + kCtaOverheadTiles);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
       best_ns = (int)used;
@@ -816,11 +829,20 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
                      (v_ctx->stride[1] * 2) % 16 == 0 && (v_ctx->stride[0] * 2) % 16 == 0 &&
                      k_ctx->stride[1] > 0 && v_ctx->stride[1] > 0 && k_ctx->stride[0] > 0 &&
                      v_ctx->stride[0] > 0;
-  const int64_t mtiles = (n * G + 127) / 128;
+  const int64_t mtiles = (n * G + 128 * kBifQueryTiles - 1) / (128 * kBifQueryTiles);
   const int ns_ctx = ctx_splits > 0 ? ctx_splits
                      : tc_ok ? choose_ctx_splits(Lc, mtiles * Hkv, info->sms)
                              : choose_splits_host(n, Hkv, Lc, info->sms);
-  const int ns_dec = Ld > 0 ? 1 : 0;
+  // Decode part: about two CTAs per SM over (sample, kv head) units, at
+  // most one 64-token tile per split.
+  int ns_dec = 0;
+  if (Ld > 0) {
+    int64_t want = (2 * (int64_t)info->sms) / (n * Hkv);
+    const int64_t cap = (Ld + 63) / 64;
+    if (want > cap) want = cap;
+    if (want > kMaxSplits) want = kMaxSplits;
+    ns_dec = want < 1 ? 1 : (int)want;
+  }
   const int S = ns_ctx + ns_dec;
   const int64_t bytes = workspace_bytes(n, Hq, D, S);
   void* ws = nullptr;
@@ -850,7 +872,11 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         bp.Lc = (int)Lc;
         bp.ns = ns_ctx;
         bp.rows = (int)(n * G);
-        bp.scale_log2 = scale * 1.4426950408889634f;
+        // A zero scale becomes 1e-30: every scaled score then rounds to an
+        // exponent of 0 in fp32 (uniform weights, as scale 0 means), while
+        // masked tail scores stay at -inf instead of 0 * inf = NaN.
+        bp.scale_log2 = scale == 0.f ? 1e-30f : std::fabs(scale) * 1.4426950408889634f;
+        bp.negate_q = scale < 0.f ? 1 : 0;
         bp.o = po;
         bp.o_sb = Hq * S * D;
         bp.o_sh = S * D;
@@ -875,14 +901,14 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
     st = enqueue_split(dc, q, k_ctx, v_ctx, nullptr, ns_ctx, scale, po, Hq * S * D, S * D, D, pl,
                        Hq * S, S, 1, true, cs);
   }
-  // Decode part: each sample's own tokens, one split, written after the
-  // context splits.
+  // Decode part: each sample's own tokens, ns_dec splits, written after
+  // the context splits.
   if (st == FD_OK && ns_dec) {
     DecodeDesc dd = {n, Hq, Hkv, D, Ld, Hq / Hkv, FD_BF16, FD_BF16};
     st = enqueue_split(dd, q, k_dec, v_dec,
-                       dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr, 1,
-                       scale, po + (int64_t)ns_ctx * D, Hq * S * D, S * D, 0, pl + ns_ctx, Hq * S,
-                       S, 0, false, cs);
+                       dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr,
+                       ns_dec, scale, po + (int64_t)ns_ctx * D, Hq * S * D, S * D, D,
+                       pl + ns_ctx, Hq * S, S, 1, false, cs);
   }
   if (st == FD_OK) {
     CombineParams cp = {};

@@ -55,15 +55,18 @@ struct CombineParams {
 struct BifCtxParams {
   int n, Hq, Hkv, G, Lc, ns;
   int rows;                   // n * G
-  float scale_log2;           // scale * log2(e)
+  float scale_log2;           // |scale| * log2(e)
+  int negate_q;               // 1: scale < 0, the kernel negates Q in the MMA
   float* o;                   // partial outputs, fp32
   int64_t o_sb, o_sh, o_ss;   // strides over (sample, q head, split)
   float* lse;                 // natural-log partial lse
   int64_t l_sb, l_sh, l_ss;
 };
 
-// Tokens per tile of the bifurcated context kernel.
+// Tokens per tile, and 128-row query tiles per CTA, of the bifurcated
+// context kernel.
 constexpr int kBifTileTokens = 128;
+constexpr int kBifQueryTiles = 2;
 
 // Host launchers (return a cudaError_t from the launch).
 cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,

@@ -112,3 +112,14 @@ def test_bifurcated_peaked_context(cuda_device, ctx_path, ctx_splits):
     O_ref, L_ref = _ref(case)
     assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16,
                   f"{ctx_path} peaked ns={ctx_splits}")
+
+
+@pytest.mark.parametrize("scale", [-0.07, 0.0, 0.3])
+def test_bifurcated_scale_sign_and_zero(cuda_device, ctx_path, scale):
+    """A negative scale (the tensor-core path negates Q in the MMA), a zero
+    scale (uniform weights) and a large one."""
+    case = inputs.bifurcated_case(6, 16, 1, 128, 700, 20, seed=91, ragged_dec=(0, 20),
+                                  scale=scale)
+    O, L = _run(case)
+    O_ref, L_ref = _ref(case)
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16, f"{ctx_path} scale={scale}")
