@@ -53,6 +53,38 @@ KERNEL_NAMES = {FD_KERNEL_SPLIT: "split_mma_kernel (mma.sync bf16, TMA ring)",
                 FD_KERNEL_BIF_CTX: "bif_ctx_kernel (tcgen05.mma, TMEM accumulators)"}
 
 
+# Source files each roofline kernel is built from: a DRAM-traffic figure in
+# profiles/traffic.json is used only while these files hash to the value it
+# was captured with (otherwise the kernel has changed and traffic is null).
+KERNEL_SOURCES = {
+    FD_KERNEL_SPLIT: ["fd_split_mma.cuh", "fd_split.cuh", "fd_device.cuh"],
+    FD_KERNEL_BIF_CTX: ["fd_bif_ctx.cuh", "fd_tcgen05.cuh", "fd_split.cuh", "fd_device.cuh"],
+}
+
+
+def kernel_source_hash(kind):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, "decode_attention_20_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kind, workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when none matches this workload and source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        table = json.load(f)
+    e = table.get(f"{kind}:{workload}")
+    if not e or e.get("source_hash") != kernel_source_hash(kind):
+        return None
+    return int(e["dram_bytes_per_launch"])
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -609,7 +641,8 @@ def run_fd(args, rank, world):
         "direct_call_us": round(us_direct, 3),
         "kernels": kern,
         "roofline": {"bound": w.bound, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": w.unit, "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": w.unit, "frac": round(achieved / peak, 4),
+                     "traffic": measured_traffic(w.dominant, w.short),
                      "kernel": KERNEL_NAMES[w.dominant], "peak_kind": peaks["kind"],
                      "per_launch": per_launch, "launch_us": round(dom_us, 3)},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],

@@ -393,7 +393,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
                                  p.v_sh, tile, 64);
     if (okk && okv) {
       const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
-      e = launch_split_mma(p, tmK, tmV, (int)d.G, variant, st, &launched);
+      e = launch_split_mma(p, tmK, tmV, (int)d.G, variant, st, &launched, !prof);
       prof_end(FD_KERNEL_SPLIT, st, prof && launched, rec);
       if (prof && !launched) {
         std::lock_guard<std::mutex> lock(g_prof_mu);
@@ -412,7 +412,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
                                  p.v_sh, kSplitTileTokens);
     if (okk && okv) {
       const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
-      e = launch_split_tma(p, tmK, tmV, (int)d.D, (int)d.G, st, &launched);
+      e = launch_split_tma(p, tmK, tmV, (int)d.D, (int)d.G, st, &launched, !prof);
       prof_end(FD_KERNEL_SPLIT, st, prof && launched, rec);
       if (prof && !launched) {
         std::lock_guard<std::mutex> lock(g_prof_mu);
@@ -423,7 +423,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   }
   if (!launched) {
     const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
-    e = launch_split_generic(p, (int)d.D, d.kv_dt == FD_BF16, st);
+    e = launch_split_generic(p, (int)d.D, d.kv_dt == FD_BF16, st, !prof);
     prof_end(FD_KERNEL_SPLIT, st, prof, rec);
     if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
   }
@@ -442,12 +442,12 @@ fd_status enqueue_combine(const CombineParams& cp, cudaStream_t st, bool pdl) {
 }
 
 // Context split count of the bifurcated tensor-core kernel: the fewest
-// splits that reach the smallest makespan waves x (tiles per split + 2) when
+// splits that reach the smallest makespan waves x (tiles per split + 4) when
 // `units` CTAs (query-tile pairs x kv heads) run per split on `num_sms` SMs,
-// one CTA per SM; the 2 tiles (256 tokens) charge each CTA its start-up
+// one CTA per SM; the 4 tiles (256 tokens) charge each CTA its start-up
 // (query load, pipeline fill) and epilogue.
 int choose_ctx_splits(int64_t Lc, int64_t units, int num_sms) {
-  constexpr int64_t kCtaOverheadTiles = 2;
+  constexpr int64_t kCtaOverheadTiles = 4;
   const int64_t tiles = (Lc + kBifTileTokens - 1) / kBifTileTokens;
   int best_ns = 1;
   int64_t best_cost = -1;
@@ -887,7 +887,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         bp.l_ss = 1;
         ProfRecord rec;
         const bool prof = prof_begin(FD_KERNEL_BIF_CTX, cs, &rec);
-        e = launch_bif_ctx(bp, tmQ, tmK, tmV, (int)mtiles, cs);
+        e = launch_bif_ctx(bp, tmQ, tmK, tmV, (int)mtiles, cs, !prof);
         prof_end(FD_KERNEL_BIF_CTX, cs, prof, rec);
         if (e != cudaSuccess) st = cuda_fail(e, "bifurcated context kernel launch");
         ctx_done = true;

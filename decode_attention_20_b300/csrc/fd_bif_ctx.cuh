@@ -19,26 +19,33 @@
 //
 // CTA = two 128-row query tiles (256 rows) x one context split x one kv head;
 // 10 warps:
-//   warp 0      TMA producer: both Q tiles once, then K and V tiles of 128
-//               tokens into separate 2-stage rings, 128-byte swizzle (two
+//   warp 0      TMA producer: both Q tiles once, then K and V tiles of 64
+//               tokens into separate 4-stage rings, 128-byte swizzle (two
 //               64-column boxes per tile).  Every K/V tile feeds both Q tiles.
 //   warp 1      allocates all 512 TMEM columns; one thread issues every MMA.
-//               TMEM: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each.
-//                 S_t  = Q_t K_j^T               (A, B from shared memory)
-//                 O_t += P_t V_j                 (A = P_t from TMEM, B = V
-//                                                 from shared memory, MN-major)
-//               P_t (bf16 pairs, 64 columns) overwrites the first half of S_t.
+//               TMEM: for each query tile t two score buffers S_t[0], S_t[1]
+//               (64 fp32 columns each, columns 128 t + 64 b) and the output
+//               accumulator O_t (128 columns at 256 + 128 t).
+//                 S_t[j % 2]  = Q_t K_j^T        (A, B from shared memory)
+//                 O_t        += P_t,j V_j        (A = P from TMEM, B = V from
+//                                                 shared memory, MN-major)
+//               P_t,j (bf16 pairs, 32 columns) overwrites the first half of
+//               the score buffer it was computed from.
 //   warps 2..5  softmax of query tile 0, warps 6..9 softmax of query tile 1:
-//               thread = one row (its TMEM lane).  Reads the row of S_t,
+//               thread = one row (its TMEM lane).  Reads the row of S_t,j,
 //               keeps the running max m / sum l in base 2, writes the bf16
 //               probabilities back into TMEM, and rescales O_t on the rare
 //               tiles where the running max grows by more than 8 (lazy
 //               rescale; p <= 256 always; numerator and denominator share m).
-// The two tiles ping-pong: while one warpgroup runs its softmax, the tensor
-// core runs the other tile's P V and next Q K^T.  Ordering needs no extra
-// waits: the MMAs of one thread execute in issue order, and the barrier that
-// signals "S_t of tile j is ready" is committed after O_t += P_t V_{j-1}, so
-// when a softmax warp sees S_t it may also rescale O_t and overwrite P_t.
+// Score buffers are double-buffered, so the tensor core computes S_t,j+1 while
+// the softmax warps work on S_t,j, and the two query tiles interleave their
+// P V products.  The MMAs of one thread execute in issue order: S_t,j+2 is
+// issued after O_t += P_t,j V_j and so never overwrites P_t,j before it is
+// read.  A rescale of O_t before tile j waits for O_t += P_t,j-1 V_j-1
+// (o_done[t]).  The softmax warps may run two tiles ahead of the MMA issuer,
+// so "P ready" and "S ready" barriers exist per score buffer: each completes
+// once per use of its buffer, and a buffer is reused only after its previous
+// barrier phase has been consumed.
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees its tensor memory and returns with the device error flag set.
 #pragma once
@@ -64,28 +71,30 @@ struct BifCfg {
   static constexpr int ROWS = MT * NQ;          // rows per CTA
   static constexpr int D = 128;                 // head dim
   static constexpr int TN = kBifTileTokens;     // tokens per K/V tile
-  static constexpr int NK = 2;                  // K stages
-  static constexpr int NV = 2;                  // V stages
+  static constexpr int NK = 4;                  // K stages
+  static constexpr int NV = 4;                  // V stages
   static constexpr int NSW = 4 * NQ;            // softmax warps
   static constexpr int THREADS = 64 + NSW * 32;
-  static constexpr int CHUNK_BYTES = 128 * 128; // 128 rows x 64 bf16 (one swizzled box)
-  static constexpr int Q_BYTES = 2 * CHUNK_BYTES;       // one query tile
-  static constexpr int KV_BYTES = 2 * TN * 128;         // one K or V tile (two boxes)
+  static constexpr int Q_CHUNK = 128 * 128;     // 128 rows x 64 bf16 (one swizzled box)
+  static constexpr int Q_BYTES = 2 * Q_CHUNK;   // one query tile
+  static constexpr int KV_CHUNK = TN * 128;     // TN rows x 64 bf16
+  static constexpr int KV_BYTES = 2 * KV_CHUNK; // one K or V tile (two boxes)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
   // barriers: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-  // s_full[NQ], p_full[NQ], o_done, drain
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NQ + 2;
+  // s_full[NQ][2], p_full[NQ][2], o_done[NQ], drain
+  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NQ + 2 * NQ + NQ + 1;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0;          // + t * 128
-  static constexpr uint32_t COL_O = 256;        // + t * 128
-  static_assert(TN == 128, "score buffers are laid out for 128-token tiles");
-  static_assert(NQ == 2, "TMEM holds two score and two output tiles");
+  static constexpr uint32_t COL_S = 0;          // + 128 t + 64 b
+  static constexpr uint32_t COL_O = 256;        // + 128 t
+  static_assert(TN == 64, "score buffers are laid out for 64-token tiles");
+  static_assert(NQ == 2, "TMEM holds two query tiles");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
   static_assert(NQ * MT * (D + 4) * 4 <= OFF_BAR, "epilogue staging fits the operand buffers");
+  static_assert(MT * (D + 4) * 4 <= OFF_V, "tile 0 stages below the V ring");
 };
 
 // Context split i of ns over [0, Lc): whole 128-token tiles.
@@ -101,6 +110,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     bif_ctx_kernel(const __grid_constant__ BifCtxParams p, const __grid_constant__ CUtensorMap tmQ,
                    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = BifCfg;
+  pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -110,10 +120,10 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   uint64_t* k_empty = k_full + C::NK;
   uint64_t* v_full = k_empty + C::NK;
   uint64_t* v_empty = v_full + C::NV;
-  uint64_t* s_full = v_empty + C::NV;
-  uint64_t* p_full = s_full + C::NQ;
-  uint64_t* o_done = p_full + C::NQ;
-  uint64_t* drain = o_done + 1;
+  uint64_t* s_full = v_empty + C::NV;           // [NQ][2]
+  uint64_t* p_full = s_full + 2 * C::NQ;        // [NQ][2]
+  uint64_t* o_done = p_full + 2 * C::NQ;
+  uint64_t* drain = o_done + C::NQ;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_s = reinterpret_cast<int*>(taddr_s + 1);
 
@@ -143,7 +153,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
-      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + C::NQ);
+      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + 2 * C::NQ);
       mbar_init(&bars[i], is_p ? 128 : 1);
     }
     *abort_s = 0;
@@ -170,7 +180,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
         const int s0 = (mtile * C::NQ + t) * samples_per_qtile;
         unsigned char* dst = smem + C::OFF_Q + t * C::Q_BYTES;
         tma_load_3d(dst, &tmQ, q_full, 0, g * p.G, s0);
-        tma_load_3d(dst + C::CHUNK_BYTES, &tmQ, q_full, 64, g * p.G, s0);
+        tma_load_3d(dst + C::Q_CHUNK, &tmQ, q_full, 64, g * p.G, s0);
       }
       int kt = 0, vt = 0;                           // next K / V tile to issue
       bool ok = true;
@@ -184,7 +194,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
           const int tok = begin + kt * C::TN;
           tma_load_3d(dst, &tmK, &k_full[st], 0, g, tok);
-          tma_load_3d(dst + C::KV_BYTES / 2, &tmK, &k_full[st], 64, g, tok);
+          tma_load_3d(dst + C::KV_CHUNK, &tmK, &k_full[st], 64, g, tok);
           ++kt;
         }
         if (vt < ntiles && vt < kt) {
@@ -195,7 +205,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
           const int tok = begin + vt * C::TN;
           tma_load_3d(dst, &tmV, &v_full[st], 0, g, tok);
-          tma_load_3d(dst + C::KV_BYTES / 2, &tmV, &v_full[st], 64, g, tok);
+          tma_load_3d(dst + C::KV_CHUNK, &tmV, &v_full[st], 64, g, tok);
           ++vt;
         }
       }
@@ -215,58 +225,62 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           tc::idesc_bf16_f32(C::MT, C::TN, false, false) | (p.negate_q ? (1u << 13) : 0u);
       constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(C::MT, C::D, false, true);
       bool ok = mbar_wait_or_abort(q_full, 0, abort_s);
-      // S_t = Q_t K_j^T (8 MMAs of K = 16 head dims).
+      // S_t[j % 2] = Q_t K_j^T (8 MMAs of K = 16 head dims).
       auto issue_s = [&](int t, int j) {
         const uint32_t q_addr = sbase + C::OFF_Q + t * C::Q_BYTES;
         const uint32_t k_addr = sbase + C::OFF_K + (j % C::NK) * C::KV_BYTES;
+        const uint32_t d_tmem = tmem + C::COL_S + t * 128 + (j & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          tc::mma_bf16_ss(tmem + C::COL_S + t * 128, tc::smem_desc_sw128(q_addr + off, 16, 1024),
-                          tc::smem_desc_sw128(k_addr + off, 16, 1024), IDESC_S, kk > 0);
+          const uint32_t qoff = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
+          tc::mma_bf16_ss(d_tmem, tc::smem_desc_sw128(q_addr + qoff, 16, 1024),
+                          tc::smem_desc_sw128(k_addr + koff, 16, 1024), IDESC_S, kk > 0);
         }
-        tc::commit(&s_full[t]);
+        tc::commit(&s_full[t * 2 + (j & 1)]);
       };
-      // O_t += P_t V_j (8 MMAs of K = 16 tokens; P_t from TMEM columns
-      // COL_S + t*128 + 8 kk, V MN-major: 16 token rows at 16 kk, two
-      // 64-wide head-dim blocks KV_BYTES/2 apart).
+      // O_t += P_t,j V_j (4 MMAs of K = 16 tokens; P from the TMEM columns
+      // of S_t[j % 2], 8 per MMA; V MN-major: 16 token rows at 16 kk, two
+      // 64-wide head-dim blocks KV_CHUNK apart).
       auto issue_pv = [&](int t, int j) {
         const uint32_t v_addr = sbase + C::OFF_V + (j % C::NV) * C::KV_BYTES;
+        const uint32_t a_tmem = tmem + C::COL_S + t * 128 + (j & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < C::TN / 16; ++kk)
-          tc::mma_bf16_ts(tmem + C::COL_O + t * 128, tmem + C::COL_S + t * 128 + kk * 8,
-                          tc::smem_desc_sw128(v_addr + kk * 16 * 128, C::KV_BYTES / 2, 1024),
+          tc::mma_bf16_ts(tmem + C::COL_O + t * 128, a_tmem + kk * 8,
+                          tc::smem_desc_sw128(v_addr + kk * 16 * 128, C::KV_CHUNK, 1024),
                           IDESC_O, (j > 0) || (kk > 0));
+        tc::commit(&o_done[t]);
       };
-      if (ok) ok = mbar_wait_or_abort(&k_full[0], 0, abort_s);
-      if (ok) {
+      // Prologue: scores of tiles 0 and 1 for both query tiles.
+      for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
+        if (!mbar_wait_or_abort(&k_full[j % C::NK], (j / C::NK) & 1, abort_s)) { ok = false; break; }
         tc::fence_after_sync();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        tc::commit(&k_empty[0]);
+        issue_s(0, j);
+        issue_s(1, j);
+        tc::commit(&k_empty[j % C::NK]);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        const bool more = j + 1 < ntiles;
+        const bool more = j + 2 < ntiles;
         if (!mbar_wait_or_abort(&v_full[j % C::NV], (j / C::NV) & 1, abort_s)) break;
-        // tile 0: O_0 += P_0 V_j, then S_0 for tile j+1
-        if (!mbar_wait_or_abort(&p_full[0], j & 1, abort_s)) break;
+        // query tile 0: O_0 += P_0,j V_j, then S_0 of tile j+2
+        if (!mbar_wait_or_abort(&p_full[0 * 2 + (j & 1)], (j >> 1) & 1, abort_s)) break;
         tc::fence_after_sync();
         issue_pv(0, j);
         if (more) {
-          if (!mbar_wait_or_abort(&k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1, abort_s)) break;
-          issue_s(0, j + 1);
+          if (!mbar_wait_or_abort(&k_full[(j + 2) % C::NK], ((j + 2) / C::NK) & 1, abort_s)) break;
+          issue_s(0, j + 2);
         }
-        // tile 1: O_1 += P_1 V_j, then S_1 for tile j+1
-        if (!mbar_wait_or_abort(&p_full[1], j & 1, abort_s)) break;
+        // query tile 1: O_1 += P_1,j V_j, then S_1 of tile j+2
+        if (!mbar_wait_or_abort(&p_full[1 * 2 + (j & 1)], (j >> 1) & 1, abort_s)) break;
         tc::fence_after_sync();
         issue_pv(1, j);
         tc::commit(&v_empty[j % C::NV]);
         if (more) {
-          issue_s(1, j + 1);
-          tc::commit(&k_empty[(j + 1) % C::NK]);
+          issue_s(1, j + 2);
+          tc::commit(&k_empty[(j + 2) % C::NK]);
         }
       }
-      tc::commit(o_done);
       // Drain: every MMA issued above completes before the TMEM is freed.
       tc::commit(drain);
       mbar_wait_bounded(drain, 0);
@@ -277,7 +291,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;               // row of the query tile
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t s_tmem = tmem + lane_base + C::COL_S + t * 128;
+    const uint32_t s_tmem0 = tmem + lane_base + C::COL_S + t * 128;
     const uint32_t o_tmem = tmem + lane_base + C::COL_O + t * 128;
     float m_run = kNegInf, l_run = 0.f;
     bool ok = true;
@@ -286,18 +300,19 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     // row maximum of the scaled scores is scale_log2 times the raw maximum.
     const float c2 = p.scale_log2;
     for (int j = 0; j < ntiles; ++j) {
+      const uint32_t s_tmem = s_tmem0 + (j & 1) * 64;
       // Waits are made warp-uniform before any .sync.aligned tcgen05 access.
-      const bool got = mbar_wait_or_abort(&s_full[t], j & 1, abort_s);
+      const bool got = mbar_wait_or_abort(&s_full[t * 2 + (j & 1)], (j >> 1) & 1, abort_s);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc::fence_after_sync();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, sr[c]);
+      uint32_t sr[2][32];
+      tc::tmem_ld32(s_tmem, sr[0]);
+      tc::tmem_ld32(s_tmem + 32, sr[1]);
       tc::tmem_wait_ld();
       const int nvalid = min(C::TN, end - (begin + j * C::TN));
       if (nvalid < C::TN) {                        // tail tile only (uniform branch)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (c * 32 + i >= nvalid) sr[c][i] = __float_as_uint(kNegInf);
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = kNegInf;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
 #pragma unroll
@@ -316,11 +331,11 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
       const float m_new = (mx > m_run + 8.f) ? mx : m_run;
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
       const float m_use = (m_new == kNegInf) ? 0.f : m_new;   // all -inf: p = 0, not NaN
-      // p = 2^(s * c2 - m); P_t as bf16 pairs (even token in the low half)
-      // packed in place and stored into the first 64 columns of S_t.
+      // p = 2^(s * c2 - m); P as bf16 pairs (even token in the low half)
+      // packed in place and stored into the first 32 columns of the buffer.
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i]), c2, -m_use));
@@ -332,10 +347,12 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
         }
         tc::tmem_st16(s_tmem + c * 16, sr[c]);
       }
-      // O_t += P_t V_{j-1} is complete (it was issued before S_t of tile j):
-      // rescale O_t where its max moved (after P, so the score registers are
-      // free again).
+      // Rescale O_t where its max moved, once O_t += P_t,j-1 V_j-1 is done
+      // (rare: the running max grew by more than 8).
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const bool got_o = mbar_wait_or_abort(&o_done[t], (j - 1) & 1, abort_s);
+        if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
+        tc::fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orr[32];
@@ -349,16 +366,24 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(&p_full[t]);
+      mbar_arrive(&p_full[t * 2 + (j & 1)]);
       l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m_run = m_new;
     }
     // ------------------------------------------------------------ epilogue
-    // Every MMA has completed once o_done fires, so the Q / K / V buffers are
-    // free: each row owner normalises its O row into a padded staging tile
-    // there, then each warp writes whole rows (512 contiguous bytes per store
-    // instruction) instead of 32 rows at once.
-    const bool got_last = ok && mbar_wait_or_abort(o_done, 0, abort_s);
+    // Once this tile's last P V has completed, so has every MMA issued
+    // before it (all score MMAs included), and the Q and K buffers are dead.
+    // Tile 0 stages in [0, 66 KB), which only the Q and K buffers occupy (the
+    // other tile's last P V may still read the V ring); tile 1's last P V is
+    // the last MMA of the CTA.  Each row owner normalises its O row into the
+    // padded staging tile, then each warp writes whole rows (512 contiguous
+    // bytes per store instruction) instead of 32 rows at once.
+    // o_done[t] completes once per P V of this tile.  Seeing S of the last
+    // tile only guarantees the P V two tiles earlier, so wait for the last
+    // two phases in order (a parity wait must not fall two phases behind).
+    bool got_last = ok;
+    if (got_last && ntiles >= 2) got_last = mbar_wait_or_abort(&o_done[t], (ntiles - 2) & 1, abort_s);
+    if (got_last) got_last = mbar_wait_or_abort(&o_done[t], (ntiles - 1) & 1, abort_s);
     const bool done = __all_sync(0xffffffffu, got_last);
     constexpr int SROW = C::D + 4;                            // padded row (floats)
     float* stage = reinterpret_cast<float*>(smem) + t * (C::MT * SROW);

@@ -23,7 +23,7 @@
 //           the SG group sums are added through shared memory.
 // Launched with programmatic stream serialisation behind the split kernel:
 // the launch overlaps its tail, and griddepcontrol.wait orders the reads
-// after the partial writes.
+// after the partial writes.  It lets its own dependents launch at once.
 #pragma once
 
 #include "fd_device.cuh"
@@ -42,6 +42,9 @@ __global__ void __launch_bounds__(kCombineThreads)
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int row = blockIdx.x;
+  // The next kernel on the stream (the next call's split kernel, launched
+  // with PDL) may start now: it waits for this grid before touching memory.
+  pdl_launch_dependents();
   pdl_wait_prerequisites();
   if (row >= p.R1 * p.R2) return;
   const int r1 = row / p.R2;

@@ -65,21 +65,23 @@ struct BifCtxParams {
 
 // Tokens per tile, and 128-row query tiles per CTA, of the bifurcated
 // context kernel.
-constexpr int kBifTileTokens = 128;
+constexpr int kBifTileTokens = 64;
 constexpr int kBifQueryTiles = 2;
 
-// Host launchers (return a cudaError_t from the launch).
+// Host launchers (return a cudaError_t from the launch).  `pdl` launches
+// with programmatic stream serialisation (the kernel may start while the
+// previous kernel on the stream drains; it waits before touching memory).
 cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
                              const CUtensorMap& tmV, int D, int G, cudaStream_t st,
-                             bool* launched);
+                             bool* launched, bool pdl);
 cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             int G, int variant, cudaStream_t st, bool* launched);
+                             int G, int variant, cudaStream_t st, bool* launched, bool pdl);
 int mma_tile_tokens(int variant);
-cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16,
-                                 cudaStream_t st);
+cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaStream_t st,
+                                 bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, int mtiles, cudaStream_t st);
+                           const CUtensorMap& tmV, int mtiles, cudaStream_t st, bool pdl);
 
 // Tile height (tokens) of the TMA split kernel; the tensor-map box uses it.
 constexpr int kSplitTileTokens = 64;

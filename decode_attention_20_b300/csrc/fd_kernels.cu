@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "fd_combine.cuh"
 #include "fd_internal.h"
 #include "fd_split.cuh"
@@ -11,6 +13,26 @@
 #include "fd_bif_ctx.cuh"
 
 namespace fd {
+
+// Launch with cudaLaunchKernelEx; `pdl` adds programmatic stream
+// serialisation, so the grid may start while the previous kernel on the
+// stream finishes (every kernel here executes griddepcontrol.wait before its
+// first global-memory access).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 cudaError_t read_and_clear_device_error(unsigned int* bits, cudaStream_t st) {
   unsigned int zero = 0u;
@@ -27,7 +49,7 @@ cudaError_t read_and_clear_device_error(unsigned int* bits, cudaStream_t st) {
 
 template <int GH, int HC>
 static cudaError_t launch_tma_variant(const SplitParams& p, const CUtensorMap& tmK,
-                                      const CUtensorMap& tmV, cudaStream_t st) {
+                                      const CUtensorMap& tmV, cudaStream_t st, bool pdl) {
   using C = TmaCfg<GH, HC>;
   auto kern = split_tma_kernel<GH, HC>;
   // The shared-memory opt-in is per (function, device): remember it per device.
@@ -41,32 +63,31 @@ static cudaError_t launch_tma_variant(const SplitParams& p, const CUtensorMap& t
     if (e != cudaSuccess) return e;
     attr_set |= bit;
   }
-  dim3 grid(p.ns, p.Hkv, p.B);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
-  return cudaGetLastError();
+  return launch_ex(kern, dim3(p.ns, p.Hkv, p.B), dim3(C::THREADS), C::SMEM_BYTES, st, pdl, p,
+                   tmK, tmV);
 }
 
 cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
                              const CUtensorMap& tmV, int D, int G, cudaStream_t st,
-                             bool* launched) {
+                             bool* launched, bool pdl) {
   *launched = false;
   if (D != 128) return cudaSuccess;
   *launched = true;
   switch (G) {
-    case 1: return launch_tma_variant<1, 1>(p, tmK, tmV, st);
-    case 2: return launch_tma_variant<2, 1>(p, tmK, tmV, st);
-    case 4: return launch_tma_variant<4, 1>(p, tmK, tmV, st);
-    case 8: return launch_tma_variant<8, 1>(p, tmK, tmV, st);
-    case 16: return launch_tma_variant<8, 2>(p, tmK, tmV, st);
-    case 32: return launch_tma_variant<8, 4>(p, tmK, tmV, st);
-    case 64: return launch_tma_variant<8, 8>(p, tmK, tmV, st);
+    case 1: return launch_tma_variant<1, 1>(p, tmK, tmV, st, pdl);
+    case 2: return launch_tma_variant<2, 1>(p, tmK, tmV, st, pdl);
+    case 4: return launch_tma_variant<4, 1>(p, tmK, tmV, st, pdl);
+    case 8: return launch_tma_variant<8, 1>(p, tmK, tmV, st, pdl);
+    case 16: return launch_tma_variant<8, 2>(p, tmK, tmV, st, pdl);
+    case 32: return launch_tma_variant<8, 4>(p, tmK, tmV, st, pdl);
+    case 64: return launch_tma_variant<8, 8>(p, tmK, tmV, st, pdl);
     default: *launched = false; return cudaSuccess;
   }
 }
 
 template <int NT, int WN, int W, int T, int NSTAGE>
 static cudaError_t launch_mma_variant(const SplitParams& p, const CUtensorMap& tmK,
-                                      const CUtensorMap& tmV, cudaStream_t st) {
+                                      const CUtensorMap& tmV, cudaStream_t st, bool pdl) {
   using C = MmaCfg<NT, WN, W, T, NSTAGE>;
   auto kern = split_mma_kernel<NT, WN, W, T, NSTAGE>;
   static unsigned long long attr_set = 0ull;
@@ -79,38 +100,37 @@ static cudaError_t launch_mma_variant(const SplitParams& p, const CUtensorMap& t
     if (e != cudaSuccess) return e;
     attr_set |= bit;
   }
-  dim3 grid(p.ns, p.Hkv, p.B);
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p, tmK, tmV);
-  return cudaGetLastError();
+  return launch_ex(kern, dim3(p.ns, p.Hkv, p.B), dim3(C::THREADS), C::SMEM_BYTES, st, pdl, p,
+                   tmK, tmV);
 }
 
 int mma_tile_tokens(int variant) { return variant == 1 ? 128 : 64; }
 
 cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             int G, int variant, cudaStream_t st, bool* launched) {
+                             int G, int variant, cudaStream_t st, bool* launched, bool pdl) {
   *launched = true;
   if (variant == 1) {            // 8 warps, 128-token tiles, 3 stages
     switch (G) {
-      case 4: case 8: return launch_mma_variant<1, 1, 8, 128, 3>(p, tmK, tmV, st);
-      case 16: return launch_mma_variant<2, 1, 8, 128, 3>(p, tmK, tmV, st);
-      case 32: return launch_mma_variant<4, 2, 8, 128, 3>(p, tmK, tmV, st);
-      case 64: return launch_mma_variant<8, 4, 8, 128, 3>(p, tmK, tmV, st);
+      case 4: case 8: return launch_mma_variant<1, 1, 8, 128, 3>(p, tmK, tmV, st, pdl);
+      case 16: return launch_mma_variant<2, 1, 8, 128, 3>(p, tmK, tmV, st, pdl);
+      case 32: return launch_mma_variant<4, 2, 8, 128, 3>(p, tmK, tmV, st, pdl);
+      case 64: return launch_mma_variant<8, 4, 8, 128, 3>(p, tmK, tmV, st, pdl);
       default: break;
     }
   } else if (variant == 2) {     // 4 warps, 64-token tiles, 3 stages (two CTAs per SM)
     switch (G) {
-      case 4: case 8: return launch_mma_variant<1, 1, 4, 64, 3>(p, tmK, tmV, st);
-      case 16: return launch_mma_variant<2, 1, 4, 64, 3>(p, tmK, tmV, st);
-      case 32: return launch_mma_variant<4, 2, 4, 64, 3>(p, tmK, tmV, st);
-      case 64: return launch_mma_variant<8, 4, 4, 64, 3>(p, tmK, tmV, st);
+      case 4: case 8: return launch_mma_variant<1, 1, 4, 64, 3>(p, tmK, tmV, st, pdl);
+      case 16: return launch_mma_variant<2, 1, 4, 64, 3>(p, tmK, tmV, st, pdl);
+      case 32: return launch_mma_variant<4, 2, 4, 64, 3>(p, tmK, tmV, st, pdl);
+      case 64: return launch_mma_variant<8, 4, 4, 64, 3>(p, tmK, tmV, st, pdl);
       default: break;
     }
   } else {                       // 4 warps, 64-token tiles, 6 stages
     switch (G) {
-      case 4: case 8: return launch_mma_variant<1, 1, 4, 64, 6>(p, tmK, tmV, st);
-      case 16: return launch_mma_variant<2, 1, 4, 64, 6>(p, tmK, tmV, st);
-      case 32: return launch_mma_variant<4, 2, 4, 64, 6>(p, tmK, tmV, st);
-      case 64: return launch_mma_variant<8, 4, 4, 64, 6>(p, tmK, tmV, st);
+      case 4: case 8: return launch_mma_variant<1, 1, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 16: return launch_mma_variant<2, 1, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 32: return launch_mma_variant<4, 2, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 64: return launch_mma_variant<8, 4, 4, 64, 6>(p, tmK, tmV, st, pdl);
       default: break;
     }
   }
@@ -118,37 +138,26 @@ cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const
   return cudaSuccess;
 }
 
-cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaStream_t st) {
-  dim3 grid(p.ns, p.Hq, p.B);
+cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaStream_t st,
+                                 bool pdl) {
+  const dim3 grid(p.ns, p.Hq, p.B);
   if (D == 128) {
-    if (kv_bf16) split_generic_kernel<128, true><<<grid, 128, 0, st>>>(p);
-    else split_generic_kernel<128, false><<<grid, 128, 0, st>>>(p);
-  } else if (D == 64) {
-    if (kv_bf16) split_generic_kernel<64, true><<<grid, 128, 0, st>>>(p);
-    else split_generic_kernel<64, false><<<grid, 128, 0, st>>>(p);
-  } else {
-    return cudaErrorInvalidValue;
+    if (kv_bf16) return launch_ex(split_generic_kernel<128, true>, grid, dim3(128), 0, st, pdl, p);
+    return launch_ex(split_generic_kernel<128, false>, grid, dim3(128), 0, st, pdl, p);
   }
-  return cudaGetLastError();
+  if (D == 64) {
+    if (kv_bf16) return launch_ex(split_generic_kernel<64, true>, grid, dim3(128), 0, st, pdl, p);
+    return launch_ex(split_generic_kernel<64, false>, grid, dim3(128), 0, st, pdl, p);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
-  const int rows = p.R1 * p.R2;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(rows);
-  cfg.blockDim = dim3(kCombineThreads);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, lse_combine_kernel, p);
+  return launch_ex(lse_combine_kernel, dim3(p.R1 * p.R2), dim3(kCombineThreads), 0, st, pdl, p);
 }
 
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, int mtiles, cudaStream_t st) {
+                           const CUtensorMap& tmV, int mtiles, cudaStream_t st, bool pdl) {
   static unsigned long long attr_set = 0ull;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -160,9 +169,8 @@ cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmQ, const 
     if (e != cudaSuccess) return e;
     attr_set |= bit;
   }
-  dim3 grid(mtiles, p.ns, p.Hkv);
-  bif_ctx_kernel<<<grid, BifCfg::THREADS, BifCfg::SMEM_BYTES, st>>>(p, tmQ, tmK, tmV);
-  return cudaGetLastError();
+  return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
+                   BifCfg::SMEM_BYTES, st, pdl, p, tmQ, tmK, tmV);
 }
 
 }  // namespace fd

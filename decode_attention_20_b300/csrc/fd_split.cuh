@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
   using C = TmaCfg<GH, HC>;
+  pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -416,6 +417,7 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
 
 template <int D, bool KV_BF16>
 __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constant__ SplitParams p) {
+  pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   constexpr int NW = 4;
   constexpr int EPL = D / 32;
   __shared__ float ml_s[NW][2];

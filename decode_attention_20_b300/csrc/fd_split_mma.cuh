@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(W * 32, 1)
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
   using C = MmaCfg<NT, WN, W, T, NSTAGE>;
+  pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   constexpr int NPW = C::NPW;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
