@@ -369,6 +369,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   p.o_sb = o_sb;
   p.o_sh = o_sh;
   p.o_ss = o_ss;
+  p.o_vec4 = aligned16(o) && o_sb % 4 == 0 && o_sh % 4 == 0 && o_ss % 4 == 0;
   p.lse = lse;
   p.l_sb = l_sb;
   p.l_sh = l_sh;
@@ -818,10 +819,10 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   if (n == 0 || Hq == 0) return FD_OK;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
 
-  // Tensor-core context path: head dim 128, group size dividing 128,
-  // 16-byte aligned bases and strides.
+  // Tensor-core context path: head dim 128, 16-byte aligned bases and
+  // strides (query rows are read as 16-byte vectors, K/V through TMA).
   const int64_t G = Hq / Hkv;
-  const bool tc_ok = bif_ctx_tensor_core_allowed() && D == 128 && G <= 128 && 128 % G == 0 &&
+  const bool tc_ok = bif_ctx_tensor_core_allowed() && D == 128 &&
                      aligned16(q->data) && aligned16(k_ctx->data) && aligned16(v_ctx->data) &&
                      (q->stride[1] * 2) % 16 == 0 && (q->stride[0] * 2) % 16 == 0 &&
                      q->stride[1] > 0 && (q->stride[0] > 0 || n == 1) &&
@@ -856,15 +857,16 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   if (tc_ok) {
     // Context part on the tensor cores: rows (sample, head of the group).
     if ((st = get_encoder()) == FD_OK) {
-      CUtensorMap tmQ, tmK, tmV;
-      const bool okq = make_3d_map(&tmQ, q->data, D, Hq, n, q->stride[1], q->stride[0], (int)G,
-                                   (int)(128 / G));
+      CUtensorMap tmK, tmV;
       const bool okk = make_3d_map(&tmK, k_ctx->data, D, Hkv, Lc, k_ctx->stride[1],
                                    k_ctx->stride[0], 1, kBifTileTokens);
       const bool okv = make_3d_map(&tmV, v_ctx->data, D, Hkv, Lc, v_ctx->stride[1],
                                    v_ctx->stride[0], 1, kBifTileTokens);
-      if (okq && okk && okv) {
+      if (okk && okv) {
         BifCtxParams bp = {};
+        bp.q = reinterpret_cast<const uint16_t*>(q->data);
+        bp.q_sb = q->stride[0];
+        bp.q_sh = q->stride[1];
         bp.n = (int)n;
         bp.Hq = (int)Hq;
         bp.Hkv = (int)Hkv;
@@ -887,7 +889,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         bp.l_ss = 1;
         ProfRecord rec;
         const bool prof = prof_begin(FD_KERNEL_BIF_CTX, cs, &rec);
-        e = launch_bif_ctx(bp, tmQ, tmK, tmV, (int)mtiles, cs, !prof);
+        e = launch_bif_ctx(bp, tmK, tmV, (int)mtiles, cs, !prof);
         prof_end(FD_KERNEL_BIF_CTX, cs, prof, rec);
         if (e != cudaSuccess) st = cuda_fail(e, "bifurcated context kernel launch");
         ctx_done = true;

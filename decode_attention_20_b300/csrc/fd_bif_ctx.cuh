@@ -19,33 +19,33 @@
 //
 // CTA = two 128-row query tiles (256 rows) x one context split x one kv head;
 // 10 warps:
-//   warp 0      TMA producer: both Q tiles once, then K and V tiles of 64
-//               tokens into separate 4-stage rings, 128-byte swizzle (two
-//               64-column boxes per tile).  Every K/V tile feeds both Q tiles.
+//   warp 0      TMA producer: K and V tiles of 64 tokens into separate
+//               5-stage rings, 128-byte swizzle (two 64-column boxes per
+//               tile).  Every K/V tile feeds both query tiles.
 //   warp 1      allocates all 512 TMEM columns; one thread issues every MMA.
-//               TMEM: for each query tile t two score buffers S_t[0], S_t[1]
-//               (64 fp32 columns each, columns 128 t + 64 b) and the output
-//               accumulator O_t (128 columns at 256 + 128 t).
-//                 S_t[j % 2]  = Q_t K_j^T        (A, B from shared memory)
-//                 O_t        += P_t,j V_j        (A = P from TMEM, B = V from
-//                                                 shared memory, MN-major)
-//               P_t,j (bf16 pairs, 32 columns) overwrites the first half of
-//               the score buffer it was computed from.
-//   warps 2..5  softmax of query tile 0, warps 6..9 softmax of query tile 1:
-//               thread = one row (its TMEM lane).  Reads the row of S_t,j,
-//               keeps the running max m / sum l in base 2, writes the bf16
-//               probabilities back into TMEM, and rescales O_t on the rare
-//               tiles where the running max grows by more than 8 (lazy
+//               TMEM per query tile t: Q_t (bf16 pairs, 64 columns at 64 t),
+//               S_t (64 fp32 columns at 128 + 64 t), O_t (128 fp32 columns
+//               at 256 + 128 t).
+//                 S_t  = Q_t K_j^T     A = Q_t from TMEM, B = K from shared
+//                                      memory (K-major)
+//                 O_t += P_t V_j       A = P_t from TMEM, B = V from shared
+//                                      memory (MN-major)
+//               P_t (bf16 pairs, 32 columns) overwrites the first half of
+//               S_t.  With both A operands in tensor memory each MMA reads
+//               only its B tile from shared memory.
+//   warps 2..5  query tile 0, warps 6..9 query tile 1; thread = one row (its
+//               TMEM lane).  First each thread loads its query row from
+//               global memory into Q_t; then, per tile, it reads its row of
+//               S_t, keeps the running max m / sum l in base 2, writes the
+//               bf16 probabilities back into TMEM, and rescales O_t on the
+//               rare tiles where the running max grows by more than 8 (lazy
 //               rescale; p <= 256 always; numerator and denominator share m).
-// Score buffers are double-buffered, so the tensor core computes S_t,j+1 while
-// the softmax warps work on S_t,j, and the two query tiles interleave their
-// P V products.  The MMAs of one thread execute in issue order: S_t,j+2 is
-// issued after O_t += P_t,j V_j and so never overwrites P_t,j before it is
-// read.  A rescale of O_t before tile j waits for O_t += P_t,j-1 V_j-1
-// (o_done[t]).  The softmax warps may run two tiles ahead of the MMA issuer,
-// so "P ready" and "S ready" barriers exist per score buffer: each completes
-// once per use of its buffer, and a buffer is reused only after its previous
-// barrier phase has been consumed.
+// The two query tiles ping-pong on the tensor core: while one warpgroup runs
+// its softmax, the tensor core runs the other tile's P V and next Q K^T.
+// Ordering needs no extra waits: the MMAs of one thread execute in issue
+// order, and the barrier that signals "S_t of tile j is ready" is committed
+// after O_t += P_t V_{j-1}, so when a softmax warp sees S_t it may also
+// rescale O_t and overwrite P_t.
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees its tensor memory and returns with the device error flag set.
 #pragma once
@@ -71,33 +71,30 @@ struct BifCfg {
   static constexpr int ROWS = MT * NQ;          // rows per CTA
   static constexpr int D = 128;                 // head dim
   static constexpr int TN = kBifTileTokens;     // tokens per K/V tile
-  static constexpr int NK = 4;                  // K stages
-  static constexpr int NV = 4;                  // V stages
+  static constexpr int NK = 5;                  // K stages
+  static constexpr int NV = 5;                  // V stages
   static constexpr int NSW = 4 * NQ;            // softmax warps
   static constexpr int THREADS = 64 + NSW * 32;
-  static constexpr int Q_CHUNK = 128 * 128;     // 128 rows x 64 bf16 (one swizzled box)
-  static constexpr int Q_BYTES = 2 * Q_CHUNK;   // one query tile
-  static constexpr int KV_CHUNK = TN * 128;     // TN rows x 64 bf16
+  static constexpr int KV_CHUNK = TN * 128;     // TN rows x 64 bf16 (one swizzled box)
   static constexpr int KV_BYTES = 2 * KV_CHUNK; // one K or V tile (two boxes)
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + NQ * Q_BYTES;
+  static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
-  // barriers: q_full, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-  // s_full[NQ][2], p_full[NQ][2], o_done[NQ], drain
-  static constexpr int NBAR = 1 + 2 * NK + 2 * NV + 2 * NQ + 2 * NQ + NQ + 1;
+  // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready,
+  // s_full[NQ], p_full[NQ], o_done, drain
+  static constexpr int NBAR = 2 * NK + 2 * NV + 1 + 2 * NQ + 2;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S = 0;          // + 128 t + 64 b
+  static constexpr uint32_t COL_Q = 0;          // + 64 t
+  static constexpr uint32_t COL_S = 128;        // + 64 t
   static constexpr uint32_t COL_O = 256;        // + 128 t
-  static_assert(TN == 64, "score buffers are laid out for 64-token tiles");
+  static_assert(TN == 64, "score columns are laid out for 64-token tiles");
   static_assert(NQ == 2, "TMEM holds two query tiles");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-  static_assert(NQ * MT * (D + 4) * 4 <= OFF_BAR, "epilogue staging fits the operand buffers");
-  static_assert(MT * (D + 4) * 4 <= OFF_V, "tile 0 stages below the V ring");
+  static_assert(NQ * MT * (D + 4) * 4 <= OFF_BAR, "epilogue staging fits the K/V rings");
 };
 
-// Context split i of ns over [0, Lc): whole 128-token tiles.
+// Context split i of ns over [0, Lc): whole 64-token tiles.
 __device__ __forceinline__ void bif_split_range(int Lc, int ns, int i, int& begin, int& end) {
   const int per = (Lc + ns - 1) / ns;
   const long long chunk = (long long)((per + BifCfg::TN - 1) / BifCfg::TN) * BifCfg::TN;
@@ -107,23 +104,23 @@ __device__ __forceinline__ void bif_split_range(int Lc, int ns, int i, int& begi
 }
 
 __global__ void __launch_bounds__(BifCfg::THREADS, 1)
-    bif_ctx_kernel(const __grid_constant__ BifCtxParams p, const __grid_constant__ CUtensorMap tmQ,
-                   const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+    bif_ctx_kernel(const __grid_constant__ BifCtxParams p, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV) {
   using C = BifCfg;
   pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;
-  uint64_t* k_full = q_full + 1;
+  uint64_t* k_full = bars;
   uint64_t* k_empty = k_full + C::NK;
   uint64_t* v_full = k_empty + C::NK;
   uint64_t* v_empty = v_full + C::NV;
-  uint64_t* s_full = v_empty + C::NV;           // [NQ][2]
-  uint64_t* p_full = s_full + 2 * C::NQ;        // [NQ][2]
-  uint64_t* o_done = p_full + 2 * C::NQ;
-  uint64_t* drain = o_done + C::NQ;
+  uint64_t* q_ready = v_empty + C::NV;
+  uint64_t* s_full = q_ready + 1;               // [NQ]
+  uint64_t* p_full = s_full + C::NQ;            // [NQ]
+  uint64_t* o_done = p_full + C::NQ;
+  uint64_t* drain = o_done + 1;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_s = reinterpret_cast<int*>(taddr_s + 1);
 
@@ -135,7 +132,6 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   int begin, end;
   bif_split_range(p.Lc, p.ns, split, begin, end);
   const int ntiles = (end - begin + C::TN - 1) / C::TN;
-  const int samples_per_qtile = C::MT / p.G;
 
   if (ntiles == 0) {
     // Empty split: O = 0, lse = -inf for every valid row.
@@ -153,8 +149,9 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
-      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + 2 * C::NQ);
-      mbar_init(&bars[i], is_p ? 128 : 1);
+      const bool is_q = &bars[i] == q_ready;
+      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + C::NQ);
+      mbar_init(&bars[i], is_q ? C::NSW * 32 : (is_p ? 128 : 1));
     }
     *abort_s = 0;
     fence_barrier_init();
@@ -172,16 +169,8 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensormap(&tmQ);
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
-      mbar_arrive_expect_tx(q_full, C::NQ * C::Q_BYTES);
-      for (int t = 0; t < C::NQ; ++t) {
-        const int s0 = (mtile * C::NQ + t) * samples_per_qtile;
-        unsigned char* dst = smem + C::OFF_Q + t * C::Q_BYTES;
-        tma_load_3d(dst, &tmQ, q_full, 0, g * p.G, s0);
-        tma_load_3d(dst + C::Q_CHUNK, &tmQ, q_full, 64, g * p.G, s0);
-      }
       int kt = 0, vt = 0;                           // next K / V tile to issue
       bool ok = true;
       while (ok && (kt < ntiles || vt < ntiles)) {
@@ -211,7 +200,6 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
       }
       // Never leave with copies in flight: wait for the last load of every
       // stage (earlier loads of a stage completed before it was refilled).
-      mbar_wait_bounded(q_full, 0);
       for (int t = (kt > C::NK ? kt - C::NK : 0); t < kt; ++t)
         mbar_wait_bounded(&k_full[t % C::NK], (t / C::NK) & 1);
       for (int t = (vt > C::NV ? vt - C::NV : 0); t < vt; ++t)
@@ -220,67 +208,60 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      // Bit 13 of the instruction descriptor negates A (Q) for negative scales.
-      const uint32_t IDESC_S =
-          tc::idesc_bf16_f32(C::MT, C::TN, false, false) | (p.negate_q ? (1u << 13) : 0u);
+      constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(C::MT, C::TN, false, false);
       constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(C::MT, C::D, false, true);
-      bool ok = mbar_wait_or_abort(q_full, 0, abort_s);
-      // S_t[j % 2] = Q_t K_j^T (8 MMAs of K = 16 head dims).
+      // S_t = Q_t K_j^T (8 MMAs of K = 16 head dims; Q_t columns 8 kk).
       auto issue_s = [&](int t, int j) {
-        const uint32_t q_addr = sbase + C::OFF_Q + t * C::Q_BYTES;
         const uint32_t k_addr = sbase + C::OFF_K + (j % C::NK) * C::KV_BYTES;
-        const uint32_t d_tmem = tmem + C::COL_S + t * 128 + (j & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint32_t qoff = (kk >> 2) * C::Q_CHUNK + (kk & 3) * 32;
           const uint32_t koff = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-          tc::mma_bf16_ss(d_tmem, tc::smem_desc_sw128(q_addr + qoff, 16, 1024),
+          tc::mma_bf16_ts(tmem + C::COL_S + t * 64, tmem + C::COL_Q + t * 64 + kk * 8,
                           tc::smem_desc_sw128(k_addr + koff, 16, 1024), IDESC_S, kk > 0);
         }
-        tc::commit(&s_full[t * 2 + (j & 1)]);
+        tc::commit(&s_full[t]);
       };
-      // O_t += P_t,j V_j (4 MMAs of K = 16 tokens; P from the TMEM columns
-      // of S_t[j % 2], 8 per MMA; V MN-major: 16 token rows at 16 kk, two
+      // O_t += P_t V_j (4 MMAs of K = 16 tokens; P_t from the first 32
+      // columns of S_t, 8 per MMA; V MN-major: 16 token rows at 16 kk, two
       // 64-wide head-dim blocks KV_CHUNK apart).
       auto issue_pv = [&](int t, int j) {
         const uint32_t v_addr = sbase + C::OFF_V + (j % C::NV) * C::KV_BYTES;
-        const uint32_t a_tmem = tmem + C::COL_S + t * 128 + (j & 1) * 64;
 #pragma unroll
         for (int kk = 0; kk < C::TN / 16; ++kk)
-          tc::mma_bf16_ts(tmem + C::COL_O + t * 128, a_tmem + kk * 8,
+          tc::mma_bf16_ts(tmem + C::COL_O + t * 128, tmem + C::COL_S + t * 64 + kk * 8,
                           tc::smem_desc_sw128(v_addr + kk * 16 * 128, C::KV_CHUNK, 1024),
                           IDESC_O, (j > 0) || (kk > 0));
-        tc::commit(&o_done[t]);
       };
-      // Prologue: scores of tiles 0 and 1 for both query tiles.
-      for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
-        if (!mbar_wait_or_abort(&k_full[j % C::NK], (j / C::NK) & 1, abort_s)) { ok = false; break; }
+      bool ok = mbar_wait_or_abort(q_ready, 0, abort_s);
+      if (ok) ok = mbar_wait_or_abort(&k_full[0], 0, abort_s);
+      if (ok) {
         tc::fence_after_sync();
-        issue_s(0, j);
-        issue_s(1, j);
-        tc::commit(&k_empty[j % C::NK]);
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc::commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        const bool more = j + 2 < ntiles;
+        const bool more = j + 1 < ntiles;
         if (!mbar_wait_or_abort(&v_full[j % C::NV], (j / C::NV) & 1, abort_s)) break;
-        // query tile 0: O_0 += P_0,j V_j, then S_0 of tile j+2
-        if (!mbar_wait_or_abort(&p_full[0 * 2 + (j & 1)], (j >> 1) & 1, abort_s)) break;
+        // query tile 0: O_0 += P_0 V_j, then S_0 of tile j+1
+        if (!mbar_wait_or_abort(&p_full[0], j & 1, abort_s)) break;
         tc::fence_after_sync();
         issue_pv(0, j);
         if (more) {
-          if (!mbar_wait_or_abort(&k_full[(j + 2) % C::NK], ((j + 2) / C::NK) & 1, abort_s)) break;
-          issue_s(0, j + 2);
+          if (!mbar_wait_or_abort(&k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1, abort_s)) break;
+          issue_s(0, j + 1);
         }
-        // query tile 1: O_1 += P_1,j V_j, then S_1 of tile j+2
-        if (!mbar_wait_or_abort(&p_full[1 * 2 + (j & 1)], (j >> 1) & 1, abort_s)) break;
+        // query tile 1: O_1 += P_1 V_j, then S_1 of tile j+1
+        if (!mbar_wait_or_abort(&p_full[1], j & 1, abort_s)) break;
         tc::fence_after_sync();
         issue_pv(1, j);
         tc::commit(&v_empty[j % C::NV]);
         if (more) {
-          issue_s(1, j + 2);
-          tc::commit(&k_empty[(j + 2) % C::NK]);
+          issue_s(1, j + 1);
+          tc::commit(&k_empty[(j + 1) % C::NK]);
         }
       }
+      tc::commit(o_done);
       // Drain: every MMA issued above completes before the TMEM is freed.
       tc::commit(drain);
       mbar_wait_bounded(drain, 0);
@@ -291,18 +272,45 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;               // row of the query tile
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t s_tmem0 = tmem + lane_base + C::COL_S + t * 128;
+    const uint32_t q_tmem = tmem + lane_base + C::COL_Q + t * 64;
+    const uint32_t s_tmem = tmem + lane_base + C::COL_S + t * 64;
     const uint32_t o_tmem = tmem + lane_base + C::COL_O + t * 128;
+    const int m0 = (mtile * C::NQ + t) * C::MT;   // first row of this tile
+    {
+      // Query row -> Q_t (bf16 pairs, dim 2c in the low half of column c).
+      // Rows past n * G load zeros.  A negative scale is folded in here (the
+      // sign bits flip), so the softmax below always scales by |scale|.
+      uint32_t qv[2][32];
+      const int m = m0 + r;
+      if (m < p.rows) {
+        const int s = m / p.G;
+        const int h = g * p.G + (m - s * p.G);
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + s * p.q_sb + h * p.q_sh);
+        const uint32_t flip = p.negate_q ? 0x80008000u : 0u;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint4 w = src[i];
+          qv[i >> 3][(i & 7) * 4 + 0] = w.x ^ flip;
+          qv[i >> 3][(i & 7) * 4 + 1] = w.y ^ flip;
+          qv[i >> 3][(i & 7) * 4 + 2] = w.z ^ flip;
+          qv[i >> 3][(i & 7) * 4 + 3] = w.w ^ flip;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) qv[0][i] = qv[1][i] = 0u;
+      }
+      tc::tmem_st32(q_tmem, qv[0]);
+      tc::tmem_st32(q_tmem + 32, qv[1]);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      mbar_arrive(q_ready);
+    }
     float m_run = kNegInf, l_run = 0.f;
     bool ok = true;
-    // Scores arrive unscaled; the host negates Q through the instruction
-    // descriptor when the scale is negative, so scale_log2 >= 0 here and the
-    // row maximum of the scaled scores is scale_log2 times the raw maximum.
-    const float c2 = p.scale_log2;
+    const float c2 = p.scale_log2;                 // |scale| * log2(e) >= 0
     for (int j = 0; j < ntiles; ++j) {
-      const uint32_t s_tmem = s_tmem0 + (j & 1) * 64;
       // Waits are made warp-uniform before any .sync.aligned tcgen05 access.
-      const bool got = mbar_wait_or_abort(&s_full[t * 2 + (j & 1)], (j >> 1) & 1, abort_s);
+      const bool got = mbar_wait_or_abort(&s_full[t], j & 1, abort_s);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc::fence_after_sync();
       uint32_t sr[2][32];
@@ -331,8 +339,8 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
       const float m_new = (mx > m_run + 8.f) ? mx : m_run;
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
       const float m_use = (m_new == kNegInf) ? 0.f : m_new;   // all -inf: p = 0, not NaN
-      // p = 2^(s * c2 - m); P as bf16 pairs (even token in the low half)
-      // packed in place and stored into the first 32 columns of the buffer.
+      // p = 2^(s * c2 - m); P_t as bf16 pairs (even token in the low half)
+      // packed in place and stored into the first 32 columns of S_t.
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -347,12 +355,9 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
         }
         tc::tmem_st16(s_tmem + c * 16, sr[c]);
       }
-      // Rescale O_t where its max moved, once O_t += P_t,j-1 V_j-1 is done
-      // (rare: the running max grew by more than 8).
+      // O_t += P_t V_{j-1} is complete (it was issued before S_t of tile j):
+      // rescale O_t where its max moved (rare).
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const bool got_o = mbar_wait_or_abort(&o_done[t], (j - 1) & 1, abort_s);
-        if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
-        tc::fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orr[32];
@@ -366,28 +371,19 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(&p_full[t * 2 + (j & 1)]);
+      mbar_arrive(&p_full[t]);
       l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m_run = m_new;
     }
     // ------------------------------------------------------------ epilogue
-    // Once this tile's last P V has completed, so has every MMA issued
-    // before it (all score MMAs included), and the Q and K buffers are dead.
-    // Tile 0 stages in [0, 66 KB), which only the Q and K buffers occupy (the
-    // other tile's last P V may still read the V ring); tile 1's last P V is
-    // the last MMA of the CTA.  Each row owner normalises its O row into the
-    // padded staging tile, then each warp writes whole rows (512 contiguous
+    // o_done is committed after the last MMA of the CTA: once it fires the
+    // K/V rings are dead.  Each row owner normalises its O row into a padded
+    // staging tile there, then each warp writes whole rows (512 contiguous
     // bytes per store instruction) instead of 32 rows at once.
-    // o_done[t] completes once per P V of this tile.  Seeing S of the last
-    // tile only guarantees the P V two tiles earlier, so wait for the last
-    // two phases in order (a parity wait must not fall two phases behind).
-    bool got_last = ok;
-    if (got_last && ntiles >= 2) got_last = mbar_wait_or_abort(&o_done[t], (ntiles - 2) & 1, abort_s);
-    if (got_last) got_last = mbar_wait_or_abort(&o_done[t], (ntiles - 1) & 1, abort_s);
+    const bool got_last = ok && mbar_wait_or_abort(o_done, 0, abort_s);
     const bool done = __all_sync(0xffffffffu, got_last);
     constexpr int SROW = C::D + 4;                            // padded row (floats)
     float* stage = reinterpret_cast<float*>(smem) + t * (C::MT * SROW);
-    const int m0 = (mtile * C::NQ + t) * C::MT;                // first row of this tile
     if (done) {
       tc::fence_after_sync();
       const int m = m0 + r;

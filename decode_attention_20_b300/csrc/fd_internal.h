@@ -31,6 +31,7 @@ struct SplitParams {
   float scale_log2;           // scale * log2(e): scores are kept in base 2
   float* o;                   // partial (or final, ns == 1) output, fp32
   int64_t o_sb, o_sh, o_ss;   // strides over (b, q head, split)
+  int o_vec4;                 // 1: o and its strides allow 16-byte stores
   float* lse;                 // natural-log lse, or nullptr
   int64_t l_sb, l_sh, l_ss;
   int kv_batch_broadcast;     // 1: every sequence reads kv batch row 0
@@ -53,10 +54,12 @@ struct CombineParams {
 // context split, kv head)); rows of kv head g are (sample, head-in-group)
 // pairs, row m = sample * G + r.
 struct BifCtxParams {
+  const uint16_t* q;          // [n, Hq, D] bf16, rows 16-byte aligned
+  int64_t q_sb, q_sh;         // element strides over (sample, q head)
   int n, Hq, Hkv, G, Lc, ns;
   int rows;                   // n * G
   float scale_log2;           // |scale| * log2(e)
-  int negate_q;               // 1: scale < 0, the kernel negates Q in the MMA
+  int negate_q;               // 1: scale < 0, the kernel negates Q as it loads it
   float* o;                   // partial outputs, fp32
   int64_t o_sb, o_sh, o_ss;   // strides over (sample, q head, split)
   float* lse;                 // natural-log partial lse
@@ -80,8 +83,8 @@ int mma_tile_tokens(int variant);
 cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaStream_t st,
                                  bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
-cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, int mtiles, cudaStream_t st, bool pdl);
+cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           int mtiles, cudaStream_t st, bool pdl);
 
 // Tile height (tokens) of the TMA split kernel; the tensor-map box uses it.
 constexpr int kSplitTileTokens = 64;

@@ -156,8 +156,8 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
   return launch_ex(lse_combine_kernel, dim3(p.R1 * p.R2), dim3(kCombineThreads), 0, st, pdl, p);
 }
 
-cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                           const CUtensorMap& tmV, int mtiles, cudaStream_t st, bool pdl) {
+cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           int mtiles, cudaStream_t st, bool pdl) {
   static unsigned long long attr_set = 0ull;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -170,7 +170,7 @@ cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmQ, const 
     attr_set |= bit;
   }
   return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
-                   BifCfg::SMEM_BYTES, st, pdl, p, tmQ, tmK, tmV);
+                   BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV);
 }
 
 }  // namespace fd

@@ -104,7 +104,7 @@ struct MmaCfg {
   static constexpr int SMEM_BYTES = 1024 + RING_BYTES + 2 * NSTAGE * 8 + 16;
   static_assert(NT % WN == 0, "n-tiles split evenly over warps");
   static_assert(W % WN == 0 && BLK % WT == 0 && BPW >= 1, "blocks split evenly over warps");
-  static_assert(WT * GP * (D + 2) * 4 <= RING_BYTES, "epilogue fits the ring");
+  static_assert(WT * GP * (D + 3) * 4 <= RING_BYTES, "epilogue fits the ring");
   static_assert(HALF_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
 };
 
@@ -375,26 +375,53 @@ __global__ void __launch_bounds__(W * 32, 1)
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * C::D; idx += C::THREADS) {
-    const int h = idx / C::D;
-    const int d = idx - h * C::D;
+  // Per head: the common max, each token group's weight 2^(m_w - M) / l_tot
+  // (into SF_s) and the log-sum-exp; then every output element is a short
+  // weighted sum over the token groups, four elements per thread at a time.
+  float* SF_s = ACC_s + C::WT * C::GP * C::D;                // [WT][GP]
+  for (int h = threadIdx.x; h < G; h += C::THREADS) {
     float M = kNegInf;
 #pragma unroll
     for (int w = 0; w < C::WT; ++w) M = fmaxf(M, ML_s[(w * C::GP + h) * 2]);
-    float lt = 0.f, o = 0.f;
-    if (M != kNegInf) {
+    float lt = 0.f;
+    float f[C::WT];
 #pragma unroll
-      for (int w = 0; w < C::WT; ++w) {
-        const float ms = ML_s[(w * C::GP + h) * 2];
-        const float f = (ms == kNegInf) ? 0.f : fast_exp2(ms - M);
-        lt += f * ML_s[(w * C::GP + h) * 2 + 1];
-        o += f * ACC_s[(w * C::GP + h) * C::D + d];
-      }
+    for (int w = 0; w < C::WT; ++w) {
+      const float ms = ML_s[(w * C::GP + h) * 2];
+      f[w] = (ms == kNegInf) ? 0.f : fast_exp2(ms - M);
+      lt += f[w] * ML_s[(w * C::GP + h) * 2 + 1];
+    }
+    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+    for (int w = 0; w < C::WT; ++w) SF_s[w * C::GP + h] = f[w] * inv;
+    const int hq = g * G + h;
+    if (p.lse != nullptr)
+      p.lse[b * p.l_sb + hq * p.l_sh + split * p.l_ss] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * (C::D / 4); idx += C::THREADS) {
+    const int h = idx / (C::D / 4);
+    const int d = (idx - h * (C::D / 4)) * 4;
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < C::WT; ++w) {
+      const float sf = SF_s[w * C::GP + h];
+      const float4 a = *reinterpret_cast<const float4*>(ACC_s + (w * C::GP + h) * C::D + d);
+      o.x = fmaf(sf, a.x, o.x);
+      o.y = fmaf(sf, a.y, o.y);
+      o.z = fmaf(sf, a.z, o.z);
+      o.w = fmaf(sf, a.w, o.w);
     }
     const int hq = g * G + h;
-    p.o[b * p.o_sb + hq * p.o_sh + split * p.o_ss + d] = lt > 0.f ? o / lt : 0.f;
-    if (d == 0 && p.lse != nullptr)
-      p.lse[b * p.l_sb + hq * p.l_sh + split * p.l_ss] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
+    float* dst = p.o + b * p.o_sb + hq * p.o_sh + split * p.o_ss + d;
+    if (p.o_vec4) {
+      *reinterpret_cast<float4*>(dst) = o;
+    } else {
+      dst[0] = o.x;
+      dst[1] = o.y;
+      dst[2] = o.z;
+      dst[3] = o.w;
+    }
   }
 }
 
