@@ -443,12 +443,12 @@ fd_status enqueue_combine(const CombineParams& cp, cudaStream_t st, bool pdl) {
 }
 
 // Context split count of the bifurcated tensor-core kernel: the fewest
-// splits that reach the smallest makespan waves x (tiles per split + 4) when
-// `units` CTAs (query-tile pairs x kv heads) run per split on `num_sms` SMs,
-// one CTA per SM; the 4 tiles (256 tokens) charge each CTA its start-up
-// (query load, pipeline fill) and epilogue.
+// splits that reach the smallest makespan waves x (tiles per split + 2) when
+// `units` CTAs (query tiles x kv heads) run per split on `num_sms` SMs, one
+// CTA per SM; the 2 tiles (256 tokens) charge each CTA its start-up (query
+// load, pipeline fill) and epilogue.
 int choose_ctx_splits(int64_t Lc, int64_t units, int num_sms) {
-  constexpr int64_t kCtaOverheadTiles = 4;
+  constexpr int64_t kCtaOverheadTiles = 2;
   const int64_t tiles = (Lc + kBifTileTokens - 1) / kBifTileTokens;
   int best_ns = 1;
   int64_t best_cost = -1;
@@ -822,7 +822,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   // Tensor-core context path: head dim 128, 16-byte aligned bases and
   // strides (query rows are read as 16-byte vectors, K/V through TMA).
   const int64_t G = Hq / Hkv;
-  const bool tc_ok = bif_ctx_tensor_core_allowed() && D == 128 &&
+  bool tc_ok = bif_ctx_tensor_core_allowed() && D == 128 &&
                      aligned16(q->data) && aligned16(k_ctx->data) && aligned16(v_ctx->data) &&
                      (q->stride[1] * 2) % 16 == 0 && (q->stride[0] * 2) % 16 == 0 &&
                      q->stride[1] > 0 && (q->stride[0] > 0 || n == 1) &&
@@ -830,6 +830,15 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
                      (v_ctx->stride[1] * 2) % 16 == 0 && (v_ctx->stride[0] * 2) % 16 == 0 &&
                      k_ctx->stride[1] > 0 && v_ctx->stride[1] > 0 && k_ctx->stride[0] > 0 &&
                      v_ctx->stride[0] > 0;
+  // Tensor maps of the context K / V (the tensor-core path needs both).
+  CUtensorMap tmK, tmV;
+  if (tc_ok) {
+    if ((st = get_encoder())) return st;
+    tc_ok = make_3d_map(&tmK, k_ctx->data, D, Hkv, Lc, k_ctx->stride[1], k_ctx->stride[0], 1,
+                        kBifTileTokens) &&
+            make_3d_map(&tmV, v_ctx->data, D, Hkv, Lc, v_ctx->stride[1], v_ctx->stride[0], 1,
+                        kBifTileTokens);
+  }
   const int64_t mtiles = (n * G + 128 * kBifQueryTiles - 1) / (128 * kBifQueryTiles);
   const int ns_ctx = ctx_splits > 0 ? ctx_splits
                      : tc_ok ? choose_ctx_splits(Lc, mtiles * Hkv, info->sms)
@@ -844,7 +853,26 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
     if (want > kMaxSplits) want = kMaxSplits;
     ns_dec = want < 1 ? 1 : (int)want;
   }
-  const int S = ns_ctx + ns_dec;
+  // Optional thread-block clusters along the context splits merge them on
+  // chip (distributed shared memory) instead of writing one partial per
+  // split.  Off by default: on B300 the clustered launch measured slower
+  // (clusters of 8 CTAs of ~190 KB shared memory each are hard to co-place
+  // in one GPC).  FD_BIF_CLUSTER = 2, 4 or 8 enables clusters of at most
+  // that many CTAs: the cluster size is then the largest power of two up to
+  // it dividing ns_ctx (it must divide the 128 rows of a tile), used only
+  // when every split holds tokens.
+  int csize = 1;
+  if (tc_ok) {
+    const char* ce = getenv("FD_BIF_CLUSTER");
+    const int cmax = ce ? atoi(ce) : 1;
+    const int64_t per = (Lc + ns_ctx - 1) / ns_ctx;
+    const int64_t chunk = ((per + kBifTileTokens - 1) / kBifTileTokens) * kBifTileTokens;
+    const bool all_full = (int64_t)(ns_ctx - 1) * chunk < Lc;
+    if (cmax >= 2 && all_full)
+      for (int d = 8; d >= 2; d /= 2)
+        if (d <= cmax && ns_ctx % d == 0) { csize = d; break; }
+  }
+  const int S = ns_ctx / csize + ns_dec;
   const int64_t bytes = workspace_bytes(n, Hq, D, S);
   void* ws = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)bytes, info->pool, cs);
@@ -856,13 +884,8 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   bool ctx_done = false;
   if (tc_ok) {
     // Context part on the tensor cores: rows (sample, head of the group).
-    if ((st = get_encoder()) == FD_OK) {
-      CUtensorMap tmK, tmV;
-      const bool okk = make_3d_map(&tmK, k_ctx->data, D, Hkv, Lc, k_ctx->stride[1],
-                                   k_ctx->stride[0], 1, kBifTileTokens);
-      const bool okv = make_3d_map(&tmV, v_ctx->data, D, Hkv, Lc, v_ctx->stride[1],
-                                   v_ctx->stride[0], 1, kBifTileTokens);
-      if (okk && okv) {
+    {
+      {
         BifCtxParams bp = {};
         bp.q = reinterpret_cast<const uint16_t*>(q->data);
         bp.q_sb = q->stride[0];
@@ -879,6 +902,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         // masked tail scores stay at -inf instead of 0 * inf = NaN.
         bp.scale_log2 = scale == 0.f ? 1e-30f : std::fabs(scale) * 1.4426950408889634f;
         bp.negate_q = scale < 0.f ? 1 : 0;
+        bp.cs = csize;
         bp.o = po;
         bp.o_sb = Hq * S * D;
         bp.o_sh = S * D;
@@ -909,8 +933,8 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
     DecodeDesc dd = {n, Hq, Hkv, D, Ld, Hq / Hkv, FD_BF16, FD_BF16};
     st = enqueue_split(dd, q, k_dec, v_dec,
                        dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr,
-                       ns_dec, scale, po + (int64_t)ns_ctx * D, Hq * S * D, S * D, D,
-                       pl + ns_ctx, Hq * S, S, 1, false, cs);
+                       ns_dec, scale, po + (int64_t)(ns_ctx / csize) * D, Hq * S * D, S * D, D,
+                       pl + ns_ctx / csize, Hq * S, S, 1, false, cs);
   }
   if (st == FD_OK) {
     CombineParams cp = {};

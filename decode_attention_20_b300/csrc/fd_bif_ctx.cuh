@@ -6,8 +6,8 @@
 //   S = Q_g K_ctx[g]^T          (GEMM 1, K-dim = D)
 //   online softmax over the tokens of a split
 //   O = P V_ctx[g]              (GEMM 2, K-dim = tokens)
-// and the context KV is read once per pair of 128-row query tiles instead of
-// once per sample.  Each CTA writes, for its rows and one token split of the
+// and the context KV is read once per 128-row query tile instead of once per
+// sample.  Each CTA writes, for its rows and one token split of the
 // context, the normalised partial output and its natural-log log-sum-exp, in
 // the same partial format as the split kernel; the log-sum-exp reduction then
 // merges them with the per-sample decode part.  Source: summary of
@@ -17,35 +17,35 @@
 // "How does Flash Attention reduce memory traffic during local inference?",
 // section on online softmax.
 //
-// CTA = two 128-row query tiles (256 rows) x one context split x one kv head;
-// 10 warps:
-//   warp 0      TMA producer: K and V tiles of 64 tokens into separate
-//               5-stage rings, 128-byte swizzle (two 64-column boxes per
-//               tile).  Every K/V tile feeds both query tiles.
-//   warp 1      allocates all 512 TMEM columns; one thread issues every MMA.
-//               TMEM per query tile t: Q_t (bf16 pairs, 64 columns at 64 t),
-//               S_t (64 fp32 columns at 128 + 64 t), O_t (128 fp32 columns
-//               at 256 + 128 t).
-//                 S_t  = Q_t K_j^T     A = Q_t from TMEM, B = K from shared
-//                                      memory (K-major)
-//                 O_t += P_t V_j       A = P_t from TMEM, B = V from shared
-//                                      memory (MN-major)
-//               P_t (bf16 pairs, 32 columns) overwrites the first half of
-//               S_t.  With both A operands in tensor memory each MMA reads
-//               only its B tile from shared memory.
-//   warps 2..5  query tile 0, warps 6..9 query tile 1; thread = one row (its
-//               TMEM lane).  First each thread loads its query row from
-//               global memory into Q_t; then, per tile, it reads its row of
-//               S_t, keeps the running max m / sum l in base 2, writes the
-//               bf16 probabilities back into TMEM, and rescales O_t on the
-//               rare tiles where the running max grows by more than 8 (lazy
-//               rescale; p <= 256 always; numerator and denominator share m).
-// The two query tiles ping-pong on the tensor core: while one warpgroup runs
-// its softmax, the tensor core runs the other tile's P V and next Q K^T.
-// Ordering needs no extra waits: the MMAs of one thread execute in issue
-// order, and the barrier that signals "S_t of tile j is ready" is committed
-// after O_t += P_t V_{j-1}, so when a softmax warp sees S_t it may also
-// rescale O_t and overwrite P_t.
+// CTA = one 128-row query tile x one context split x one kv head; 6 warps:
+//   warp 0      TMA producer: K and V tiles of 128 tokens into separate
+//               3-stage rings, 128-byte swizzle (two 64-column boxes per
+//               tile).
+//   warp 1      allocates 512 TMEM columns; one thread issues every MMA.
+//               TMEM: Q (bf16 pairs, 64 columns at 0), two score buffers
+//               S[0], S[1] (128 fp32 columns each, at 64 and 192) and the
+//               output accumulator O (128 fp32 columns at 320).
+//                 S[j % 2]  = Q K_j^T     A = Q from TMEM, B = K from shared
+//                                         memory (K-major), N = 128 tokens
+//                 O        += P_j V_j     A = P_j from TMEM, B = V from shared
+//                                         memory (MN-major), N = 128 dims
+//               P_j (bf16 pairs, 64 columns) overwrites the first half of the
+//               score buffer it was computed from.  Every MMA is 128 x 128 x
+//               16 and reads only its B tile from shared memory.
+//   warps 2..5  softmax: thread = one row (its TMEM lane).  First each thread
+//               loads its query row from global memory into Q; then, per
+//               tile, it reads its row of S, keeps the running max m / sum l
+//               in base 2, writes the bf16 probabilities back into TMEM, and
+//               rescales O on the rare tiles where the running max grows by
+//               more than 8 (lazy rescale; p <= 256 always; numerator and
+//               denominator share m).
+// The score buffers are double-buffered, so the tensor core computes
+// S_{j+1} while the softmax warps work on S_j.  The MMAs of one thread
+// execute in issue order: S_{j+2} is issued after O += P_j V_j and so never
+// overwrites P_j before it is read.  A rescale of O before tile j first
+// waits for O += P_{j-1} V_{j-1} (o_done).  The softmax warps may run one
+// tile ahead of the MMA issuer, so "S ready" and "P ready" barriers exist
+// per score buffer.
 // Every wait is bounded; on a timeout the CTA drains its copies and MMAs,
 // frees its tensor memory and returns with the device error flag set.
 #pragma once
@@ -66,14 +66,13 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
 }
 
 struct BifCfg {
-  static constexpr int MT = 128;                // rows per query tile (TMEM lanes)
-  static constexpr int NQ = kBifQueryTiles;     // query tiles per CTA
-  static constexpr int ROWS = MT * NQ;          // rows per CTA
+  static constexpr int MT = 128;                // rows per CTA (TMEM lanes)
+  static constexpr int ROWS = MT;
   static constexpr int D = 128;                 // head dim
   static constexpr int TN = kBifTileTokens;     // tokens per K/V tile
-  static constexpr int NK = 5;                  // K stages
-  static constexpr int NV = 5;                  // V stages
-  static constexpr int NSW = 4 * NQ;            // softmax warps
+  static constexpr int NK = 3;                  // K stages
+  static constexpr int NV = 3;                  // V stages
+  static constexpr int NSW = 4;                 // softmax warps
   static constexpr int THREADS = 64 + NSW * 32;
   static constexpr int KV_CHUNK = TN * 128;     // TN rows x 64 bf16 (one swizzled box)
   static constexpr int KV_BYTES = 2 * KV_CHUNK; // one K or V tile (two boxes)
@@ -81,20 +80,20 @@ struct BifCfg {
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
   // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready,
-  // s_full[NQ], p_full[NQ], o_done, drain
-  static constexpr int NBAR = 2 * NK + 2 * NV + 1 + 2 * NQ + 2;
+  // s_full[2], p_full[2], o_done, o_final, drain
+  static constexpr int NBAR = 2 * NK + 2 * NV + 1 + 2 + 2 + 3;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_Q = 0;          // + 64 t
-  static constexpr uint32_t COL_S = 128;        // + 64 t
-  static constexpr uint32_t COL_O = 256;        // + 128 t
-  static_assert(TN == 64, "score columns are laid out for 64-token tiles");
-  static_assert(NQ == 2, "TMEM holds two query tiles");
+  static constexpr uint32_t COL_Q = 0;          // 64 columns
+  static constexpr uint32_t COL_S = 64;         // + 128 b
+  static constexpr uint32_t COL_O = 320;        // 128 columns
+  static_assert(TN == 128, "score buffers are laid out for 128-token tiles");
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
-  static_assert(NQ * MT * (D + 4) * 4 <= OFF_BAR, "epilogue staging fits the K/V rings");
+  static constexpr int STAGE_BYTES = MT * (D + 4) * 4;        // padded O rows
+  static_assert(STAGE_BYTES + MT * 8 <= OFF_BAR, "epilogue staging fits the K/V rings");
 };
 
-// Context split i of ns over [0, Lc): whole 64-token tiles.
+// Context split i of ns over [0, Lc): whole 128-token tiles.
 __device__ __forceinline__ void bif_split_range(int Lc, int ns, int i, int& begin, int& end) {
   const int per = (Lc + ns - 1) / ns;
   const long long chunk = (long long)((per + BifCfg::TN - 1) / BifCfg::TN) * BifCfg::TN;
@@ -117,14 +116,15 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   uint64_t* v_full = k_empty + C::NK;
   uint64_t* v_empty = v_full + C::NV;
   uint64_t* q_ready = v_empty + C::NV;
-  uint64_t* s_full = q_ready + 1;               // [NQ]
-  uint64_t* p_full = s_full + C::NQ;            // [NQ]
-  uint64_t* o_done = p_full + C::NQ;
-  uint64_t* drain = o_done + 1;
+  uint64_t* s_full = q_ready + 1;               // [2]
+  uint64_t* p_full = s_full + 2;                // [2]
+  uint64_t* o_done = p_full + 2;
+  uint64_t* o_final = o_done + 1;
+  uint64_t* drain = o_final + 1;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_s = reinterpret_cast<int*>(taddr_s + 1);
 
-  const int mtile = blockIdx.x;                 // pair of 128-row query tiles
+  const int mtile = blockIdx.x;                 // 128-row query tile
   const int split = blockIdx.y;
   const int g = blockIdx.z;
   const int warp = threadIdx.x >> 5;
@@ -133,8 +133,10 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   bif_split_range(p.Lc, p.ns, split, begin, end);
   const int ntiles = (end - begin + C::TN - 1) / C::TN;
 
-  if (ntiles == 0) {
-    // Empty split: O = 0, lse = -inf for every valid row.
+  if (ntiles == 0 && p.cs == 1) {
+    // Empty split: O = 0, lse = -inf for every valid row.  (In a cluster an
+    // empty split still runs through, stages (m, l) = (-inf, 0) and joins the
+    // cluster barriers.)
     for (int rr = threadIdx.x; rr < C::ROWS; rr += C::THREADS) {
       const int m = mtile * C::ROWS + rr;
       if (m < p.rows) {
@@ -150,8 +152,8 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::NBAR; ++i) {
       const bool is_q = &bars[i] == q_ready;
-      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + C::NQ);
-      mbar_init(&bars[i], is_q ? C::NSW * 32 : (is_p ? 128 : 1));
+      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + 2);
+      mbar_init(&bars[i], (is_q || is_p) ? C::NSW * 32 : 1);
     }
     *abort_s = 0;
     fence_barrier_init();
@@ -210,74 +212,66 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(C::MT, C::TN, false, false);
       constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(C::MT, C::D, false, true);
-      // S_t = Q_t K_j^T (8 MMAs of K = 16 head dims; Q_t columns 8 kk).
-      auto issue_s = [&](int t, int j) {
+      // S[j % 2] = Q K_j^T (8 MMAs of K = 16 head dims; Q columns 8 kk).
+      auto issue_s = [&](int j) {
         const uint32_t k_addr = sbase + C::OFF_K + (j % C::NK) * C::KV_BYTES;
+        const uint32_t d_tmem = tmem + C::COL_S + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < C::D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-          tc::mma_bf16_ts(tmem + C::COL_S + t * 64, tmem + C::COL_Q + t * 64 + kk * 8,
+          tc::mma_bf16_ts(d_tmem, tmem + C::COL_Q + kk * 8,
                           tc::smem_desc_sw128(k_addr + koff, 16, 1024), IDESC_S, kk > 0);
         }
-        tc::commit(&s_full[t]);
+        tc::commit(&s_full[j & 1]);
       };
-      // O_t += P_t V_j (4 MMAs of K = 16 tokens; P_t from the first 32
-      // columns of S_t, 8 per MMA; V MN-major: 16 token rows at 16 kk, two
+      // O += P_j V_j (8 MMAs of K = 16 tokens; P_j from the first 64 columns
+      // of S[j % 2], 8 per MMA; V MN-major: 16 token rows at 16 kk, two
       // 64-wide head-dim blocks KV_CHUNK apart).
-      auto issue_pv = [&](int t, int j) {
+      auto issue_pv = [&](int j) {
         const uint32_t v_addr = sbase + C::OFF_V + (j % C::NV) * C::KV_BYTES;
+        const uint32_t a_tmem = tmem + C::COL_S + (j & 1) * 128;
 #pragma unroll
         for (int kk = 0; kk < C::TN / 16; ++kk)
-          tc::mma_bf16_ts(tmem + C::COL_O + t * 128, tmem + C::COL_S + t * 64 + kk * 8,
+          tc::mma_bf16_ts(tmem + C::COL_O, a_tmem + kk * 8,
                           tc::smem_desc_sw128(v_addr + kk * 16 * 128, C::KV_CHUNK, 1024),
                           IDESC_O, (j > 0) || (kk > 0));
+        tc::commit(o_done);
       };
       bool ok = mbar_wait_or_abort(q_ready, 0, abort_s);
-      if (ok) ok = mbar_wait_or_abort(&k_full[0], 0, abort_s);
-      if (ok) {
+      // Prologue: scores of tiles 0 and 1.
+      for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
+        if (!mbar_wait_or_abort(&k_full[j % C::NK], (j / C::NK) & 1, abort_s)) { ok = false; break; }
         tc::fence_after_sync();
-        issue_s(0, 0);
-        issue_s(1, 0);
-        tc::commit(&k_empty[0]);
+        issue_s(j);
+        tc::commit(&k_empty[j % C::NK]);
       }
       for (int j = 0; ok && j < ntiles; ++j) {
-        const bool more = j + 1 < ntiles;
         if (!mbar_wait_or_abort(&v_full[j % C::NV], (j / C::NV) & 1, abort_s)) break;
-        // query tile 0: O_0 += P_0 V_j, then S_0 of tile j+1
-        if (!mbar_wait_or_abort(&p_full[0], j & 1, abort_s)) break;
+        if (!mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1, abort_s)) break;
         tc::fence_after_sync();
-        issue_pv(0, j);
-        if (more) {
-          if (!mbar_wait_or_abort(&k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1, abort_s)) break;
-          issue_s(0, j + 1);
-        }
-        // query tile 1: O_1 += P_1 V_j, then S_1 of tile j+1
-        if (!mbar_wait_or_abort(&p_full[1], j & 1, abort_s)) break;
-        tc::fence_after_sync();
-        issue_pv(1, j);
+        issue_pv(j);
         tc::commit(&v_empty[j % C::NV]);
-        if (more) {
-          issue_s(1, j + 1);
-          tc::commit(&k_empty[(j + 1) % C::NK]);
+        if (j + 2 < ntiles) {
+          if (!mbar_wait_or_abort(&k_full[(j + 2) % C::NK], ((j + 2) / C::NK) & 1, abort_s)) break;
+          issue_s(j + 2);
+          tc::commit(&k_empty[(j + 2) % C::NK]);
         }
       }
-      tc::commit(o_done);
+      tc::commit(o_final);
       // Drain: every MMA issued above completes before the TMEM is freed.
       tc::commit(drain);
       mbar_wait_bounded(drain, 0);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) >> 2;                // query tile of this warpgroup
     const int quad = warp & 3;                    // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;               // row of the query tile
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    const uint32_t q_tmem = tmem + lane_base + C::COL_Q + t * 64;
-    const uint32_t s_tmem = tmem + lane_base + C::COL_S + t * 64;
-    const uint32_t o_tmem = tmem + lane_base + C::COL_O + t * 128;
-    const int m0 = (mtile * C::NQ + t) * C::MT;   // first row of this tile
+    const uint32_t q_tmem = tmem + lane_base + C::COL_Q;
+    const uint32_t o_tmem = tmem + lane_base + C::COL_O;
+    const int m0 = mtile * C::MT;                 // first row of this tile
     {
-      // Query row -> Q_t (bf16 pairs, dim 2c in the low half of column c).
+      // Query row -> Q (bf16 pairs, dim 2c in the low half of column c).
       // Rows past n * G load zeros.  A negative scale is folded in here (the
       // sign bits flip), so the softmax below always scales by |scale|.
       uint32_t qv[2][32];
@@ -309,18 +303,19 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     bool ok = true;
     const float c2 = p.scale_log2;                 // |scale| * log2(e) >= 0
     for (int j = 0; j < ntiles; ++j) {
+      const uint32_t s_tmem = tmem + lane_base + C::COL_S + (j & 1) * 128;
       // Waits are made warp-uniform before any .sync.aligned tcgen05 access.
-      const bool got = mbar_wait_or_abort(&s_full[t], j & 1, abort_s);
+      const bool got = mbar_wait_or_abort(&s_full[j & 1], (j >> 1) & 1, abort_s);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc::fence_after_sync();
-      uint32_t sr[2][32];
-      tc::tmem_ld32(s_tmem, sr[0]);
-      tc::tmem_ld32(s_tmem + 32, sr[1]);
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, sr[c]);
       tc::tmem_wait_ld();
       const int nvalid = min(C::TN, end - (begin + j * C::TN));
       if (nvalid < C::TN) {                        // tail tile only (uniform branch)
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (c * 32 + i >= nvalid) sr[c][i] = __float_as_uint(kNegInf);
@@ -330,7 +325,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = kNegInf;
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
 #pragma unroll
@@ -339,11 +334,11 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
       const float m_new = (mx > m_run + 8.f) ? mx : m_run;
       const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
       const float m_use = (m_new == kNegInf) ? 0.f : m_new;   // all -inf: p = 0, not NaN
-      // p = 2^(s * c2 - m); P_t as bf16 pairs (even token in the low half)
-      // packed in place and stored into the first 32 columns of S_t.
+      // p = 2^(s * c2 - m); P_j as bf16 pairs (even token in the low half)
+      // packed in place and stored into the first 64 columns of the buffer.
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i]), c2, -m_use));
@@ -355,9 +350,12 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
         }
         tc::tmem_st16(s_tmem + c * 16, sr[c]);
       }
-      // O_t += P_t V_{j-1} is complete (it was issued before S_t of tile j):
-      // rescale O_t where its max moved (rare).
+      // Rescale O where its max moved (rare), once O += P_{j-1} V_{j-1} is
+      // done: o_done has then completed phases 0..j-1 (phase j needs P_j).
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const bool got_o = mbar_wait_or_abort(o_done, (j - 1) & 1, abort_s);
+        if (!__all_sync(0xffffffffu, got_o)) { ok = false; break; }
+        tc::fence_after_sync();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t orr[32];
@@ -371,19 +369,20 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
       }
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(&p_full[t]);
+      mbar_arrive(&p_full[j & 1]);
       l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
       m_run = m_new;
     }
     // ------------------------------------------------------------ epilogue
-    // o_done is committed after the last MMA of the CTA: once it fires the
+    // o_final is committed after the last MMA of the CTA: once it fires the
     // K/V rings are dead.  Each row owner normalises its O row into a padded
     // staging tile there, then each warp writes whole rows (512 contiguous
     // bytes per store instruction) instead of 32 rows at once.
-    const bool got_last = ok && mbar_wait_or_abort(o_done, 0, abort_s);
+    const bool got_last = ok && mbar_wait_or_abort(o_final, 0, abort_s);
     const bool done = __all_sync(0xffffffffu, got_last);
     constexpr int SROW = C::D + 4;                            // padded row (floats)
-    float* stage = reinterpret_cast<float*>(smem) + t * (C::MT * SROW);
+    float* stage = reinterpret_cast<float*>(smem);
+    float2* ml_stage = reinterpret_cast<float2*>(smem + C::STAGE_BYTES);
     if (done) {
       tc::fence_after_sync();
       const int m = m0 + r;
@@ -399,15 +398,20 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
               make_float4(__uint_as_float(orr[i]) * inv_l, __uint_as_float(orr[i + 1]) * inv_l,
                           __uint_as_float(orr[i + 2]) * inv_l, __uint_as_float(orr[i + 3]) * inv_l);
       }
-      if (m < p.rows && p.lse) {
+      if (p.cs > 1) {
+        // Clustered: keep (m, l) of the row for the cluster reduction below.
+        ml_stage[r] = make_float2(m_run, l_run);
+      } else if (m < p.rows && p.lse) {
         const int s = m / p.G;
         const int h = g * p.G + (m - s * p.G);
         p.lse[s * p.l_sb + h * p.l_sh + split * p.l_ss] = (m_run + __log2f(l_run)) * kLn2;
       }
+    } else if (p.cs > 1) {
+      ml_stage[r] = make_float2(kNegInf, 0.f);    // aborted: contributes nothing
     }
-    // The four warps of this query tile: named barrier 1 + t, 128 threads.
-    named_barrier_sync(1 + t, 128);
-    if (done) {
+    // The four softmax warps: named barrier 1, 128 threads.
+    named_barrier_sync(1, 128);
+    if (done && p.cs == 1) {
       for (int rr = quad; rr < C::MT; rr += 4) {
         const int m = m0 + rr;
         if (m >= p.rows) break;
@@ -422,6 +426,70 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   pdl_launch_dependents();
   tc::fence_before_sync();
   __syncthreads();
+  if (p.cs > 1) {
+    // Cluster reduction over the cs splits of this query tile (the cluster
+    // spans consecutive splits of one tile and kv head): every CTA has its
+    // normalised O rows and (m, l) staged in shared memory; CTA `rank`
+    // merges rows [rank * 128 / cs, (rank + 1) * 128 / cs) of all of them
+    // through distributed shared memory and writes one partial per row,
+    // partial slot split / cs:
+    //   M = max_k m_k,  w_k = l_k 2^(m_k - M),  O = sum_k w_k O_k / sum_k w_k
+    //   lse = (M + log2 sum_k w_k) ln 2.
+    // One warp per row; lane = 4 head-dim elements.
+    cluster_sync_all();
+    const uint32_t rank = cluster_ctarank();
+    const int rows_per = C::MT / p.cs;
+    const uint32_t stage_addr = smem_u32(smem);
+    const uint32_t ml_addr = smem_u32(smem + C::STAGE_BYTES);
+    for (int rr = warp; rr < rows_per; rr += C::THREADS / 32) {
+      const int row = (int)rank * rows_per + rr;
+      const int m = mtile * C::MT + row;
+      if (m >= p.rows) break;
+      float mk[8], lk[8];
+      float M = kNegInf;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k < p.cs) {
+          const float2 v = dsmem_ld_f2(dsmem_map(ml_addr + row * 8, (uint32_t)k));
+          mk[k] = v.x;
+          lk[k] = v.y;
+          M = fmaxf(M, v.x);
+        } else {
+          mk[k] = kNegInf;
+          lk[k] = 0.f;
+        }
+      }
+      float L = 0.f;
+      float wk[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        wk[k] = (mk[k] == kNegInf) ? 0.f : lk[k] * fast_exp2(mk[k] - M);
+        L += wk[k];
+      }
+      const float invL = L > 0.f ? 1.f / L : 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (k < p.cs && wk[k] != 0.f) {
+          const float4 v =
+              dsmem_ld_f4(dsmem_map(stage_addr + (row * (C::D + 4) + lane * 4) * 4, (uint32_t)k));
+          const float w = wk[k] * invL;
+          acc.x = fmaf(w, v.x, acc.x);
+          acc.y = fmaf(w, v.y, acc.y);
+          acc.z = fmaf(w, v.z, acc.z);
+          acc.w = fmaf(w, v.w, acc.w);
+        }
+      }
+      const int s = m / p.G;
+      const int h = g * p.G + (m - s * p.G);
+      const int slot = split / p.cs;
+      *reinterpret_cast<float4*>(p.o + s * p.o_sb + h * p.o_sh + slot * p.o_ss + lane * 4) = acc;
+      if (lane == 0 && p.lse)
+        p.lse[s * p.l_sb + h * p.l_sh + slot * p.l_ss] = L > 0.f ? (M + __log2f(L)) * kLn2 : kNegInf;
+    }
+    // No CTA leaves (and frees its shared memory) while a peer still reads it.
+    cluster_sync_all();
+  }
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, C::TMEM_COLS);

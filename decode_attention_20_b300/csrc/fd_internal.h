@@ -60,6 +60,8 @@ struct BifCtxParams {
   int rows;                   // n * G
   float scale_log2;           // |scale| * log2(e)
   int negate_q;               // 1: scale < 0, the kernel negates Q as it loads it
+  int cs;                     // CTAs per cluster along the splits (1, 2, 4 or 8); a
+                              // cluster merges its splits into partial slot split / cs
   float* o;                   // partial outputs, fp32
   int64_t o_sb, o_sh, o_ss;   // strides over (sample, q head, split)
   float* lse;                 // natural-log partial lse
@@ -68,8 +70,8 @@ struct BifCtxParams {
 
 // Tokens per tile, and 128-row query tiles per CTA, of the bifurcated
 // context kernel.
-constexpr int kBifTileTokens = 64;
-constexpr int kBifQueryTiles = 2;
+constexpr int kBifTileTokens = 128;
+constexpr int kBifQueryTiles = 1;
 
 // Host launchers (return a cudaError_t from the launch).  `pdl` launches
 // with programmatic stream serialisation (the kernel may start while the

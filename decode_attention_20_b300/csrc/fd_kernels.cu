@@ -169,8 +169,23 @@ cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const 
     if (e != cudaSuccess) return e;
     attr_set |= bit;
   }
-  return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
-                   BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV);
+  if (p.cs <= 1)
+    return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
+                     BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV);
+  // Clusters of cs CTAs along the splits (grid.y is a multiple of cs).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(mtiles, p.ns, p.Hkv);
+  cfg.blockDim = dim3(BifCfg::THREADS);
+  cfg.dynamicSmemBytes = BifCfg::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = p.cs;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bif_ctx_kernel, p, tmK, tmV);
 }
 
 }  // namespace fd

@@ -76,9 +76,14 @@ def test_bifurcated_mqa_sampling_workload(cuda_device):
 # oracle, across M-tile tails, context tails, split counts and a peaked
 # softmax that makes the running max jump (accumulator rescaling).
 
-@pytest.fixture(params=["tc", "split"])
+@pytest.fixture(params=["tc", "tc_cluster", "split"])
 def ctx_path(request, monkeypatch):
-    monkeypatch.setenv("FD_BIF_CTX", request.param)
+    """tc: tensor-core context kernel, one partial per split (default);
+    tc_cluster: the same kernel with its splits merged in thread-block
+    clusters of up to 8 CTAs where they divide evenly; split: the split
+    kernel over a broadcast view of the context."""
+    monkeypatch.setenv("FD_BIF_CTX", "split" if request.param == "split" else "tc")
+    monkeypatch.setenv("FD_BIF_CLUSTER", "8" if request.param == "tc_cluster" else "1")
     return request.param
 
 
@@ -89,6 +94,9 @@ def ctx_path(request, monkeypatch):
     (3, 2, 64, 129, 5, 2),         # G = 64, second split holds one token
     (16, 1, 8, 4173, 20, 1),       # one split streams 33 tiles (rings wrap many times)
     (2, 1, 1, 700, 9, 0),          # G = 1
+    (12, 1, 32, 2000, 17, 4),      # 4 splits of 512 tokens: one cluster of 4
+    (12, 1, 32, 2000, 17, 8),      # 8 splits, the last holds 208 tokens: cluster of 8
+    (9, 2, 16, 1500, 3, 2),        # cluster of 2, GQA, M-tile tail
 ])
 def test_bifurcated_ctx_paths(cuda_device, ctx_path, n, hkv, G, lc, ld, ctx_splits):
     case = inputs.bifurcated_case(n, hkv * G, hkv, 128, lc, ld, seed=n * 7 + G,
