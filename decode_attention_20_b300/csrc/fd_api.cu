@@ -877,6 +877,8 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   void* ws = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)bytes, info->pool, cs);
   if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  // Partials slot-major, [S][n][Hq][D] and [S][n][Hq]: a context CTA's 128
+  // rows are then one contiguous block (for one kv head).
   float* po = reinterpret_cast<float*>(ws);
   float* pl = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + ((n * Hq * S * D * 4 + 255) / 256) * 256);
 
@@ -904,13 +906,13 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         bp.negate_q = scale < 0.f ? 1 : 0;
         bp.cs = csize;
         bp.o = po;
-        bp.o_sb = Hq * S * D;
-        bp.o_sh = S * D;
-        bp.o_ss = D;
+        bp.o_sb = Hq * D;
+        bp.o_sh = D;
+        bp.o_ss = n * Hq * D;
         bp.lse = pl;
-        bp.l_sb = Hq * S;
-        bp.l_sh = S;
-        bp.l_ss = 1;
+        bp.l_sb = Hq;
+        bp.l_sh = 1;
+        bp.l_ss = n * Hq;
         ProfRecord rec;
         const bool prof = prof_begin(FD_KERNEL_BIF_CTX, cs, &rec);
         e = launch_bif_ctx(bp, tmK, tmV, (int)mtiles, cs, !prof);
@@ -924,8 +926,8 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
     // Context part on the split kernel: every sample reads the one shared
     // context through a batch-broadcast view (batch stride 0).
     DecodeDesc dc = {n, Hq, Hkv, D, Lc, Hq / Hkv, FD_BF16, FD_BF16};
-    st = enqueue_split(dc, q, k_ctx, v_ctx, nullptr, ns_ctx, scale, po, Hq * S * D, S * D, D, pl,
-                       Hq * S, S, 1, true, cs);
+    st = enqueue_split(dc, q, k_ctx, v_ctx, nullptr, ns_ctx, scale, po, Hq * D, D, n * Hq * D, pl,
+                       Hq, 1, n * Hq, true, cs);
   }
   // Decode part: each sample's own tokens, ns_dec splits, written after
   // the context splits.
@@ -933,19 +935,20 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
     DecodeDesc dd = {n, Hq, Hkv, D, Ld, Hq / Hkv, FD_BF16, FD_BF16};
     st = enqueue_split(dd, q, k_dec, v_dec,
                        dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr,
-                       ns_dec, scale, po + (int64_t)(ns_ctx / csize) * D, Hq * S * D, S * D, D,
-                       pl + ns_ctx / csize, Hq * S, S, 1, false, cs);
+                       ns_dec, scale, po + (int64_t)(ns_ctx / csize) * n * Hq * D, Hq * D, D,
+                       n * Hq * D, pl + (int64_t)(ns_ctx / csize) * n * Hq, Hq, 1, n * Hq, false,
+                       cs);
   }
   if (st == FD_OK) {
     CombineParams cp = {};
     cp.part_o = po;
-    cp.po_r1 = Hq * S * D;
-    cp.po_r2 = S * D;
-    cp.po_s = D;
+    cp.po_r1 = Hq * D;
+    cp.po_r2 = D;
+    cp.po_s = n * Hq * D;
     cp.part_lse = pl;
-    cp.pl_r1 = Hq * S;
-    cp.pl_r2 = S;
-    cp.pl_s = 1;
+    cp.pl_r1 = Hq;
+    cp.pl_r2 = 1;
+    cp.pl_s = n * Hq;
     cp.out = reinterpret_cast<float*>(out->data);
     cp.out_r1 = out->stride[0];
     cp.out_r2 = out->stride[1];

@@ -409,17 +409,17 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     } else if (p.cs > 1) {
       ml_stage[r] = make_float2(kNegInf, 0.f);    // aborted: contributes nothing
     }
-    // The four softmax warps: named barrier 1, 128 threads.
-    named_barrier_sync(1, 128);
     if (done && p.cs == 1) {
-      for (int rr = quad; rr < C::MT; rr += 4) {
-        const int m = m0 + rr;
-        if (m >= p.rows) break;
+      // Each thread hands its own staged row to the bulk-copy engine (one
+      // 512-byte copy), after making its shared-memory writes visible to
+      // the async proxy, and waits for the copy before the CTA can exit.
+      const int m = m0 + r;
+      tc::fence_proxy_async_smem();
+      if (m < p.rows) {
         const int s = m / p.G;
         const int h = g * p.G + (m - s * p.G);
-        float* o = p.o + s * p.o_sb + h * p.o_sh + split * p.o_ss;
-        *reinterpret_cast<float4*>(o + lane * 4) =
-            *reinterpret_cast<const float4*>(stage + rr * SROW + lane * 4);
+        bulk_store(p.o + s * p.o_sb + h * p.o_sh + split * p.o_ss, stage + r * SROW, C::D * 4);
+        bulk_store_commit_and_wait();
       }
     }
   }
