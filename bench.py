@@ -1,7 +1,8 @@
 """Benchmark of the decode-attention hot path on one B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
-                    [--workload b1_64k|ragged_b32|long_b4|bif_mqa] [--num-splits S]
+                    [--workload b1_64k|ragged_b32|long_b4|bif_mqa|paged_b1_64k]
+                    [--num-splits S]
 
 Default workload: split-KV decode attention at batch 1 over a 65536-token
 history of a CodeLlama-34B-shaped layer (64 query heads, 8 kv heads, head
@@ -13,6 +14,8 @@ kernel + log-sum-exp combine) over the whole history.  Other workloads:
   bif_mqa     bifurcated attention: 64 samples share an 8192-token context,
               256 own decode tokens each, 32 query heads on 1 kv head; the
               line also carries the replicated-context decode time
+  paged_b1_64k the batch-1 64K layer with its history in 64-token pages
+              scattered by a seeded permutation (paged KV cache)
 Prints ONE JSON line (rank 0):
   value        device-timed microseconds per call: CUDA events around K calls
                replayed from a CUDA graph, inputs resident in HBM and rotated
@@ -446,6 +449,99 @@ class BifWorkload(Workload):
             f"tokens per call, extrapolated linearly to {self.n} samples"), dt
 
 
+class PagedWorkload(DecodeWorkload):
+    """The batch-1 64K layer with its history in scattered 64-token pages
+    (fd_decode_attention_paged)."""
+
+    def __init__(self, device):
+        import torch
+        from decode_attention_20_b300 import inputs
+        self.short = "paged_b1_64k"
+        c = self.pcase = inputs.paged_flash_decoding_b1(65536, 64, device=device)
+        self.name = c.name
+        self.B, self.Hq, self.D = c.q.shape
+        self.Hkv = c.k_pages.shape[2]
+        self.page_size = c.page_size
+        self.Lcap = c.block_table.shape[1] * c.page_size
+        self.lens = c.lens
+        self.seqlens_dev = None
+        self.bt_dev = c.block_table.to(device)
+        kv_bytes = c.k_pages.numel() * c.k_pages.element_size() * 2
+        self.nbuf = max(1, min(8, math.ceil(2 * L2_BYTES / kv_bytes) + (1 if kv_bytes < 4 * L2_BYTES else 0)))
+        self.ks = [c.k_pages] + [c.k_pages.clone() for _ in range(self.nbuf - 1)]
+        self.vs = [c.v_pages] + [c.v_pages.clone() for _ in range(self.nbuf - 1)]
+        self.out = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=device)
+        self.lse = torch.empty((self.B, self.Hq), dtype=torch.float32, device=device)
+        self.kv_req = sum(self.lens) * self.Hkv * self.D * 2 * 2
+        self.required = self.kv_req + c.q.numel() * 2 + self.out.numel() * 4 + self.lse.numel() * 4
+        self.dominant_units = self.kv_req + c.q.numel() * 2
+        self.bound, self.unit = "hbm", "GB/s"
+        # the oracle sample and e2e reuse the contiguous view of the same tokens
+        from decode_attention_20_b300.inputs import DecodeCase
+        bt = c.block_table.to(c.k_pages.device).long()
+        kc = c.k_pages[bt].reshape(1, self.Lcap, self.Hkv, self.D)
+        vc = c.v_pages[bt].reshape(1, self.Lcap, self.Hkv, self.D)
+        self.case = DecodeCase(name=c.name, q=c.q, k=kc, v=vc, seqlens=None, scale=c.scale)
+
+    def config(self, ns):
+        cfg = super().config(ns)
+        cfg["page_size"] = self.page_size
+        return cfg
+
+    def prepare(self, L, stream, ns):
+        from decode_attention_20_b300.api import _desc
+        c = self.pcase
+        self.ns = ns
+        self.dq, self.do, self.dl = _desc(c.q, "q"), _desc(self.out, "out"), _desc(self.lse, "lse")
+        self.dbt = _desc(self.bt_dev, "block_table")
+        self.dks = [_desc(x, "k") for x in self.ks]
+        self.dvs = [_desc(x, "v") for x in self.vs]
+        self.L = L
+        self.sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def call(self, i):
+        r = ctypes.byref
+        st = self.L.fd_decode_attention_paged(r(self.dq), r(self.dks[i % self.nbuf]),
+                                              r(self.dvs[i % self.nbuf]), r(self.dbt), None,
+                                              self.ns, ctypes.c_float(self.pcase.scale), r(self.do),
+                                              r(self.dl), self.sptr)
+        if st:
+            raise RuntimeError(self.L.fd_last_error().decode())
+
+    def e2e(self, stream, steps):
+        """Per step: H2D of the new query and of the newest token's K/V row
+        into its page, the paged call, D2H of out + lse."""
+        import torch
+        import decode_attention_20_b300 as fd
+        c = self.pcase
+        hq = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
+        hq.copy_(c.q.cpu())
+        last = self.Lcap - 1
+        pid = int(c.block_table[0, last // self.page_size])
+        row = pid * self.page_size + last % self.page_size
+        hk = torch.empty((1, self.Hkv * self.D), dtype=c.k_pages.dtype).pin_memory()
+        hv = torch.empty_like(hk).pin_memory()
+        hk.copy_(c.k_pages.view(-1, self.Hkv * self.D)[row:row + 1].cpu())
+        hv.copy_(c.v_pages.view(-1, self.Hkv * self.D)[row:row + 1].cpu())
+        hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
+        hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
+                c.q.copy_(hq, non_blocking=True)
+                kb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(hk, non_blocking=True)
+                vb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(hv, non_blocking=True)
+                fd.decode_attention_paged(c.q, kb, vb, self.bt_dev, None, self.ns, c.scale,
+                                          out=self.out, lse=self.lse, stream=stream)
+                hout.copy_(self.out, non_blocking=True)
+                hlse.copy_(self.lse, non_blocking=True)
+                stream.synchronize()
+        us = (time.perf_counter() - t0) * 1e6 / steps
+        return us, hq.numel() * 2 + hk.numel() * 2 * 2, hout.numel() * 4 + hlse.numel() * 4
+
+
 def make_workload(short, device):
     from decode_attention_20_b300 import inputs
     if short == "b1_64k":
@@ -456,6 +552,8 @@ def make_workload(short, device):
         return DecodeWorkload(short, lambda d: inputs.long_context_peaked(device=d), device)
     if short == "bif_mqa":
         return BifWorkload(device)
+    if short == "paged_b1_64k":
+        return PagedWorkload(device)
     raise SystemExit(f"unknown workload {short}")
 
 
@@ -525,14 +623,18 @@ def run_fd(args, rank, world):
     fd.check_device_error(stream)
 
     # CUDA graph of nbuf consecutive calls (one per rotating input copy)
-    reps = max(1, math.ceil(args.steps / w.nbuf))
-    steps = reps * w.nbuf
+    # One graph holds at least 16 back-to-back calls (cycling the rotating
+    # input copies), so graph-launch boundaries, which break the
+    # programmatic overlap of consecutive calls, are rare.
+    glen = w.nbuf * max(1, math.ceil(16 / w.nbuf))
+    reps = max(1, math.ceil(args.steps / glen))
+    steps = reps * glen
     graph = None
-    timing = f"CUDA graph of {w.nbuf} calls, replayed"
+    timing = f"CUDA graph of {glen} calls, replayed"
     try:
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(w.nbuf):
+            for i in range(glen):
                 w.call(i)
         for _ in range(2):
             g.replay()
@@ -722,7 +824,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="b1_64k",
-                    choices=["b1_64k", "ragged_b32", "long_b4", "bif_mqa"])
+                    choices=["b1_64k", "ragged_b32", "long_b4", "bif_mqa", "paged_b1_64k"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -68,6 +68,27 @@ def decode_attention(q, k_cache, v_cache, seqlens=None, num_splits=0, scale=None
     return out, lse
 
 
+def decode_attention_paged(q, k_pages, v_pages, block_table, seqlens=None, num_splits=0,
+                           scale=None, out=None, lse=None, return_lse=True, stream=None):
+    """Split-KV decode attention over a paged cache
+    (fd_decode_attention_paged): k_pages, v_pages [num_pages, page_size,
+    Hkv, D]; block_table [B, max_pages] int32 CUDA tensor; seqlens [B] int32
+    or None.  Returns (out [B,Hq,D] fp32, lse [B,Hq] fp32 or None)."""
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    a = [_desc(q, "q"), _desc(k_pages, "k_pages"), _desc(v_pages, "v_pages"),
+         _desc(block_table, "block_table"), _desc(seqlens, "seqlens")]
+    do, dl = _desc(out, "out"), _desc(lse, "lse")
+    check(lib().fd_decode_attention_paged(*[_ref(x) for x in a], int(num_splits), float(scale),
+                                          _ref(do), _ref(dl), _stream(stream)))
+    return out, lse
+
+
 def decode_attention_partials(q, k_cache, v_cache, num_splits, seqlens=None, scale=None,
                               part_o=None, part_lse=None, stream=None):
     """The split stage alone (fd_decode_attention_partials): returns

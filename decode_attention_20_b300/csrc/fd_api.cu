@@ -293,13 +293,14 @@ bool tma_ok(const DecodeDesc& d, const void* kd, const void* vd, const int64_t (
 
 // Which split kernel variant to use.  Tuning and test knob, read on every
 // call: FD_SPLIT_VARIANT = "cuda" forces the CUDA-core kernel, "mma0" /
-// "mma1" / "mma2" pick a tensor-core tiling.  Unset: "mma0" (6-stage ring,
-// one CTA per SM) for splits that stream more than three 64-token tiles,
-// "mma2" (3-stage ring, two CTAs per SM) for shorter ones, where a deep ring
-// cannot fill and a second resident CTA hides the start-up latency instead.
+// "mma1" / "mma2" pick a tensor-core tiling.  Unset: "mma2" (3-stage ring of
+// 64-token tiles, two CTAs per SM): in the split-count sweeps it matched the
+// 6-stage one-CTA-per-SM tiling at batch 1 and beat it by 5% on the ragged
+// batch, the second resident CTA covering the first one's start and tail.
 int split_variant(int64_t chunk_tokens) {
+  (void)chunk_tokens;
   const char* e = getenv("FD_SPLIT_VARIANT");
-  if (e == nullptr || e[0] == 0) return chunk_tokens <= 3 * 64 ? 2 : 0;
+  if (e == nullptr || e[0] == 0) return 2;
   if (!strcmp(e, "cuda")) return -1;
   if (!strcmp(e, "mma1")) return 1;
   if (!strcmp(e, "mma2")) return 2;
@@ -310,9 +311,10 @@ bool mma_group_ok(int64_t G) { return G == 4 || G == 8 || G == 16 || G == 32 || 
 
 // Split-count heuristic: the smallest ns with the lowest makespan
 // waves(ns) * (chunk(ns) + kSplitOverheadTokens), where chunk is the
-// fd_split_bounds chunk of a max_len history and waves counts rounds of one
-// CTA per SM over batch * kv_heads * (non-empty splits) CTAs; ns is capped at
-// ceil(max_len / 256) and FD_MAX_SPLITS.
+// fd_split_bounds chunk of a max_len history and waves counts rounds of two
+// CTAs per SM (the default split kernel's occupancy) over batch * kv_heads *
+// (non-empty splits) CTAs; ns is capped at ceil(max_len / 256) and
+// FD_MAX_SPLITS.
 int32_t choose_splits_host(int64_t batch, int64_t kv_heads, int64_t max_len, int32_t num_sms) {
   constexpr int64_t kMinChunk = 256;
   constexpr int64_t kSplitOverheadTokens = 256;
@@ -326,7 +328,7 @@ int32_t choose_splits_host(int64_t batch, int64_t kv_heads, int64_t max_len, int
     const int64_t per = (max_len + ns - 1) / ns;
     const int64_t chunk = ((per + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
     const int64_t used = (max_len + chunk - 1) / chunk;
-    const int64_t waves = (units * used + num_sms - 1) / num_sms;
+    const int64_t waves = (units * used + 2 * (int64_t)num_sms - 1) / (2 * (int64_t)num_sms);
     const int64_t cost = waves * (chunk + kSplitOverheadTokens);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
@@ -337,12 +339,29 @@ int32_t choose_splits_host(int64_t batch, int64_t kv_heads, int64_t max_len, int
 }
 
 // Enqueue the split stage for one cache.
+// A paged cache: k / v tensors are [num_pages, page_size, Hkv, D].
+struct PageDesc {
+  const int32_t* table;       // [B, max_pages] device
+  int64_t stride;             // elements between rows of the table
+  int page_size, num_pages;
+};
+
+// Page sizes the TMA split kernel streams (every box stays inside a page).
+bool page_size_tma_ok(int ps) { return ps == 16 || ps == 32 || (ps >= 64 && ps % 64 == 0); }
+
 fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor* k,
                         const fd_tensor* v, const int32_t* seqlens, int ns, float scale,
                         float* o, int64_t o_sb, int64_t o_sh, int64_t o_ss, float* lse,
                         int64_t l_sb, int64_t l_sh, int64_t l_ss, bool kv_broadcast,
-                        cudaStream_t st) {
+                        cudaStream_t st, const PageDesc* pg = nullptr) {
   SplitParams p = {};
+  if (pg) {
+    p.block_table = pg->table;
+    p.bt_stride = pg->stride;
+    p.page_size = pg->page_size;
+    p.num_pages = pg->num_pages;
+    p.page_rows = pg->page_size < 64 ? pg->page_size : 64;
+  }
   p.q = q->data;
   p.q_sb = q->stride[0];
   p.q_sh = q->stride[1];
@@ -379,18 +398,22 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   ProfRecord rec;
   bool launched = false;
   cudaError_t e = cudaSuccess;
-  const int64_t kv_batch = kv_broadcast ? 1 : d.B;
+  // The tensor maps span the kv batch, or for a paged cache the pages (a
+  // page is a "sequence" of page_size tokens, boxes page_rows tall).
+  const int64_t kv_batch = pg ? pg->num_pages : (kv_broadcast ? 1 : d.B);
+  const int64_t map_len = pg ? pg->page_size : d.Lcap;
   const int64_t strides[6] = {p.k_sl, p.k_sh, p.v_sl, p.v_sh, p.k_sb, p.v_sb};
   const int variant = split_variant(split_chunk(d.Lcap, ns));
   if (variant >= 0 && d.q_dt == FD_BF16 && mma_group_ok(d.G) &&
-      d.Lcap >= mma_tile_tokens(variant) && tma_ok(d, k->data, v->data, strides, kv_batch)) {
+      d.Lcap >= mma_tile_tokens(variant) && tma_ok(d, k->data, v->data, strides, kv_batch) &&
+      (!pg || page_size_tma_ok(pg->page_size))) {
     fd_status gs = get_encoder();
     if (gs) return gs;
     CUtensorMap tmK, tmV;
-    const int tile = mma_tile_tokens(variant);
-    const bool okk = make_kv_map(&tmK, k->data, kv_batch, d.Lcap, d.Hkv, d.D, p.k_sb, p.k_sl,
+    const int tile = pg ? p.page_rows : mma_tile_tokens(variant);
+    const bool okk = make_kv_map(&tmK, k->data, kv_batch, map_len, d.Hkv, d.D, p.k_sb, p.k_sl,
                                  p.k_sh, tile, 64);
-    const bool okv = make_kv_map(&tmV, v->data, kv_batch, d.Lcap, d.Hkv, d.D, p.v_sb, p.v_sl,
+    const bool okv = make_kv_map(&tmV, v->data, kv_batch, map_len, d.Hkv, d.D, p.v_sb, p.v_sl,
                                  p.v_sh, tile, 64);
     if (okk && okv) {
       const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
@@ -403,7 +426,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
       if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
     }
   }
-  if (!launched && tma_ok(d, k->data, v->data, strides, kv_batch)) {
+  if (!launched && !pg && tma_ok(d, k->data, v->data, strides, kv_batch)) {
     fd_status gs = get_encoder();
     if (gs) return gs;
     CUtensorMap tmK, tmV;
@@ -581,16 +604,17 @@ int64_t fd_workspace_bytes(int64_t batch, int64_t q_heads, int64_t head_dim, int
   return workspace_bytes(batch, q_heads, head_dim, num_splits);
 }
 
-fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
-                              const fd_tensor* v_cache, const fd_tensor* seqlens,
-                              int32_t num_splits, float scale, fd_tensor* out, fd_tensor* lse,
-                              fd_stream stream) {
-  DecodeDesc d;
-  fd_status st = validate_decode(q, k_cache, v_cache, seqlens, out, lse, 3, 0, &d);
-  if (st) return st;
-  if (num_splits < 0 || num_splits > kMaxSplits)
-    return fail(FD_ERR_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
-  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+}  // extern "C"
+
+namespace {
+
+// Split stage + log-sum-exp combine into out / lse, workspace from the
+// library pool (shared by the contiguous and the paged entry points).
+fd_status run_decode(const DecodeDesc& d, const fd_tensor* q, const fd_tensor* k_cache,
+                     const fd_tensor* v_cache, const fd_tensor* seqlens, int32_t num_splits,
+                     float scale, fd_tensor* out, fd_tensor* lse, fd_stream stream,
+                     const PageDesc* pg) {
+  fd_status st;
   int dev;
   DeviceInfo* info;
   if ((st = current_device(&dev, &info))) return st;
@@ -602,7 +626,8 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
   float* l = lse ? reinterpret_cast<float*>(lse->data) : nullptr;
   if (ns == 1) {
     return enqueue_split(d, q, k_cache, v_cache, sl, 1, scale, o, out->stride[0], out->stride[1],
-                         0, l, lse ? lse->stride[0] : 0, lse ? lse->stride[1] : 0, 0, false, cs);
+                         0, l, lse ? lse->stride[0] : 0, lse ? lse->stride[1] : 0, 0, false, cs,
+                         pg);
   }
   const int64_t bytes = workspace_bytes(d.B, d.Hq, d.D, ns);
   void* ws = nullptr;
@@ -612,7 +637,7 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
   float* pl = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
                                        ((d.B * d.Hq * ns * d.D * 4 + 255) / 256) * 256);
   st = enqueue_split(d, q, k_cache, v_cache, sl, ns, scale, po, d.Hq * ns * d.D, ns * d.D, d.D,
-                     pl, d.Hq * ns, ns, 1, false, cs);
+                     pl, d.Hq * ns, ns, 1, false, cs, pg);
   if (st == FD_OK) {
     CombineParams cp = {};
     cp.part_o = po;
@@ -639,6 +664,81 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
   if (st) return st;
   if (e != cudaSuccess) return cuda_fail(e, "workspace release");
   return FD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
+                              const fd_tensor* v_cache, const fd_tensor* seqlens,
+                              int32_t num_splits, float scale, fd_tensor* out, fd_tensor* lse,
+                              fd_stream stream) {
+  DecodeDesc d;
+  fd_status st = validate_decode(q, k_cache, v_cache, seqlens, out, lse, 3, 0, &d);
+  if (st) return st;
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
+  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  return run_decode(d, q, k_cache, v_cache, seqlens, num_splits, scale, out, lse, stream, nullptr);
+}
+
+fd_status fd_decode_attention_paged(const fd_tensor* q, const fd_tensor* k_pages,
+                                    const fd_tensor* v_pages, const fd_tensor* block_table,
+                                    const fd_tensor* seqlens, int32_t num_splits, float scale,
+                                    fd_tensor* out, fd_tensor* lse, fd_stream stream) {
+  fd_status st;
+  if ((st = check_tensor(q, "q", 3))) return st;
+  if ((st = check_tensor(k_pages, "k_pages", 4))) return st;
+  if ((st = check_tensor(v_pages, "v_pages", 4))) return st;
+  if ((st = check_tensor(block_table, "block_table", 2))) return st;
+  if ((st = check_tensor(out, "out", 3))) return st;
+  if (lse && (st = check_tensor(lse, "lse", 2))) return st;
+  if (seqlens && (st = check_tensor(seqlens, "seqlens", 1))) return st;
+  DecodeDesc d;
+  d.B = q->shape[0];
+  d.Hq = q->shape[1];
+  d.D = q->shape[2];
+  const int64_t P = k_pages->shape[0], ps = k_pages->shape[1];
+  d.Hkv = k_pages->shape[2];
+  for (int i = 0; i < 4; ++i)
+    if (k_pages->shape[i] != v_pages->shape[i])
+      return fail(FD_ERR_SHAPE, "k_pages and v_pages shapes differ");
+  if (k_pages->shape[3] != d.D) return fail(FD_ERR_SHAPE, "k_pages head dim != q head dim");
+  if (block_table->dtype != FD_I32) return fail(FD_ERR_DTYPE, "block_table must be int32");
+  if (block_table->shape[0] != d.B) return fail(FD_ERR_SHAPE, "block_table must have B rows");
+  if (block_table->stride[1] != 1 && block_table->shape[1] > 1)
+    return fail(FD_ERR_LAYOUT, "block_table rows must be contiguous");
+  if (ps < 1 || P < 1) return fail(FD_ERR_SHAPE, "k_pages must hold at least one page of one token");
+  d.Lcap = block_table->shape[1] * ps;
+  if (q->dtype != FD_BF16 && q->dtype != FD_F32) return fail(FD_ERR_DTYPE, "q must be bf16 or f32");
+  if (k_pages->dtype != v_pages->dtype) return fail(FD_ERR_DTYPE, "k_pages and v_pages dtypes differ");
+  if (k_pages->dtype != FD_BF16 && k_pages->dtype != FD_F32)
+    return fail(FD_ERR_DTYPE, "k_pages / v_pages must be bf16 or f32");
+  if (out->dtype != FD_F32 || (lse && lse->dtype != FD_F32)) return fail(FD_ERR_DTYPE, "out / lse must be f32");
+  if (out->shape[0] != d.B || out->shape[1] != d.Hq || out->shape[2] != d.D)
+    return fail(FD_ERR_SHAPE, "out must be [B, Hq, D]");
+  if (lse && (lse->shape[0] != d.B || lse->shape[1] != d.Hq)) return fail(FD_ERR_SHAPE, "lse must be [B, Hq]");
+  if (seqlens) {
+    if (seqlens->dtype != FD_I32) return fail(FD_ERR_DTYPE, "seqlens must be int32");
+    if (seqlens->shape[0] != d.B) return fail(FD_ERR_SHAPE, "seqlens must have B entries");
+    if (seqlens->stride[0] != 1 && d.B > 1) return fail(FD_ERR_LAYOUT, "seqlens must be contiguous");
+  }
+  if (d.Hkv < 1 || d.Hq < 1 || d.Hq % d.Hkv != 0)
+    return fail(FD_ERR_UNSUPPORTED, "Hq must be a positive multiple of Hkv");
+  if (d.D != 64 && d.D != 128) return fail(FD_ERR_UNSUPPORTED, "head dim not in {64, 128}");
+  if (d.B > 65535 || d.Hq > 65535) return fail(FD_ERR_UNSUPPORTED, "batch and query heads must be <= 65535");
+  if (d.Lcap > (int64_t)INT32_MAX - 2 * kSplitAlign || P > INT32_MAX)
+    return fail(FD_ERR_UNSUPPORTED, "paged cache too large");
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
+  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  d.G = d.Hq / d.Hkv;
+  d.q_dt = q->dtype;
+  d.kv_dt = k_pages->dtype;
+  PageDesc pg = {reinterpret_cast<const int32_t*>(block_table->data), block_table->stride[0],
+                 (int)ps, (int)P};
+  return run_decode(d, q, k_pages, v_pages, seqlens, num_splits, scale, out, lse, stream, &pg);
 }
 
 fd_status fd_decode_attention_noalloc(const fd_tensor* q, const fd_tensor* k_cache,

@@ -35,6 +35,13 @@ struct SplitParams {
   float* lse;                 // natural-log lse, or nullptr
   int64_t l_sb, l_sh, l_ss;
   int kv_batch_broadcast;     // 1: every sequence reads kv batch row 0
+  // Paged cache (block_table != nullptr): k / v are [num_pages, page_size,
+  // Hkv, D]; token j of sequence b is row j % page_size of page
+  // block_table[b * bt_stride + j / page_size].  The TMA kernels load
+  // page_rows = min(64, page_size) rows per box.
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int page_size, num_pages, page_rows;
 };
 
 // Arguments of the log-sum-exp combine kernel.

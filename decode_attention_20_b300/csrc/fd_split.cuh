@@ -67,6 +67,17 @@ __device__ __forceinline__ int resolve_len(const int32_t* seqlens, int b, int ca
   return len;
 }
 
+// Page of token j of sequence b in a paged cache; an id outside
+// [0, num_pages) raises the device bounds flag and is replaced by `bad`.
+__device__ __forceinline__ int page_of(const SplitParams& p, int b, int j, int bad) {
+  int pid = p.block_table[(int64_t)b * p.bt_stride + j / p.page_size];
+  if (pid < 0 || pid >= p.num_pages) {
+    raise_device_error(FD_DEVERR_BOUNDS);
+    pid = bad;
+  }
+  return pid;
+}
+
 template <int N>
 struct Log2 {
   static constexpr int value = 1 + Log2<N / 2>::value;
@@ -449,8 +460,18 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
   float m = kNegInf, l = 0.f;
   for (int j = begin + warp; j < end; j += NW) {
     float kf[EPL], vf[EPL];
-    const int64_t ko = b * p.k_sb + (int64_t)j * p.k_sl + g * p.k_sh + lane * EPL;
-    const int64_t vo = b * p.v_sb + (int64_t)j * p.v_sl + g * p.v_sh + lane * EPL;
+    int64_t kbase, vbase;
+    if (p.block_table) {                       // paged: clamp bad ids to page 0
+      const int pid = page_of(p, b, j, 0);
+      const int off = j % p.page_size;
+      kbase = (int64_t)pid * p.k_sb + (int64_t)off * p.k_sl;
+      vbase = (int64_t)pid * p.v_sb + (int64_t)off * p.v_sl;
+    } else {
+      kbase = b * p.k_sb + (int64_t)j * p.k_sl;
+      vbase = b * p.v_sb + (int64_t)j * p.v_sl;
+    }
+    const int64_t ko = kbase + g * p.k_sh + lane * EPL;
+    const int64_t vo = vbase + g * p.v_sh + lane * EPL;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       if (KV_BF16) {

@@ -154,10 +154,28 @@ __global__ void __launch_bounds__(W * 32, 1)
     unsigned char* stage = smem + s * C::STAGE_BYTES;
     mbar_arrive_expect_tx(&full_bar[s], C::STAGE_BYTES);
     const int tok = begin + t * C::T;
-    tma_load_4d(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
-    tma_load_4d(stage + C::HALF_BYTES, &tmK, &full_bar[s], 64, g, tok, kvb, policy);
-    tma_load_4d(stage + 2 * C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
-    tma_load_4d(stage + 3 * C::HALF_BYTES, &tmV, &full_bar[s], 64, g, tok, kvb, policy);
+    if (p.block_table == nullptr) {
+      tma_load_4d(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
+      tma_load_4d(stage + C::HALF_BYTES, &tmK, &full_bar[s], 64, g, tok, kvb, policy);
+      tma_load_4d(stage + 2 * C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
+      tma_load_4d(stage + 3 * C::HALF_BYTES, &tmV, &full_bar[s], 64, g, tok, kvb, policy);
+    } else {
+      // Paged cache: the tile is page_rows-row segments, each inside one page
+      // (tiles start on multiples of 64 tokens; page_rows = min(64, page
+      // size) divides both).  Segments past the split's end load page -1:
+      // out of range, so the copy fills zeros (and still counts its bytes).
+      const int nseg = C::T / p.page_rows;
+      for (int sg = 0; sg < nseg; ++sg) {
+        const int tk = tok + sg * p.page_rows;
+        const int pid = tk < end ? page_of(p, b, tk, -1) : -1;
+        const int off = tk % p.page_size;
+        const int so = sg * p.page_rows * 128;
+        tma_load_4d(stage + so, &tmK, &full_bar[s], 0, g, off, pid, policy);
+        tma_load_4d(stage + C::HALF_BYTES + so, &tmK, &full_bar[s], 64, g, off, pid, policy);
+        tma_load_4d(stage + 2 * C::HALF_BYTES + so, &tmV, &full_bar[s], 0, g, off, pid, policy);
+        tma_load_4d(stage + 3 * C::HALF_BYTES + so, &tmV, &full_bar[s], 64, g, off, pid, policy);
+      }
+    }
   };
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tmK);

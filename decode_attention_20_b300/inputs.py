@@ -214,3 +214,69 @@ def replicate_context(case: BifurcatedCase):
     lens = torch.tensor([lc + x for x in case.lens], dtype=torch.int32)
     return DecodeCase(name=case.name + "_replicated", q=case.q, k=k, v=v,
                       seqlens=lens, scale=case.scale)
+
+
+@dataclass
+class PagedCase:
+    """Decode attention over a paged cache: q [B,Hq,D], k/v pages
+    [num_pages, page_size, Hkv, D], block_table [B, max_pages] int32 (CPU),
+    seqlens [B] int32 (CPU) or None."""
+    name: str
+    q: torch.Tensor
+    k_pages: torch.Tensor
+    v_pages: torch.Tensor
+    block_table: torch.Tensor
+    seqlens: Optional[torch.Tensor]
+    page_size: int
+    scale: float
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def lens(self):
+        B, mp = self.block_table.shape
+        if self.seqlens is None:
+            return [mp * self.page_size] * B
+        return [int(x) for x in self.seqlens.tolist()]
+
+
+def paged_case(batch, hq, hkv, d, page_size, max_pages, num_pages=None, dtype=torch.bfloat16,
+               seed=0, seqlens=None, ragged=None, shared_prefix_pages=0, device="cpu",
+               scale=None, name="paged"):
+    """Paged workload: N(0,1) pages; each sequence's block table is a slice
+    of one seeded permutation of the pages (sequences own distinct pages),
+    except that the first ``shared_prefix_pages`` entries of every row
+    point at sequence 0's first pages (a shared prefix)."""
+    if num_pages is None:
+        num_pages = batch * max_pages
+    g = _gen(seed, device)
+    q = _randn((batch, hq, d), dtype, g, device)
+    k_pages = _randn((num_pages, page_size, hkv, d), dtype, g, device)
+    v_pages = _randn((num_pages, page_size, hkv, d), dtype, g, device)
+    extra = _gen(seed + 1, "cpu")
+    perm = torch.randperm(num_pages, generator=extra)
+    need = batch * max_pages
+    if need > num_pages:
+        raise ValueError("num_pages must cover batch * max_pages")
+    bt = perm[:need].reshape(batch, max_pages).to(torch.int32)
+    if shared_prefix_pages:
+        bt[:, :shared_prefix_pages] = bt[0, :shared_prefix_pages]
+    lens_t = None
+    cap = max_pages * page_size
+    if ragged is not None:
+        lo, hi = ragged
+        lens_t = torch.randint(lo, hi + 1, (batch,), generator=extra, dtype=torch.int64).to(torch.int32)
+    elif seqlens is not None:
+        lens_t = torch.tensor(list(seqlens), dtype=torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return PagedCase(name=name, q=q, k_pages=k_pages, v_pages=v_pages, block_table=bt,
+                     seqlens=lens_t, page_size=page_size, scale=scale,
+                     meta={"seed": seed, "capacity": cap})
+
+
+def paged_flash_decoding_b1(L=65536, page_size=64, seed=0, device="cpu"):
+    """The batch-1 CodeLlama-34B-shaped layer (64 query heads, 8 kv heads,
+    head dim 128, bf16) with its L-token history in pages of page_size
+    tokens scattered by a seeded permutation."""
+    return paged_case(1, 64, 8, 128, page_size, L // page_size, dtype=torch.bfloat16, seed=seed,
+                      device=device, name=f"paged_b1_h64_kv8_d128_bf16_L{L}_p{page_size}")

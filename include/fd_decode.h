@@ -119,6 +119,36 @@ FD_API fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cach
                               fd_tensor* lse, fd_stream stream);
 
 /*
+ * fd_decode_attention_paged — split-KV decode attention over a paged KV
+ * cache: fixed-size pages of tokens, each sequence's pages listed in a block
+ * table (the indirection-table storage named among the memory-wall
+ * techniques of the memory-bound decoding explainer).
+ *   q           [B, Hq, D]                FD_BF16 or FD_F32
+ *   k_pages     [num_pages, page_size, Hkv, D]   FD_BF16 or FD_F32 (same
+ *   v_pages     [num_pages, page_size, Hkv, D]    dtype for both)
+ *   block_table [B, max_pages] FD_I32 device tensor, rows contiguous: token j
+ *               of sequence b is row j % page_size of page
+ *               block_table[b, j / page_size].  Entries past a sequence's
+ *               last page are never read.
+ *   seqlens     [B] FD_I32 device tensor, or NULL meaning every sequence
+ *               holds max_pages * page_size tokens (its capacity).
+ *   num_splits, scale, out, lse, stream: as fd_decode_attention, with the
+ *               capacity max_pages * page_size in place of Lcap.
+ * Lengths outside [0, capacity] and page ids outside [0, num_pages) are
+ * caught on the device: the length is clamped, a bad page reads as zeros,
+ * and fd_check_device_error reports FD_ERR_DEVICE_BOUNDS.  The tensor-core
+ * split kernel streams pages whose size is 16, 32 or a multiple of 64
+ * tokens (bf16, head dim 128, group size 4..64); other shapes run on the
+ * generic kernel.  Workspace and asynchrony as fd_decode_attention.
+ */
+FD_API fd_status fd_decode_attention_paged(const fd_tensor* q, const fd_tensor* k_pages,
+                                           const fd_tensor* v_pages,
+                                           const fd_tensor* block_table,
+                                           const fd_tensor* seqlens, int32_t num_splits,
+                                           float scale, fd_tensor* out, fd_tensor* lse,
+                                           fd_stream stream);
+
+/*
  * fd_decode_attention_noalloc — fd_decode_attention without any device
  * allocation.  (The pages have no counterpart: this is a library service.)
  *
@@ -218,9 +248,9 @@ FD_API fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor
  * that minimises the modelled makespan
  *     waves(ns) * (chunk(ns) + 256)
  * where chunk(ns) is the fd_split_bounds chunk of a max_len history and
- * waves(ns) = ceil(batch * kv_heads * nonempty_splits / num_sms) rounds of
- * one CTA per SM; the 256 tokens charge each wave its fixed start-up and
- * epilogue time.  Returns 1 for any non-positive argument.  The
+ * waves(ns) = ceil(batch * kv_heads * nonempty_splits / (2 * num_sms))
+ * rounds of two CTAs per SM (the split kernel's occupancy); the 256 tokens
+ * charge each wave its fixed start-up and epilogue time.  Returns 1 for any non-positive argument.  The
  * Flash-Decoding page ("Why decoding needs different scheduling") fixes only
  * the direction: split when the batch leaves SMs idle, not when the history
  * is short or the batch already fills the GPU.

@@ -40,10 +40,12 @@ from .attention import (  # noqa: F401
     split_partials_ref,
     lse_combine_ref,
     bifurcated_attention_ref,
+    paged_gather_ref,
+    paged_decode_attention_ref,
     required_bytes_ref,
     SPLIT_ALIGN,
     MAX_SPLITS,
     MIN_CHUNK,
     SPLIT_OVERHEAD_TOKENS,
 )
-from .bruteforce import attention_bruteforce  # noqa: F401
+from .bruteforce import attention_bruteforce, paged_attention_bruteforce  # noqa: F401

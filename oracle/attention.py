@@ -171,9 +171,9 @@ def choose_num_splits_ref(batch: int, kv_heads: int, max_len: int, num_sms: int)
     split the history; a short history or a large batch makes more splitting
     useless, and more splits are no guaranteed gain.  Reading adopted: a
     makespan model.  With ns splits of a max_len history, one CTA per
-    (sequence, kv head, split) and one CTA per SM at a time,
+    (sequence, kv head, split) and two CTAs per SM at a time,
         chunk  = the split chunk of split_bounds_ref(max_len, ns, .)
-        waves  = ceil(batch * kv_heads * nonempty_splits / num_sms)
+        waves  = ceil(batch * kv_heads * nonempty_splits / (2 * num_sms))
         cost   = waves * (chunk + SPLIT_OVERHEAD_TOKENS)
     and the smallest ns in [1, min(MAX_SPLITS, ceil(max_len / MIN_CHUNK))]
     with the lowest cost wins.  SPLIT_OVERHEAD_TOKENS charges each wave the
@@ -188,7 +188,7 @@ def choose_num_splits_ref(batch: int, kv_heads: int, max_len: int, num_sms: int)
         per = -(-max_len // ns)
         chunk = -(-per // SPLIT_ALIGN) * SPLIT_ALIGN
         used = -(-max_len // chunk)
-        waves = -(-(units * used) // num_sms)
+        waves = -(-(units * used) // (2 * num_sms))
         cost = waves * (chunk + SPLIT_OVERHEAD_TOKENS)
         if best_cost is None or cost < best_cost:
             best_ns, best_cost = ns, cost
@@ -289,6 +289,48 @@ def bifurcated_attention_ref(q, k_ctx, v_ctx, k_dec, v_dec, dec_lens, scale):
             o = (e[:, :Lc] @ v_ctx[:, g, :] + e[:, Lc:] @ vd) / l[:, None]
             O[i, hs] = o
             LSE[i, hs] = m + np.log(l)
+    return O, LSE
+
+
+def paged_gather_ref(pages, block_table, page_size: int, length: int, b: int):
+    """The first ``length`` cached tokens of sequence b from a paged cache.
+
+    pages [num_pages, page_size, Hkv, D]; block_table [B, max_pages]: token j
+    of sequence b is row j % page_size of page block_table[b, j // page_size]
+    (the indirection table of paged KV storage in the memory-bound decoding
+    explainer, section on the memory wall: fixed-size KV blocks mapped
+    through a table).  Returns [length, Hkv, D]."""
+    pages = np.asarray(pages, np.float64)
+    bt = np.asarray(block_table)
+    out = np.zeros((length,) + pages.shape[2:])
+    for j in range(length):
+        pid = int(bt[b, j // page_size])
+        if pid < 0 or pid >= pages.shape[0]:
+            raise ValueError(f"page id {pid} outside [0, {pages.shape[0]})")
+        out[j] = pages[pid, j % page_size]
+    return out
+
+
+def paged_decode_attention_ref(q, k_pages, v_pages, block_table, seqlens, page_size, scale):
+    """Decode attention over a paged KV cache: the same definition as
+    decode_attention_ref with each sequence's keys and values read through
+    its block table (paged_gather_ref).  seqlens None means every sequence
+    fills its max_pages * page_size slots."""
+    q = np.asarray(q, np.float64)
+    bt = np.asarray(block_table)
+    B, Hq, D = q.shape
+    Hkv = np.asarray(k_pages).shape[2]
+    G = Hq // Hkv
+    cap = bt.shape[1] * page_size
+    lens = _lens(seqlens, B, cap)
+    O = np.zeros((B, Hq, D))
+    LSE = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        kb = paged_gather_ref(k_pages, bt, page_size, lens[b], b)
+        vb = paged_gather_ref(v_pages, bt, page_size, lens[b], b)
+        for g in range(Hkv):
+            hs = slice(g * G, (g + 1) * G)
+            O[b, hs], LSE[b, hs] = _attend(q[b, hs], kb[:, g], vb[:, g], scale)
     return O, LSE
 
 

@@ -43,3 +43,32 @@ def attention_bruteforce(q, k, v, seqlens, scale):
             for d in range(D):
                 O[b][h][d] = math.fsum(e[j] * v[b][j][g][d] for j in range(n)) / z
     return O, LSE
+
+
+def paged_attention_bruteforce(q, k_pages, v_pages, block_table, seqlens, page_size, scale):
+    """Exact single-query attention over a paged cache, by definition: every
+    key and value is fetched one token at a time through the block table
+    (page block_table[b][j // page_size], row j % page_size).  Nested lists
+    in, nested lists out, as attention_bruteforce."""
+    B = len(q)
+    Hq = len(q[0])
+    D = len(q[0][0])
+    Hkv = len(k_pages[0][0])
+    G = Hq // Hkv
+    O = [[[0.0] * D for _ in range(Hq)] for _ in range(B)]
+    LSE = [[-math.inf] * Hq for _ in range(B)]
+    for b in range(B):
+        n = len(block_table[b]) * page_size if seqlens is None else int(seqlens[b])
+        for h in range(Hq):
+            g = h // G
+            if n == 0:
+                continue
+            kk = [k_pages[block_table[b][j // page_size]][j % page_size][g] for j in range(n)]
+            vv = [v_pages[block_table[b][j // page_size]][j % page_size][g] for j in range(n)]
+            s = [scale * math.fsum(q[b][h][d] * kk[j][d] for d in range(D)) for j in range(n)]
+            e = [math.exp(x) for x in s]
+            z = math.fsum(e)
+            LSE[b][h] = math.log(z)
+            for d in range(D):
+                O[b][h][d] = math.fsum(e[j] * vv[j][d] for j in range(n)) / z
+    return O, LSE

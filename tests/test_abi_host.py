@@ -205,3 +205,28 @@ def test_python_binding_rejects_cpu_tensors():
     k = torch.zeros(1, 16, 4, 64)
     with pytest.raises(ValueError):
         fd.decode_attention(q, k, k)
+
+
+def test_paged_validation(L):
+    """fd_decode_attention_paged refuses bad descriptors before touching the
+    device (the pointers below are never dereferenced)."""
+    r = lambda x: ctypes.byref(x) if x is not None else None
+    q = _t([2, 8, 128])
+    kp = _t([10, 64, 2, 128])
+    bt = _t([2, 5], FD_I32)
+    o = _t([2, 8, 128], FD_F32)
+    call = lambda q_=q, k_=kp, v_=kp, bt_=bt, sl=None, ns=0, scale=0.1, o_=o: \
+        L.fd_decode_attention_paged(r(q_), r(k_), r(v_), r(bt_), r(sl), ns, scale, r(o_), None, None)
+    assert call(v_=_t([10, 32, 2, 128])) == 2                       # page shapes differ
+    assert call(bt_=_t([3, 5], FD_I32)) == 2                        # table rows != B
+    assert call(bt_=_t([2, 5], FD_F32)) == 3                        # table dtype
+    assert call(bt_=_t([2, 5], FD_I32, stride=[10, 2])) == 4        # table rows not contiguous
+    assert call(sl=_t([3], FD_I32)) == 2                            # seqlens shape
+    assert call(k_=_t([10, 64, 3, 128]), v_=_t([10, 64, 3, 128])) == 6   # Hq % Hkv
+    assert call(ns=300) == 5
+    assert call(scale=math.nan) == 5
+    assert call(k_=_t([0, 64, 2, 128]), v_=_t([0, 64, 2, 128])) == 2     # no pages
+    assert L.fd_last_error()
+    import torch
+    if not torch.cuda.is_available():
+        assert call() == 8                                          # valid: no device here

@@ -235,7 +235,7 @@ def test_heuristic_properties():
 def _makespan(units, L, ns, sms):
     chunk = -(-(-(-L // ns)) // oracle.SPLIT_ALIGN) * oracle.SPLIT_ALIGN
     used = -(-L // chunk)
-    return -(-(units * used) // sms) * (chunk + oracle.SPLIT_OVERHEAD_TOKENS)
+    return -(-(units * used) // (2 * sms)) * (chunk + oracle.SPLIT_OVERHEAD_TOKENS)
 
 
 def test_heuristic_is_the_makespan_minimiser():
@@ -252,11 +252,11 @@ def test_heuristic_is_the_makespan_minimiser():
 
 
 def test_heuristic_workload_choices():
-    # one wave of 144 CTAs for the batch-1 64K layer; ~two waves at batch 4
-    # over 128K; about seven waves for the batch-32 cache of 32K
-    assert oracle.choose_num_splits_ref(1, 8, 65536, 148) == 18
+    # two CTAs per SM: one wave of 296 CTAs for the batch-1 64K layer, one of
+    # 288 at batch 4 over 128K, seven for the batch-32 cache of 32K
+    assert oracle.choose_num_splits_ref(1, 8, 65536, 148) == 37
     assert oracle.choose_num_splits_ref(4, 8, 131072, 148) == 9
-    assert oracle.choose_num_splits_ref(32, 8, 32768, 148) == 4
+    assert oracle.choose_num_splits_ref(32, 8, 32768, 148) == 8
 
 
 def test_required_bytes_config_flash_decoding_64k():
