@@ -96,6 +96,82 @@ class BifurcatedCase:
         return [int(x) for x in self.dec_lens.tolist()]
 
 
+@dataclass
+class QuantCase:
+    """Decode over an 8-bit cache: q [B,Hq,D]; k/v codes [B,Lcap,Hkv,D]
+    (torch.int8, or torch.float8_e4m3fn for kind "e4m3"); k_scale, v_scale
+    [Hkv] float32 (dequantised K = k_scale[g] * code); seqlens as DecodeCase."""
+    name: str
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    k_scale: torch.Tensor
+    v_scale: torch.Tensor
+    seqlens: Optional[torch.Tensor]
+    scale: float
+    kind: str
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def lens(self):
+        B, Lcap = self.k.shape[0], self.k.shape[1]
+        if self.seqlens is None:
+            return [Lcap] * B
+        return [int(x) for x in self.seqlens.tolist()]
+
+
+def _int8_codes(shape, sigma, gen, device):
+    """Integer codes drawn from a normal of standard deviation ``sigma``,
+    rounded and clipped to [-127, 127] (a symmetric 8-bit code range), in
+    row chunks like _randn."""
+    out = torch.empty(shape, dtype=torch.int8, device=device)
+    flat = out.view(shape[0], -1)
+    row = flat.shape[1]
+    rows_per = max(1, _CHUNK_ELEMS // max(1, row))
+    for r0 in range(0, shape[0], rows_per):
+        r1 = min(shape[0], r0 + rows_per)
+        x = torch.randn((r1 - r0, row), generator=gen, dtype=torch.float32, device=device)
+        flat[r0:r1].copy_(torch.round(x * sigma).clamp_(-127, 127).to(torch.int8))
+    return out
+
+
+def quant_case(batch, hq, hkv, d, lcap, kind="int8", seed=0, seqlens=None, ragged=None,
+               q_dtype=torch.bfloat16, device="cpu", scale=None, name="quant"):
+    """Decode workload over an 8-bit cache.
+
+    kind "int8": codes ~ round(N(0, 32^2)) clipped to [-127, 127], scales
+    uniform in [0.5, 1.5] / 32 per kv head (dequantised values ~ N(0, 1)).
+    kind "e4m3": N(0, 1) draws rounded to e4m3 by ``Tensor.to``, scales
+    uniform in [0.5, 1.5] per kv head.  Scales come from the CPU generator
+    seeded with ``seed + 1`` (after the ragged lengths)."""
+    if kind not in ("int8", "e4m3"):
+        raise ValueError(f"unknown 8-bit kind {kind!r}")
+    g = _gen(seed, device)
+    q = _randn((batch, hq, d), q_dtype, g, device)
+    shape = (batch, lcap, hkv, d)
+    if kind == "int8":
+        k = _int8_codes(shape, 32.0, g, device)
+        v = _int8_codes(shape, 32.0, g, device)
+        base = 1.0 / 32.0
+    else:
+        k = _randn(shape, torch.float8_e4m3fn, g, device)
+        v = _randn(shape, torch.float8_e4m3fn, g, device)
+        base = 1.0
+    extra = _gen(seed + 1, "cpu")
+    lens_t = None
+    if ragged is not None:
+        lo, hi = ragged
+        lens_t = torch.randint(lo, hi + 1, (batch,), generator=extra, dtype=torch.int64).to(torch.int32)
+    elif seqlens is not None:
+        lens_t = torch.tensor(list(seqlens), dtype=torch.int32)
+    k_scale = ((0.5 + torch.rand(hkv, generator=extra, dtype=torch.float32)) * base).to(device)
+    v_scale = ((0.5 + torch.rand(hkv, generator=extra, dtype=torch.float32)) * base).to(device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return QuantCase(name=name, q=q, k=k, v=v, k_scale=k_scale, v_scale=v_scale, seqlens=lens_t,
+                     scale=scale, kind=kind, meta={"seed": seed})
+
+
 def decode_case(batch, hq, hkv, d, lcap, dtype=torch.bfloat16, seed=0,
                 seqlens=None, ragged=None, peaked_frac=0.0, peak_factor=8.0,
                 q_dtype=None, device="cpu", scale=None, name="decode"):
@@ -280,3 +356,10 @@ def paged_flash_decoding_b1(L=65536, page_size=64, seed=0, device="cpu"):
     tokens scattered by a seeded permutation."""
     return paged_case(1, 64, 8, 128, page_size, L // page_size, dtype=torch.bfloat16, seed=seed,
                       device=device, name=f"paged_b1_h64_kv8_d128_bf16_L{L}_p{page_size}")
+
+
+def quant_flash_decoding_b1(L=65536, kind="int8", seed=0, device="cpu"):
+    """The batch-1 CodeLlama-34B-shaped layer (64 query heads, 8 kv heads,
+    head dim 128) over an 8-bit cache of L tokens."""
+    return quant_case(1, 64, 8, 128, L, kind=kind, seed=seed, device=device,
+                      name=f"b1_h64_kv8_d128_{kind}_L{L}")

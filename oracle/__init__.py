@@ -20,6 +20,11 @@ Sources (web pages, cited by title and section):
   (zimaspace.com, Italian edition), sections on tiling and online softmax:
   the family computes exact attention.
 
+* "If you have ever watched an LLM generate a long response..." (gyaansetu.com,
+  Kannada edition), section on fighting the memory wall: paged KV storage
+  behind an indirection table, and 8-bit storage to halve the bytes moved
+  (``quant.py``).
+
 Every function works in float64 on the exact values of its inputs.  bf16
 inputs are decoded from their raw 16-bit patterns by :func:`bf16_bits_to_f64`
 (no torch conversion involved).
@@ -49,3 +54,9 @@ from .attention import (  # noqa: F401
     SPLIT_OVERHEAD_TOKENS,
 )
 from .bruteforce import attention_bruteforce, paged_attention_bruteforce  # noqa: F401
+from .quant import (  # noqa: F401
+    e4m3_to_f64,
+    int8_to_f64,
+    dequantize_kv_ref,
+    quant_decode_attention_ref,
+)

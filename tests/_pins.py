@@ -176,3 +176,119 @@ def bifurcated_concat_ok(bif_fn, decode_fn, seed=3):
     vcat = np.concatenate([np.repeat(vc[None], n, 0), vd], axis=1)
     Or, Lr = decode_fn(q, kcat, vcat, [Lc + x for x in lens], 0.4)
     return _close(O, Or, 1e-12) and _close(L, Lr, 1e-12)
+
+
+# ------------------------------------------------------------ 8-bit caches
+
+_E4M3_LANDMARKS = {
+    0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 / 8 * 2.0 ** -6, 0x08: 2.0 ** -6,
+    0x38: 1.0, 0xB8: -1.0, 0x77: 240.0, 0x7E: 448.0, 0xFE: -448.0,
+}
+
+
+def e4m3_table_ok(e4m3_fn):
+    """Every e4m3 code against PyTorch's float8_e4m3fn decoding (an
+    independent implementation of the same format), plus landmark values of
+    the format: 1.0, the largest finite 448, the smallest normal 2^-6 and
+    subnormal 2^-9, and exactly two NaN codes (0x7F, 0xFF)."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    ours = np.asarray(e4m3_fn(codes), np.float64)
+    lib = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    if not np.array_equal(np.isnan(ours), np.isnan(lib)):
+        return False
+    if sorted(np.flatnonzero(np.isnan(ours)).tolist()) != [0x7F, 0xFF]:
+        return False
+    fin = ~np.isnan(lib)
+    if not np.array_equal(ours[fin], lib[fin]):
+        return False
+    return all(ours[c] == v for c, v in _E4M3_LANDMARKS.items())
+
+
+def _code_value(kind, c):
+    """Value of one code, by hand: the integer itself, or PyTorch's e4m3."""
+    if kind == "int8":
+        return float(int(c))
+    import torch
+    t = torch.tensor([int(c)], dtype=torch.uint8).view(torch.float8_e4m3fn)
+    return float(t.to(torch.float64).item())
+
+
+def _small_codes(rng, kind, shape):
+    if kind == "int8":
+        return rng.integers(-127, 128, shape).astype(np.int8)
+    # e4m3 codes with |value| < 4 (exponent field <= 8), either sign
+    mag = rng.integers(0, 0x48, shape)
+    sign = rng.integers(0, 2, shape) << 7
+    return (mag | sign).astype(np.uint8)
+
+
+def quant_bruteforce_ok(quant_fn, bruteforce_fn):
+    """Tiny int8 and e4m3 caches with ragged lengths and a distinct scale per
+    kv head: the oracle against the loop oracle run on values dequantised by
+    hand (code value x the scale of the code's own kv head)."""
+    rng = np.random.default_rng(11)
+    for kind, ks, vs in (("int8", [0.03, 0.05, 0.021], [0.04, 0.017, 0.033]),
+                         ("e4m3", [0.7, 1.3, 0.9], [1.1, 0.6, 1.45])):
+        B, Hkv, G, D, L = 2, 3, 2, 6, 5
+        q = rng.standard_normal((B, Hkv * G, D))
+        kc = _small_codes(rng, kind, (B, L, Hkv, D))
+        vc = _small_codes(rng, kind, (B, L, Hkv, D))
+        seqlens = [5, 3]
+        scale = 0.4
+        O, LSE = quant_fn(q, kc, vc, np.array(ks, np.float32), np.array(vs, np.float32), kind,
+                          seqlens, scale)
+        ksf = [float(np.float32(x)) for x in ks]
+        vsf = [float(np.float32(x)) for x in vs]
+        kd = [[[[_code_value(kind, kc[b, j, g, d]) * ksf[g] for d in range(D)] for g in range(Hkv)]
+               for j in range(L)] for b in range(B)]
+        vd = [[[[_code_value(kind, vc[b, j, g, d]) * vsf[g] for d in range(D)] for g in range(Hkv)]
+               for j in range(L)] for b in range(B)]
+        Ob, Lb = bruteforce_fn(q.tolist(), kd, vd, seqlens, scale)
+        if not (_close(O, Ob, 1e-11) and _close(LSE, Lb, 1e-11)):
+            return False
+    return True
+
+
+def quant_closed_forms_ok(quant_fn):
+    """Closed forms on 8-bit caches:
+    - V scale: O is linear in v_scale, LSE does not depend on it;
+    - k_scale = 0: every score is 0, so O = mean of the dequantised V and
+      LSE = ln len;
+    - one cached token: O = v_scale[g] * v_code, LSE = scale * k_scale[g] *
+      <q, k_code>;
+    - codes past a sequence's length (NaN e4m3 codes included) are unused."""
+    rng = np.random.default_rng(5)
+    for kind in ("int8", "e4m3"):
+        B, Hkv, G, D, L = 1, 2, 2, 4, 7
+        q = rng.standard_normal((B, Hkv * G, D))
+        kc = _small_codes(rng, kind, (B, L, Hkv, D))
+        vc = _small_codes(rng, kind, (B, L, Hkv, D))
+        ks = np.array([0.05, 0.08], np.float32) if kind == "int8" else np.array([0.9, 1.2], np.float32)
+        vs = np.array([0.03, 0.06], np.float32) if kind == "int8" else np.array([0.5, 1.5], np.float32)
+        val = np.vectorize(lambda c: _code_value(kind, c))
+        O1, L1 = quant_fn(q, kc, vc, ks, vs, kind, None, 0.5)
+        O2, L2 = quant_fn(q, kc, vc, ks, 4.0 * vs, kind, None, 0.5)    # x4: exact in fp32
+        if not (_close(O2, 4.0 * O1) and _close(L2, L1)):
+            return False
+        O0, L0 = quant_fn(q, kc, vc, np.zeros(2, np.float32), vs, kind, [5], 0.5)
+        for h in range(Hkv * G):
+            g = h // G
+            mean = val(vc[0, :5, g]).mean(axis=0) * float(vs[g])
+            if not (_close(O0[0, h], mean) and _close(L0[0, h], math.log(5))):
+                return False
+        Os, Ls = quant_fn(q, kc, vc, ks, vs, kind, [1], 0.5)
+        for h in range(Hkv * G):
+            g = h // G
+            s = 0.5 * float(ks[g]) * float(np.dot(q[0, h], val(kc[0, 0, g])))
+            if not (_close(Os[0, h], val(vc[0, 0, g]) * float(vs[g])) and _close(Ls[0, h], s)):
+                return False
+        if kind == "e4m3":
+            kn, vn = kc.copy(), vc.copy()
+            kn[0, 4:] = 0x7F
+            vn[0, 4:] = 0xFF
+            Oa, La = quant_fn(q, kn, vn, ks, vs, kind, [4], 0.5)
+            Ob, Lb = quant_fn(q, kc, vc, ks, vs, kind, [4], 0.5)
+            if not (np.all(np.isfinite(Oa)) and _close(Oa, Ob) and _close(La, Lb)):
+                return False
+    return True
