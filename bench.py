@@ -186,6 +186,30 @@ class Workload:
         raise NotImplementedError
 
 
+def _rows(t, n):
+    """t viewed as n rows (8-bit floats as bytes, which indexing kernels take)."""
+    import torch
+    if t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    return t.view(n, -1)
+
+
+def _host_loop_us(stream, steps, step, warmup=5):
+    """Wall-clock microseconds per call of step(i) on `stream`, after
+    `warmup` untimed calls (first-use costs: lazy kernel loading, pinned
+    staging, pool growth)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(steps):
+            step(i)
+    return (time.perf_counter() - t0) * 1e6 / steps
+
+
 class DecodeWorkload(Workload):
     dominant = FD_KERNEL_SPLIT
 
@@ -238,6 +262,11 @@ class DecodeWorkload(Workload):
         if st:
             raise RuntimeError(self.L.fd_last_error().decode())
 
+    def api_call(self, q, k, v, stream):
+        import decode_attention_20_b300 as fd
+        fd.decode_attention(q, k, v, self.seqlens_dev, self.ns, self.case.scale, out=self.out,
+                            lse=self.lse, stream=stream)
+
     def e2e(self, stream, steps):
         """Per step: H2D of the new query and one new K/V row per sequence
         (written at position len_b - 1), the call, D2H of out + lse."""
@@ -258,45 +287,49 @@ class DecodeWorkload(Workload):
                             device=c.q.device)
         dk = torch.empty((self.B, self.Hkv * self.D), dtype=c.k.dtype, device=c.q.device)
         dv = torch.empty_like(dk)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for i in range(steps):
-                kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
-                c.q.copy_(hq, non_blocking=True)
-                dk.copy_(hk.view(self.B, -1), non_blocking=True)
-                dv.copy_(hv.view(self.B, -1), non_blocking=True)
-                kb.view(self.B * self.Lcap, -1).index_copy_(0, rows, dk)
-                vb.view(self.B * self.Lcap, -1).index_copy_(0, rows, dv)
-                fd.decode_attention(c.q, kb, vb, self.seqlens_dev, self.ns, c.scale, out=self.out,
-                                    lse=self.lse, stream=stream)
-                hout.copy_(self.out, non_blocking=True)
-                hlse.copy_(self.lse, non_blocking=True)
-                stream.synchronize()
-        us = (time.perf_counter() - t0) * 1e6 / steps
+
+        def step(i):
+            kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
+            c.q.copy_(hq, non_blocking=True)
+            dk.copy_(hk.view(self.B, -1), non_blocking=True)
+            dv.copy_(hv.view(self.B, -1), non_blocking=True)
+            _rows(kb, self.B * self.Lcap).index_copy_(0, rows, _rows(dk, self.B))
+            _rows(vb, self.B * self.Lcap).index_copy_(0, rows, _rows(dv, self.B))
+            self.api_call(c.q, kb, vb, stream)
+            hout.copy_(self.out, non_blocking=True)
+            hlse.copy_(self.lse, non_blocking=True)
+            stream.synchronize()
+
+        us = _host_loop_us(stream, steps, step)
         h2d = hq.numel() * hq.element_size() + hk.numel() * hk.element_size() * 2
         d2h = hout.numel() * 4 + hlse.numel() * 4
         return us, h2d, d2h
+
+    def _oracle_inputs(self, n0):
+        c = self.case
+        return f64(c.q[0:1]), f64(c.k[0:1, :n0]), f64(c.v[0:1, :n0])
+
+    def _oracle_call(self, q, k, v, T):
+        import oracle
+        oracle.decode_attention_ref(q, k[:, :T], v[:, :T], None, self.case.scale)
 
     def oracle_sample(self, target_s):
         """Time the oracle on the first T tokens of sequence 0 (all kv
         heads), T sized for about target_s seconds (at least 64 tokens);
         returns (us per full call extrapolated by tokens, sample text,
         seconds of the sample)."""
-        import oracle
-        c = self.case
         if not hasattr(self, "_of"):
             n0 = max(self.lens[0], 1)
-            self._of = (f64(c.q[0:1]), f64(c.k[0:1, :n0]), f64(c.v[0:1, :n0]))
+            self._of = self._oracle_inputs(n0)
             q, k, v = self._of
             T0 = min(n0, 2048)
             t0 = time.perf_counter()
-            oracle.decode_attention_ref(q, k[:, :T0], v[:, :T0], None, c.scale)
+            self._oracle_call(q, k, v, T0)
             self._per_tok = (time.perf_counter() - t0) / T0
         q, k, v = self._of
         T = int(max(min(64, self.lens[0]), min(self.lens[0], target_s / self._per_tok)))
         t0 = time.perf_counter()
-        oracle.decode_attention_ref(q, k[:, :T], v[:, :T], None, c.scale)
+        self._oracle_call(q, k, v, T)
         dt = time.perf_counter() - t0
         full = dt * (sum(self.lens) / T)
         return full * 1e6, (f"sequence 0, first {T} tokens x all {self.Hkv} kv heads per call, "
@@ -402,23 +435,22 @@ class BifWorkload(Workload):
                             device=c.q.device)
         dk = torch.empty((self.n, self.Hkv * self.D), dtype=c.k_dec.dtype, device=c.q.device)
         dv = torch.empty_like(dk)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for i in range(steps):
-                q, kc, vc, kd, vd = self.bufs[i % self.nbuf]
-                q.copy_(hq, non_blocking=True)
-                dk.copy_(hk.view(self.n, -1), non_blocking=True)
-                dv.copy_(hv.view(self.n, -1), non_blocking=True)
-                kd.view(self.n * self.Ld, -1).index_copy_(0, rows, dk)
-                vd.view(self.n * self.Ld, -1).index_copy_(0, rows, dv)
-                fd.bifurcated_attention(q, kc, vc, kd, vd, self.dec_dev, c.scale, out=self.out,
-                                        lse=self.lse, ctx_splits=self.ns, return_lse=True,
-                                        stream=stream)
-                hout.copy_(self.out, non_blocking=True)
-                hlse.copy_(self.lse, non_blocking=True)
-                stream.synchronize()
-        us = (time.perf_counter() - t0) * 1e6 / steps
+
+        def step(i):
+            q, kc, vc, kd, vd = self.bufs[i % self.nbuf]
+            q.copy_(hq, non_blocking=True)
+            dk.copy_(hk.view(self.n, -1), non_blocking=True)
+            dv.copy_(hv.view(self.n, -1), non_blocking=True)
+            kd.view(self.n * self.Ld, -1).index_copy_(0, rows, dk)
+            vd.view(self.n * self.Ld, -1).index_copy_(0, rows, dv)
+            fd.bifurcated_attention(q, kc, vc, kd, vd, self.dec_dev, c.scale, out=self.out,
+                                    lse=self.lse, ctx_splits=self.ns, return_lse=True,
+                                    stream=stream)
+            hout.copy_(self.out, non_blocking=True)
+            hlse.copy_(self.lse, non_blocking=True)
+            stream.synchronize()
+
+        us = _host_loop_us(stream, steps, step)
         h2d = hq.numel() * 2 + hk.numel() * 2 * 2
         d2h = hout.numel() * 4 + hlse.numel() * 4
         return us, h2d, d2h
@@ -525,21 +557,73 @@ class PagedWorkload(DecodeWorkload):
         hv.copy_(c.v_pages.view(-1, self.Hkv * self.D)[row:row + 1].cpu())
         hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
         hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for i in range(steps):
-                kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
-                c.q.copy_(hq, non_blocking=True)
-                kb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(hk, non_blocking=True)
-                vb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(hv, non_blocking=True)
-                fd.decode_attention_paged(c.q, kb, vb, self.bt_dev, None, self.ns, c.scale,
-                                          out=self.out, lse=self.lse, stream=stream)
-                hout.copy_(self.out, non_blocking=True)
-                hlse.copy_(self.lse, non_blocking=True)
-                stream.synchronize()
-        us = (time.perf_counter() - t0) * 1e6 / steps
+
+        def step(i):
+            kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
+            c.q.copy_(hq, non_blocking=True)
+            kb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(hk, non_blocking=True)
+            vb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(hv, non_blocking=True)
+            fd.decode_attention_paged(c.q, kb, vb, self.bt_dev, None, self.ns, c.scale,
+                                      out=self.out, lse=self.lse, stream=stream)
+            hout.copy_(self.out, non_blocking=True)
+            hlse.copy_(self.lse, non_blocking=True)
+            stream.synchronize()
+
+        us = _host_loop_us(stream, steps, step)
         return us, hq.numel() * 2 + hk.numel() * 2 * 2, hout.numel() * 4 + hlse.numel() * 4
+
+
+class QuantWorkload(DecodeWorkload):
+    """The batch-1 64K-token layer over an 8-bit cache (int8 or e4m3 codes,
+    one scale per kv head): fd_decode_attention_quant."""
+    dtype = "f16"
+    kernel_name = "split_mma_kernel (mma.sync f16 over 8-bit codes, TMA ring)"
+
+    def __init__(self, short, kind, device):
+        from decode_attention_20_b300 import inputs
+        super().__init__(short, lambda d: inputs.quant_flash_decoding_b1(65536, kind=kind, device=d),
+                         device)
+        self.kind = kind
+
+    def config(self, ns):
+        cfg = super().config(ns)
+        cfg["kv_codes"] = self.kind
+        return cfg
+
+    def prepare(self, L, stream, ns):
+        from decode_attention_20_b300.api import _desc
+        super().prepare(L, stream, ns)
+        self.dkscale = _desc(self.case.k_scale, "k_scale")
+        self.dvscale = _desc(self.case.v_scale, "v_scale")
+
+    def call(self, i):
+        r = ctypes.byref
+        st = self.L.fd_decode_attention_quant(r(self.dq), r(self.dks[i % self.nbuf]),
+                                              r(self.dvs[i % self.nbuf]), r(self.dkscale),
+                                              r(self.dvscale),
+                                              r(self.ds) if self.ds is not None else None, self.ns,
+                                              ctypes.c_float(self.case.scale), r(self.do),
+                                              r(self.dl), self.sptr)
+        if st:
+            raise RuntimeError(self.L.fd_last_error().decode())
+
+    def api_call(self, q, k, v, stream):
+        import decode_attention_20_b300 as fd
+        c = self.case
+        fd.decode_attention_quant(q, k, v, c.k_scale, c.v_scale, self.seqlens_dev, self.ns,
+                                  c.scale, out=self.out, lse=self.lse, stream=stream)
+
+    def _oracle_inputs(self, n0):
+        import torch
+        c = self.case
+        codes = lambda t: (t.view(torch.uint8) if t.dtype == torch.float8_e4m3fn else t).cpu().numpy()
+        return (f64(c.q[0:1]), codes(c.k[0:1, :n0]), codes(c.v[0:1, :n0]))
+
+    def _oracle_call(self, q, k, v, T):
+        import oracle
+        c = self.case
+        oracle.quant_decode_attention_ref(q, k[:, :T], v[:, :T], c.k_scale.cpu().numpy(),
+                                          c.v_scale.cpu().numpy(), self.kind, None, c.scale)
 
 
 def make_workload(short, device):
@@ -554,6 +638,10 @@ def make_workload(short, device):
         return BifWorkload(device)
     if short == "paged_b1_64k":
         return PagedWorkload(device)
+    if short == "int8_b1_64k":
+        return QuantWorkload(short, "int8", device)
+    if short == "e4m3_b1_64k":
+        return QuantWorkload(short, "e4m3", device)
     raise SystemExit(f"unknown workload {short}")
 
 
@@ -732,7 +820,7 @@ def run_fd(args, rank, world):
         "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call",
         "n_gpus": world, "steps": steps, "warmup": warm,
         "ms_per_step": us_per_call / 1e3, "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": getattr(w, "dtype", "bf16"),
         "data": "synthetic",
         "config": dict(w.config(ns), parallelism="replicas" if world > 1 else "single",
                        l2=f"inputs larger than L2: {w.nbuf} rotating input copies",
@@ -745,7 +833,8 @@ def run_fd(args, rank, world):
         "roofline": {"bound": w.bound, "achieved": round(achieved, 1), "peak": peak,
                      "unit": w.unit, "frac": round(achieved / peak, 4),
                      "traffic": measured_traffic(w.dominant, w.short),
-                     "kernel": KERNEL_NAMES[w.dominant], "peak_kind": peaks["kind"],
+                     "kernel": getattr(w, "kernel_name", KERNEL_NAMES[w.dominant]),
+                     "peak_kind": peaks["kind"],
                      "per_launch": per_launch, "launch_us": round(dom_us, 3)},
         "clocks": {"sm_mhz": clk["sm_mhz"], "sm_max_mhz": clk["sm_max_mhz"],
                    "reasons": clk["reasons"], "samples": clk["samples"]},
@@ -817,6 +906,61 @@ def run_sweep(args):
     return 0
 
 
+def run_bif_sweep(args):
+    """--bif-sweep: bifurcated attention against the replicated-context
+    decode path over samples n, context length Lc and kv heads (32 query
+    heads, head dim 128, bf16, decode lengths uniform in [1, 256]); one JSON
+    line each with both times, their ratio, the K/V byte ratio and h/g.  A
+    measurement aid, not the benchmark line."""
+    import torch
+    import decode_attention_20_b300 as fd
+    from decode_attention_20_b300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    iters = max(5, min(args.steps, 50))
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for _ in range(iters):
+            flush.fill_(1)                  # every call starts with L2 cleared
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            tot += e0.elapsed_time(e1)
+        return tot * 1e3 / iters
+
+    for hkv in [1, 8]:
+        for lc in [2048, 8192, 32768]:
+            for n in [8, 32, 64, 128]:
+                c = inputs.bifurcated_case(n, 32, hkv, 128, lc, 256, seed=n + lc + hkv,
+                                           ragged_dec=(1, 256), device="cuda")
+                dl = c.dec_lens.cuda()
+                bif_us = timed(lambda: fd.bifurcated_attention(c.q, c.k_ctx, c.v_ctx, c.k_dec,
+                                                               c.v_dec, dl, c.scale))
+                rep = inputs.replicate_context(c)
+                sl = rep.seqlens.cuda()
+                rep_us = timed(lambda: fd.decode_attention(rep.q, rep.k, rep.v, sl, 0, rep.scale))
+                fd.check_device_error()
+                kv_bif = c.k_ctx.numel() * 4 + sum(c.lens) * hkv * 128 * 4
+                kv_rep = sum(rep.lens) * hkv * 128 * 4
+                print(json.dumps({"samples": n, "context_len": lc, "kv_heads": hkv, "q_heads": 32,
+                                  "bifurcated_us": round(bif_us, 2),
+                                  "replicated_us": round(rep_us, 2),
+                                  "speedup": round(rep_us / bif_us, 2),
+                                  "kv_byte_ratio": round(kv_rep / kv_bif, 2),
+                                  "h_over_g": 32 // hkv}), flush=True)
+                del c, rep
+                torch.cuda.empty_cache()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -824,7 +968,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="b1_64k",
-                    choices=["b1_64k", "ragged_b32", "long_b4", "bif_mqa", "paged_b1_64k"])
+                    choices=["b1_64k", "ragged_b32", "long_b4", "bif_mqa", "paged_b1_64k",
+                             "int8_b1_64k", "e4m3_b1_64k"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -832,9 +977,13 @@ def main(argv=None):
                     help="comma-separated split counts: print one timing line per count instead")
     ap.add_argument("--sweep-variants", default="",
                     help="with --sweep-splits: comma-separated FD_SPLIT_VARIANT values")
+    ap.add_argument("--bif-sweep", action="store_true",
+                    help="bifurcated vs replicated-context over n, Lc and kv heads instead")
     args = ap.parse_args(argv)
     if args.sweep_splits:
         return run_sweep(args)
+    if args.bif_sweep:
+        return run_bif_sweep(args)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":

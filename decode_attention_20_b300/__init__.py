@@ -15,6 +15,7 @@ from .api import (  # noqa: F401
     decode_attention,
     decode_attention_partials,
     decode_attention_paged,
+    decode_attention_quant,
     lse_combine,
     profile_enable,
     profile_read,

@@ -13,7 +13,7 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfd_decode.so")
 
-FD_F32, FD_BF16, FD_I32 = 0, 1, 2
+FD_F32, FD_BF16, FD_I32, FD_I8, FD_E4M3 = 0, 1, 2, 3, 4
 FD_KERNEL_SPLIT, FD_KERNEL_COMBINE, FD_KERNEL_BIF_CTX = 0, 1, 2
 
 STATUS_NAMES = {
@@ -43,6 +43,7 @@ def _declare(lib):
         "fd_decode_attention": (st, [_T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_decode_attention_noalloc": (st, [_T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_decode_attention_paged": (st, [_T, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
+        "fd_decode_attention_quant": (st, [_T, _T, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_decode_attention_partials": (st, [_T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_lse_combine": (st, [_T, _T, _T, _T, ctypes.c_void_p]),
         "fd_bifurcated_attention": (st, [_T, _T, _T, _T, _T, _T, ctypes.c_float, _T, ctypes.c_void_p]),

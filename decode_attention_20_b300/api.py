@@ -18,7 +18,8 @@ import torch
 from . import _lib
 from ._lib import FdError, FdTensor, check, lib  # noqa: F401
 
-_DT = {torch.float32: _lib.FD_F32, torch.bfloat16: _lib.FD_BF16, torch.int32: _lib.FD_I32}
+_DT = {torch.float32: _lib.FD_F32, torch.bfloat16: _lib.FD_BF16, torch.int32: _lib.FD_I32,
+       torch.int8: _lib.FD_I8, torch.float8_e4m3fn: _lib.FD_E4M3}
 
 
 def _desc(t: Optional[torch.Tensor], name: str):
@@ -65,6 +66,29 @@ def decode_attention(q, k_cache, v_cache, seqlens=None, num_splits=0, scale=None
     do, dl = _desc(out, "out"), _desc(lse, "lse")
     check(lib().fd_decode_attention(_ref(dq), _ref(dk), _ref(dv), _ref(ds), int(num_splits),
                                     float(scale), _ref(do), _ref(dl), _stream(stream)))
+    return out, lse
+
+
+def decode_attention_quant(q, k_cache, v_cache, k_scale, v_scale, seqlens=None, num_splits=0,
+                           scale=None, out=None, lse=None, return_lse=True, stream=None):
+    """Split-KV decode attention over an 8-bit cache (fd_decode_attention_quant).
+
+    k_cache, v_cache [B, Lcap, Hkv, D] torch.int8 or torch.float8_e4m3fn
+    codes; k_scale, v_scale [Hkv] fp32 CUDA tensors (K = k_scale[g] * codes,
+    V likewise); the rest as decode_attention."""
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    dq, dk, dv = _desc(q, "q"), _desc(k_cache, "k_cache"), _desc(v_cache, "v_cache")
+    dks, dvs, ds = _desc(k_scale, "k_scale"), _desc(v_scale, "v_scale"), _desc(seqlens, "seqlens")
+    do, dl = _desc(out, "out"), _desc(lse, "lse")
+    check(lib().fd_decode_attention_quant(_ref(dq), _ref(dk), _ref(dv), _ref(dks), _ref(dvs),
+                                          _ref(ds), int(num_splits), float(scale), _ref(do),
+                                          _ref(dl), _stream(stream)))
     return out, lse
 
 

@@ -149,13 +149,14 @@ fd_status get_encoder() {
   return FD_OK;
 }
 
-// 4-D bf16 map over a [B, L, Hkv, D] cache with box {box_d, 1, tile, 1};
-// box_d = 64 uses the 128-byte swizzle (one swizzle row per token), box_d =
-// D leaves the tile unswizzled.
+// 4-D map over a [B, L, Hkv, D] cache of bf16 (esz 2) or 8-bit codes (esz
+// 1) with box {box_d, 1, tile, 1}; a 128-byte box row uses the 128-byte
+// swizzle (one swizzle row per token), other widths leave the tile
+// unswizzled.
 bool make_kv_map(CUtensorMap* map, const void* base, int64_t B, int64_t L, int64_t Hkv,
-                 int64_t D, int64_t sb, int64_t sl, int64_t sh, int tile, int box_d = 0) {
+                 int64_t D, int64_t sb, int64_t sl, int64_t sh, int tile, int box_d = 0,
+                 int64_t esz = 2) {
   if (box_d == 0) box_d = (int)D;
-  const int64_t esz = 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)L, (cuuint64_t)B};
   // A unit batch extent never steps along its stride; give it a legal one.
   const int64_t sb_eff = (B == 1) ? sl * L : sb;
@@ -164,8 +165,10 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t B, int64_t L, int64
   cuuint32_t box[4] = {(cuuint32_t)box_d, 1u, (cuuint32_t)tile, 1u};
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   const CUtensorMapSwizzle swz =
-      (box_d * 2 == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+      (box_d * esz == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUtensorMapDataType dt =
+      esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -191,7 +194,20 @@ bool make_3d_map(CUtensorMap* map, const void* base, int64_t D, int64_t n1, int6
 
 // ------------------------------------------------------------------ validation
 
-int64_t esize(int32_t dt) { return dt == FD_BF16 ? 2 : 4; }
+int64_t esize(int32_t dt) {
+  return dt == FD_BF16 ? 2 : (dt == FD_I8 || dt == FD_E4M3) ? 1 : 4;
+}
+
+bool is_q8(int32_t dt) { return dt == FD_I8 || dt == FD_E4M3; }
+
+int kv_kind_of(int32_t dt) {
+  switch (dt) {
+    case FD_BF16: return kKvBf16;
+    case FD_I8: return kKvI8;
+    case FD_E4M3: return kKvE4m3;
+    default: return kKvF32;
+  }
+}
 
 fd_status check_tensor(const fd_tensor* t, const char* name, int ndim) {
   if (t == nullptr) return fail(FD_ERR_NULL, "%s descriptor is NULL", name);
@@ -202,7 +218,7 @@ fd_status check_tensor(const fd_tensor* t, const char* name, int ndim) {
     numel *= t->shape[i];
   }
   if (numel > 0 && t->data == nullptr) return fail(FD_ERR_NULL, "%s data pointer is NULL", name);
-  if (t->dtype != FD_F32 && t->dtype != FD_BF16 && t->dtype != FD_I32)
+  if (t->dtype != FD_F32 && t->dtype != FD_BF16 && t->dtype != FD_I32 && !is_q8(t->dtype))
     return fail(FD_ERR_DTYPE, "%s has unknown dtype %d", name, t->dtype);
   if (t->stride[ndim - 1] != 1 && t->shape[ndim - 1] > 1)
     return fail(FD_ERR_LAYOUT, "%s innermost stride must be 1", name);
@@ -218,13 +234,17 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DecodeDesc {
   int64_t B, Hq, Hkv, D, Lcap, G;
   int32_t q_dt, kv_dt;
+  const float* k_scale = nullptr;   // 8-bit caches: [Hkv] device
+  const float* v_scale = nullptr;
 };
 
 // Validates q / k / v / seqlens / out / lse of a decode call.  `out_dims`
 // 3: out [B,Hq,D], lse [B,Hq];  4: partials out [B,Hq,ns,D], lse [B,Hq,ns].
+// `quant_kv`: the caches hold 8-bit codes (FD_I8 / FD_E4M3) instead of
+// bf16 / f32 values.
 fd_status validate_decode(const fd_tensor* q, const fd_tensor* k, const fd_tensor* v,
                           const fd_tensor* seqlens, const fd_tensor* out, const fd_tensor* lse,
-                          int out_dims, int ns, DecodeDesc* d) {
+                          int out_dims, int ns, DecodeDesc* d, bool quant_kv = false) {
   fd_status st;
   if ((st = check_tensor(q, "q", 3))) return st;
   if ((st = check_tensor(k, "k_cache", 4))) return st;
@@ -244,7 +264,9 @@ fd_status validate_decode(const fd_tensor* q, const fd_tensor* k, const fd_tenso
   if (k->shape[3] != d->D) return fail(FD_ERR_SHAPE, "k_cache head dim != q head dim");
   if (q->dtype != FD_BF16 && q->dtype != FD_F32) return fail(FD_ERR_DTYPE, "q must be bf16 or f32");
   if (k->dtype != v->dtype) return fail(FD_ERR_DTYPE, "k_cache and v_cache dtypes differ");
-  if (k->dtype != FD_BF16 && k->dtype != FD_F32)
+  if (quant_kv && !is_q8(k->dtype))
+    return fail(FD_ERR_DTYPE, "k_cache/v_cache must be int8 or e4m3 codes");
+  if (!quant_kv && k->dtype != FD_BF16 && k->dtype != FD_F32)
     return fail(FD_ERR_DTYPE, "k_cache/v_cache must be bf16 or f32");
   if (out->dtype != FD_F32) return fail(FD_ERR_DTYPE, "out must be f32");
   if (lse && lse->dtype != FD_F32) return fail(FD_ERR_DTYPE, "lse must be f32");
@@ -279,14 +301,17 @@ fd_status validate_decode(const fd_tensor* q, const fd_tensor* k, const fd_tenso
 // Whether the TMA kernel can stream this cache: bf16, head dim 128, 16-byte
 // aligned base and strides (token, kv head, batch), a group size it is
 // instantiated for.
+// (8-bit caches: the same with 1-byte codes.)
 bool tma_ok(const DecodeDesc& d, const void* kd, const void* vd, const int64_t (&strides)[6],
             int64_t batch_extent) {
-  if (d.kv_dt != FD_BF16 || d.D != 128 || d.Lcap < kSplitTileTokens) return false;
+  if ((d.kv_dt != FD_BF16 && !is_q8(d.kv_dt)) || d.D != 128 || d.Lcap < kSplitTileTokens)
+    return false;
   if (!(d.G == 1 || d.G == 2 || d.G == 4 || d.G == 8 || d.G == 16 || d.G == 32 || d.G == 64)) return false;
   if (!aligned16(kd) || !aligned16(vd)) return false;
+  const int64_t esz = esize(d.kv_dt);
   for (int i = 0; i < 6; ++i) {
     if (i >= 4 && batch_extent == 1) continue;   // batch strides unused
-    if (strides[i] <= 0 || (strides[i] * 2) % 16 != 0 || strides[i] * 2 >= (1ll << 40)) return false;
+    if (strides[i] <= 0 || (strides[i] * esz) % 16 != 0 || strides[i] * esz >= (1ll << 40)) return false;
   }
   return true;
 }
@@ -394,6 +419,10 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   p.l_sh = l_sh;
   p.l_ss = l_ss;
   p.kv_batch_broadcast = kv_broadcast ? 1 : 0;
+  p.kv_kind = kv_kind_of(d.kv_dt);
+  p.k_scale = d.k_scale;
+  p.v_scale = d.v_scale;
+  const bool q8 = is_q8(d.kv_dt);
 
   ProfRecord rec;
   bool launched = false;
@@ -404,17 +433,22 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   const int64_t map_len = pg ? pg->page_size : d.Lcap;
   const int64_t strides[6] = {p.k_sl, p.k_sh, p.v_sl, p.v_sh, p.k_sb, p.v_sb};
   const int variant = split_variant(split_chunk(d.Lcap, ns));
-  if (variant >= 0 && d.q_dt == FD_BF16 && mma_group_ok(d.G) &&
-      d.Lcap >= mma_tile_tokens(variant) && tma_ok(d, k->data, v->data, strides, kv_batch) &&
+  // The tensor-core kernel takes bf16 queries over a bf16 cache, or bf16 /
+  // f32 queries over an 8-bit cache (converted to f16 in the kernel).
+  const int mtile = mma_tile_tokens(variant, p.kv_kind);
+  if (variant >= 0 && (d.q_dt == FD_BF16 || q8) && mma_group_ok(d.G) && d.Lcap >= mtile &&
+      tma_ok(d, k->data, v->data, strides, kv_batch) &&
       (!pg || page_size_tma_ok(pg->page_size))) {
     fd_status gs = get_encoder();
     if (gs) return gs;
     CUtensorMap tmK, tmV;
-    const int tile = pg ? p.page_rows : mma_tile_tokens(variant);
+    const int tile = pg ? p.page_rows : mtile;
+    const int box_d = q8 ? 128 : 64;            // 128-byte box rows either way
+    const int64_t esz = esize(d.kv_dt);
     const bool okk = make_kv_map(&tmK, k->data, kv_batch, map_len, d.Hkv, d.D, p.k_sb, p.k_sl,
-                                 p.k_sh, tile, 64);
+                                 p.k_sh, tile, box_d, esz);
     const bool okv = make_kv_map(&tmV, v->data, kv_batch, map_len, d.Hkv, d.D, p.v_sb, p.v_sl,
-                                 p.v_sh, tile, 64);
+                                 p.v_sh, tile, box_d, esz);
     if (okk && okv) {
       const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
       e = launch_split_mma(p, tmK, tmV, (int)d.G, variant, st, &launched, !prof);
@@ -426,7 +460,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
       if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
     }
   }
-  if (!launched && !pg && tma_ok(d, k->data, v->data, strides, kv_batch)) {
+  if (!launched && !pg && !q8 && tma_ok(d, k->data, v->data, strides, kv_batch)) {
     fd_status gs = get_encoder();
     if (gs) return gs;
     CUtensorMap tmK, tmV;
@@ -447,7 +481,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   }
   if (!launched) {
     const bool prof = prof_begin(FD_KERNEL_SPLIT, st, &rec);
-    e = launch_split_generic(p, (int)d.D, d.kv_dt == FD_BF16, st, !prof);
+    e = launch_split_generic(p, (int)d.D, st, !prof);
     prof_end(FD_KERNEL_SPLIT, st, prof, rec);
     if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
   }
@@ -680,6 +714,28 @@ fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cache,
   if (num_splits < 0 || num_splits > kMaxSplits)
     return fail(FD_ERR_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
   if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  return run_decode(d, q, k_cache, v_cache, seqlens, num_splits, scale, out, lse, stream, nullptr);
+}
+
+fd_status fd_decode_attention_quant(const fd_tensor* q, const fd_tensor* k_cache,
+                                    const fd_tensor* v_cache, const fd_tensor* k_scale,
+                                    const fd_tensor* v_scale, const fd_tensor* seqlens,
+                                    int32_t num_splits, float scale, fd_tensor* out,
+                                    fd_tensor* lse, fd_stream stream) {
+  DecodeDesc d;
+  fd_status st = validate_decode(q, k_cache, v_cache, seqlens, out, lse, 3, 0, &d, true);
+  if (st) return st;
+  if ((st = check_tensor(k_scale, "k_scale", 1))) return st;
+  if ((st = check_tensor(v_scale, "v_scale", 1))) return st;
+  if (k_scale->dtype != FD_F32 || v_scale->dtype != FD_F32)
+    return fail(FD_ERR_DTYPE, "k_scale / v_scale must be f32");
+  if (k_scale->shape[0] != d.Hkv || v_scale->shape[0] != d.Hkv)
+    return fail(FD_ERR_SHAPE, "k_scale / v_scale must have Hkv (%lld) entries", (long long)d.Hkv);
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
+  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  d.k_scale = reinterpret_cast<const float*>(k_scale->data);
+  d.v_scale = reinterpret_cast<const float*>(v_scale->data);
   return run_decode(d, q, k_cache, v_cache, seqlens, num_splits, scale, out, lse, stream, nullptr);
 }
 

@@ -18,6 +18,12 @@ constexpr int kSplitAlign = 64;   // FD_SPLIT_ALIGN
 constexpr int kMaxSplits = 256;   // FD_MAX_SPLITS
 
 // Arguments of the split-partial kernels (one CTA per (split, kv head, b)).
+// Cache element kinds of the split kernels.
+constexpr int kKvF32 = 0;
+constexpr int kKvBf16 = 1;
+constexpr int kKvI8 = 2;
+constexpr int kKvE4m3 = 3;
+
 struct SplitParams {
   const void* q;              // [B, Hq, D]
   int64_t q_sb, q_sh;         // element strides
@@ -35,6 +41,11 @@ struct SplitParams {
   float* lse;                 // natural-log lse, or nullptr
   int64_t l_sb, l_sh, l_ss;
   int kv_batch_broadcast;     // 1: every sequence reads kv batch row 0
+  // Element type of the cache (kKvF32, kKvBf16, kKvI8, kKvE4m3); the 8-bit
+  // kinds carry one dequantisation scale per kv head for K and for V.
+  int kv_kind;
+  const float* k_scale;       // [Hkv] device, 8-bit kinds only
+  const float* v_scale;
   // Paged cache (block_table != nullptr): k / v are [num_pages, page_size,
   // Hkv, D]; token j of sequence b is row j % page_size of page
   // block_table[b * bt_stride + j / page_size].  The TMA kernels load
@@ -88,9 +99,8 @@ cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
                              bool* launched, bool pdl);
 cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              int G, int variant, cudaStream_t st, bool* launched, bool pdl);
-int mma_tile_tokens(int variant);
-cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaStream_t st,
-                                 bool pdl);
+int mma_tile_tokens(int variant, int kv_kind);
+cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            int mtiles, cudaStream_t st, bool pdl);

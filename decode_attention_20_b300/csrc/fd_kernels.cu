@@ -85,11 +85,11 @@ cudaError_t launch_split_tma(const SplitParams& p, const CUtensorMap& tmK,
   }
 }
 
-template <int NT, int WN, int W, int T, int NSTAGE>
+template <int KVQ, int NT, int WN, int W, int T, int NSTAGE>
 static cudaError_t launch_mma_variant(const SplitParams& p, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, cudaStream_t st, bool pdl) {
-  using C = MmaCfg<NT, WN, W, T, NSTAGE>;
-  auto kern = split_mma_kernel<NT, WN, W, T, NSTAGE>;
+  using C = MmaCfg<KVQ, NT, WN, W, T, NSTAGE>;
+  auto kern = split_mma_kernel<KVQ, NT, WN, W, T, NSTAGE>;
   static unsigned long long attr_set = 0ull;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -104,33 +104,56 @@ static cudaError_t launch_mma_variant(const SplitParams& p, const CUtensorMap& t
                    tmK, tmV);
 }
 
-int mma_tile_tokens(int variant) { return variant == 1 ? 128 : 64; }
+int mma_tile_tokens(int variant, int kv_kind) {
+  if (kv_kind == kKvI8 || kv_kind == kKvE4m3) return variant == 2 ? 64 : 128;
+  return variant == 1 ? 128 : 64;
+}
 
-cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             int G, int variant, cudaStream_t st, bool* launched, bool pdl) {
+template <int KVQ>
+static cudaError_t launch_split_mma_kind(const SplitParams& p, const CUtensorMap& tmK,
+                                         const CUtensorMap& tmV, int G, int variant,
+                                         cudaStream_t st, bool* launched, bool pdl) {
   *launched = true;
-  if (variant == 1) {            // 8 warps, 128-token tiles, 3 stages
+  if (KVQ != 0 && variant == 2) {   // 8-bit: 4 warps, 64-token tiles (8 KB + 8 KB), 6 stages
     switch (G) {
-      case 4: case 8: return launch_mma_variant<1, 1, 8, 128, 3>(p, tmK, tmV, st, pdl);
-      case 16: return launch_mma_variant<2, 1, 8, 128, 3>(p, tmK, tmV, st, pdl);
-      case 32: return launch_mma_variant<4, 2, 8, 128, 3>(p, tmK, tmV, st, pdl);
-      case 64: return launch_mma_variant<8, 4, 8, 128, 3>(p, tmK, tmV, st, pdl);
+      case 4: case 8: return launch_mma_variant<KVQ, 1, 1, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 16: return launch_mma_variant<KVQ, 2, 1, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 32: return launch_mma_variant<KVQ, 4, 2, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 64: return launch_mma_variant<KVQ, 8, 4, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      default: break;
+    }
+  } else if (KVQ != 0) {         // 8-bit: 128-token tiles (16 KB + 16 KB), 3 stages;
+    switch (G) {                 // 8 warps (variant 1, one n-tile) or 4
+      case 4: case 8:
+        if (variant == 1) return launch_mma_variant<KVQ, 1, 1, 8, 128, 3>(p, tmK, tmV, st, pdl);
+        return launch_mma_variant<KVQ, 1, 1, 4, 128, 3>(p, tmK, tmV, st, pdl);
+      case 16: return launch_mma_variant<KVQ, 2, 1, 4, 128, 3>(p, tmK, tmV, st, pdl);
+      case 32: return launch_mma_variant<KVQ, 4, 2, 4, 128, 3>(p, tmK, tmV, st, pdl);
+      case 64: return launch_mma_variant<KVQ, 8, 4, 4, 128, 3>(p, tmK, tmV, st, pdl);
+      default: break;
+    }
+  } else if (variant == 1) {     // 8 warps, 128-token tiles, 3 stages
+    switch (G) {
+      case 4: case 8: return launch_mma_variant<0, 1, 1, 8, 128, 3>(p, tmK, tmV, st, pdl);
+      case 16: return launch_mma_variant<0, 2, 1, 8, 128, 3>(p, tmK, tmV, st, pdl);
+      case 32: return launch_mma_variant<0, 4, 2, 8, 128, 3>(p, tmK, tmV, st, pdl);
+      case 64: return launch_mma_variant<0, 8, 4, 8, 128, 3>(p, tmK, tmV, st, pdl);
       default: break;
     }
   } else if (variant == 2) {     // 4 warps, 64-token tiles, 3 stages (two CTAs per SM)
     switch (G) {
-      case 4: case 8: return launch_mma_variant<1, 1, 4, 64, 3>(p, tmK, tmV, st, pdl);
-      case 16: return launch_mma_variant<2, 1, 4, 64, 3>(p, tmK, tmV, st, pdl);
-      case 32: return launch_mma_variant<4, 2, 4, 64, 3>(p, tmK, tmV, st, pdl);
-      case 64: return launch_mma_variant<8, 4, 4, 64, 3>(p, tmK, tmV, st, pdl);
+      case 4: case 8: return launch_mma_variant<0, 1, 1, 4, 64, 3>(p, tmK, tmV, st, pdl);
+      case 16: return launch_mma_variant<0, 2, 1, 4, 64, 3>(p, tmK, tmV, st, pdl);
+      case 32: return launch_mma_variant<0, 4, 2, 4, 64, 3>(p, tmK, tmV, st, pdl);
+      case 64: return launch_mma_variant<0, 8, 4, 4, 64, 3>(p, tmK, tmV, st, pdl);
       default: break;
     }
   } else {                       // 4 warps, 64-token tiles, 6 stages
     switch (G) {
-      case 4: case 8: return launch_mma_variant<1, 1, 4, 64, 6>(p, tmK, tmV, st, pdl);
-      case 16: return launch_mma_variant<2, 1, 4, 64, 6>(p, tmK, tmV, st, pdl);
-      case 32: return launch_mma_variant<4, 2, 4, 64, 6>(p, tmK, tmV, st, pdl);
-      case 64: return launch_mma_variant<8, 4, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 4: case 8: return launch_mma_variant<0, 1, 1, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 16: return launch_mma_variant<0, 2, 1, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 32: return launch_mma_variant<0, 4, 2, 4, 64, 6>(p, tmK, tmV, st, pdl);
+      case 64: return launch_mma_variant<0, 8, 4, 4, 64, 6>(p, tmK, tmV, st, pdl);
       default: break;
     }
   }
@@ -138,17 +161,31 @@ cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const
   return cudaSuccess;
 }
 
-cudaError_t launch_split_generic(const SplitParams& p, int D, int kv_bf16, cudaStream_t st,
-                                 bool pdl) {
+cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             int G, int variant, cudaStream_t st, bool* launched, bool pdl) {
+  switch (p.kv_kind) {
+    case kKvBf16: return launch_split_mma_kind<0>(p, tmK, tmV, G, variant, st, launched, pdl);
+    case kKvI8: return launch_split_mma_kind<1>(p, tmK, tmV, G, variant, st, launched, pdl);
+    case kKvE4m3: return launch_split_mma_kind<2>(p, tmK, tmV, G, variant, st, launched, pdl);
+    default: *launched = false; return cudaSuccess;
+  }
+}
+
+template <int D>
+static cudaError_t launch_generic_d(const SplitParams& p, cudaStream_t st, bool pdl) {
   const dim3 grid(p.ns, p.Hq, p.B);
-  if (D == 128) {
-    if (kv_bf16) return launch_ex(split_generic_kernel<128, true>, grid, dim3(128), 0, st, pdl, p);
-    return launch_ex(split_generic_kernel<128, false>, grid, dim3(128), 0, st, pdl, p);
+  switch (p.kv_kind) {
+    case kKvF32: return launch_ex(split_generic_kernel<D, kKvF32>, grid, dim3(128), 0, st, pdl, p);
+    case kKvBf16: return launch_ex(split_generic_kernel<D, kKvBf16>, grid, dim3(128), 0, st, pdl, p);
+    case kKvI8: return launch_ex(split_generic_kernel<D, kKvI8>, grid, dim3(128), 0, st, pdl, p);
+    case kKvE4m3: return launch_ex(split_generic_kernel<D, kKvE4m3>, grid, dim3(128), 0, st, pdl, p);
+    default: return cudaErrorInvalidValue;
   }
-  if (D == 64) {
-    if (kv_bf16) return launch_ex(split_generic_kernel<64, true>, grid, dim3(128), 0, st, pdl, p);
-    return launch_ex(split_generic_kernel<64, false>, grid, dim3(128), 0, st, pdl, p);
-  }
+}
+
+cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, bool pdl) {
+  if (D == 128) return launch_generic_d<128>(p, st, pdl);
+  if (D == 64) return launch_generic_d<64>(p, st, pdl);
   return cudaErrorInvalidValue;
 }
 

@@ -426,7 +426,22 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
 
 // ------------------------------------------------------------------ generic
 
-template <int D, bool KV_BF16>
+// One cache element as fp32 (8-bit kinds: the code, before its scale).
+template <int KVK>
+__device__ __forceinline__ float kv_elem(const void* base, int64_t i) {
+  if constexpr (KVK == kKvBf16) {
+    return __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(base)[i]) << 16);
+  } else if constexpr (KVK == kKvI8) {
+    return float(reinterpret_cast<const int8_t*>(base)[i]);
+  } else if constexpr (KVK == kKvE4m3) {
+    const __half_raw h = __nv_cvt_fp8_to_halfraw(reinterpret_cast<const __nv_fp8_storage_t*>(base)[i], __NV_E4M3);
+    return __half2float(__half(h));
+  } else {
+    return reinterpret_cast<const float*>(base)[i];
+  }
+}
+
+template <int D, int KVK>
 __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constant__ SplitParams p) {
   pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   constexpr int NW = 4;
@@ -443,6 +458,11 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
   int begin, end;
   split_range(len, p.ns, split, begin, end);
 
+  // 8-bit caches: the K scale joins the score scale, the V scale multiplies
+  // the normalised output.
+  constexpr bool kQuant = (KVK == kKvI8 || KVK == kKvE4m3);
+  const float qs = kQuant ? p.scale_log2 * p.k_scale[g] : p.scale_log2;
+  const float vs = kQuant ? p.v_scale[g] : 1.f;
   float q[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) {
@@ -452,7 +472,7 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
       x = __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.q)[b * p.q_sb + h * p.q_sh + d]) << 16);
     else
       x = reinterpret_cast<const float*>(p.q)[b * p.q_sb + h * p.q_sh + d];
-    q[e] = x * p.scale_log2;
+    q[e] = x * qs;
   }
   float acc[EPL];
 #pragma unroll
@@ -474,13 +494,8 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
     const int64_t vo = vbase + g * p.v_sh + lane * EPL;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
-      if (KV_BF16) {
-        kf[e] = __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.k)[ko + e]) << 16);
-        vf[e] = __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.v)[vo + e]) << 16);
-      } else {
-        kf[e] = reinterpret_cast<const float*>(p.k)[ko + e];
-        vf[e] = reinterpret_cast<const float*>(p.v)[vo + e];
-      }
+      kf[e] = kv_elem<KVK>(p.k, ko + e);
+      vf[e] = kv_elem<KVK>(p.v, vo + e);
     }
     float s = 0.f;
 #pragma unroll
@@ -516,7 +531,7 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
         o += f * acc_s[w][d];
       }
     }
-    p.o[b * p.o_sb + h * p.o_sh + split * p.o_ss + d] = lt > 0.f ? o / lt : 0.f;
+    p.o[b * p.o_sb + h * p.o_sh + split * p.o_ss + d] = lt > 0.f ? vs * (o / lt) : 0.f;
     if (d == 0 && p.lse != nullptr)
       p.lse[b * p.l_sb + h * p.l_sh + split * p.l_ss] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
   }

@@ -24,7 +24,13 @@
 //   O^T[128 dims x 8 heads] += V^T[128 x 16 tok] . P^T[16 tok x 8 heads]
 //                                                   2 x 8 mma (k = 16 tokens)
 // K and V tiles arrive by TMA with the 128-byte swizzle (two 64-column boxes
-// per tile), so every ldmatrix is bank-conflict free.  The probabilities
+// per tile), so every ldmatrix is bank-conflict free.
+//
+// 8-bit caches (int8 or e4m3 codes with one scale per kv head for K and for
+// V): one 128-byte box per row, codes turned into exact f16 values in
+// registers, f16 mma.sync with the queries in f16 (per-head power-of-two
+// rescale); the K scale joins the score scale and the V scale the final
+// normalisation.  Half the bytes per token of the bf16 cache.  The probabilities
 // enter the PV product as a hi + lo pair of bf16 values (two MMAs), which
 // keeps ~16 mantissa bits; the running sum l stays in fp32.
 #pragma once
@@ -75,6 +81,75 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// D = A(16x16 f16, row) * B(16x8 f16, col) + C (fp32)
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (lo, hi) floats -> f16x2 with round-to-nearest-even; lo in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Four 8-bit cache codes in a word -> two f16x2 values, exactly: bytes 0, 1
+// into `lo` (byte 0 in the low half), bytes 2, 3 into `hi`.
+//  - int8 (KVQ 1): the word arrives with every byte's sign bit flipped (code
+//    + 128 as an unsigned byte u); the f16 with bit pattern 0x6400 | u is
+//    1024 + u = code + kI8Bias (integers below 2048 are exact in f16).  The
+//    bias is left in: in QK^T it adds kI8Bias * sum_d q_d to every score of
+//    a head, which the score computation subtracts again, and in PV it adds
+//    kI8Bias * sum_j p_j, which the epilogue removes with the normaliser.
+//  - e4m3 (KVQ 2): every e4m3 value is exactly representable in f16 (3 of
+//    f16's 10 mantissa bits, exponents 2^-9 .. 2^8 inside f16's range); the
+//    hardware converts two at a time.
+constexpr float kI8Bias = 1152.f;
+
+template <int KVQ>
+__device__ __forceinline__ void q8_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  if constexpr (KVQ == 1) {
+    lo = __byte_perm(x, 0x64646464u, 0x5140);
+    hi = __byte_perm(x, 0x64646464u, 0x7362);
+  } else {
+    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(x & 0xffffu), __NV_E4M3);
+    const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(x >> 16), __NV_E4M3);
+    lo = uint32_t(a.x) | (uint32_t(a.y) << 16);
+    hi = uint32_t(b.x) | (uint32_t(b.y) << 16);
+  }
+}
+
+// A 16-byte shared-memory load of 8-bit codes, prepared for q8_to_f16x2x2.
+template <int KVQ>
+__device__ __forceinline__ uint4 lds128_q8(uint32_t addr) {
+  uint4 v = lds128(addr);
+  if constexpr (KVQ == 1) {
+    v.x ^= 0x80808080u;
+    v.y ^= 0x80808080u;
+    v.z ^= 0x80808080u;
+    v.w ^= 0x80808080u;
+  }
+  return v;
+}
+
 // Byte offset of (row, 16-byte chunk) inside a 128-byte-swizzled box whose
 // rows are 128 bytes (the TMA SWIZZLE_128B pattern on a 1024-byte aligned
 // base: chunk index XOR row % 8).
@@ -84,8 +159,10 @@ __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
 
 // ------------------------------------------------------------------ config
 
-template <int NT_, int WN_, int W_, int T_, int NSTAGE_>
+template <int KVQ_, int NT_, int WN_, int W_, int T_, int NSTAGE_>
 struct MmaCfg {
+  static constexpr int KVQ = KVQ_;             // cache: 0 bf16, 1 int8, 2 e4m3
+  static constexpr bool Q8 = KVQ_ != 0;
   static constexpr int NT = NT_;               // 8-head n-tiles per kv head (ceil(G/8))
   static constexpr int WN = WN_;               // warps sharing a token block (split n-tiles)
   static constexpr int NPW = NT / WN;          // n-tiles per warp
@@ -97,23 +174,25 @@ struct MmaCfg {
   static constexpr int THREADS = W * 32;
   static constexpr int BLK = T / 16;           // 16-token blocks per tile
   static constexpr int BPW = BLK / WT;         // blocks per warp per tile
-  static constexpr int HALF_BYTES = T * 128;   // [T][64] bf16, swizzled
-  static constexpr int STAGE_BYTES = 4 * HALF_BYTES;   // K lo, K hi, V lo, V hi
+  // One swizzled box: [T][64] bf16, or [T][128] 8-bit codes; a stage holds
+  // K lo, K hi, V lo, V hi (bf16) or K, V (8-bit).
+  static constexpr int HALF_BYTES = T * 128;
+  static constexpr int STAGE_BYTES = (Q8 ? 2 : 4) * HALF_BYTES;
   static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
   static constexpr int GP = NT * 8;            // padded heads
   static constexpr int SMEM_BYTES = 1024 + RING_BYTES + 2 * NSTAGE * 8 + 16;
   static_assert(NT % WN == 0, "n-tiles split evenly over warps");
   static_assert(W % WN == 0 && BLK % WT == 0 && BPW >= 1, "blocks split evenly over warps");
-  static_assert(WT * GP * (D + 3) * 4 <= RING_BYTES, "epilogue fits the ring");
+  static_assert(WT * GP * (D + 3) * 4 + GP * 4 <= RING_BYTES, "epilogue fits the ring");
   static_assert(HALF_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
 };
 
-template <int NT, int WN, int W, int T, int NSTAGE>
-__global__ void __launch_bounds__(W * 32, 1)
+template <int KVQ, int NT, int WN, int W, int T, int NSTAGE>
+__global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     split_mma_kernel(const __grid_constant__ SplitParams p,
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
-  using C = MmaCfg<NT, WN, W, T, NSTAGE>;
+  using C = MmaCfg<KVQ, NT, WN, W, T, NSTAGE>;
   pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   constexpr int NPW = C::NPW;
   extern __shared__ unsigned char smem_raw[];
@@ -145,6 +224,7 @@ __global__ void __launch_bounds__(W * 32, 1)
     *abort_s = 0;
     fence_barrier_init();
   }
+
   __syncthreads();
 
   uint64_t policy = 0;
@@ -155,10 +235,15 @@ __global__ void __launch_bounds__(W * 32, 1)
     mbar_arrive_expect_tx(&full_bar[s], C::STAGE_BYTES);
     const int tok = begin + t * C::T;
     if (p.block_table == nullptr) {
-      tma_load_4d(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
-      tma_load_4d(stage + C::HALF_BYTES, &tmK, &full_bar[s], 64, g, tok, kvb, policy);
-      tma_load_4d(stage + 2 * C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
-      tma_load_4d(stage + 3 * C::HALF_BYTES, &tmV, &full_bar[s], 64, g, tok, kvb, policy);
+      if constexpr (C::Q8) {
+        tma_load_4d(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
+        tma_load_4d(stage + C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
+      } else {
+        tma_load_4d(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
+        tma_load_4d(stage + C::HALF_BYTES, &tmK, &full_bar[s], 64, g, tok, kvb, policy);
+        tma_load_4d(stage + 2 * C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
+        tma_load_4d(stage + 3 * C::HALF_BYTES, &tmV, &full_bar[s], 64, g, tok, kvb, policy);
+      }
     } else {
       // Paged cache: the tile is page_rows-row segments, each inside one page
       // (tiles start on multiples of 64 tokens; page_rows = min(64, page
@@ -170,10 +255,15 @@ __global__ void __launch_bounds__(W * 32, 1)
         const int pid = tk < end ? page_of(p, b, tk, -1) : -1;
         const int off = tk % p.page_size;
         const int so = sg * p.page_rows * 128;
-        tma_load_4d(stage + so, &tmK, &full_bar[s], 0, g, off, pid, policy);
-        tma_load_4d(stage + C::HALF_BYTES + so, &tmK, &full_bar[s], 64, g, off, pid, policy);
-        tma_load_4d(stage + 2 * C::HALF_BYTES + so, &tmV, &full_bar[s], 0, g, off, pid, policy);
-        tma_load_4d(stage + 3 * C::HALF_BYTES + so, &tmV, &full_bar[s], 64, g, off, pid, policy);
+        if constexpr (C::Q8) {
+          tma_load_4d(stage + so, &tmK, &full_bar[s], 0, g, off, pid, policy);
+          tma_load_4d(stage + C::HALF_BYTES + so, &tmV, &full_bar[s], 0, g, off, pid, policy);
+        } else {
+          tma_load_4d(stage + so, &tmK, &full_bar[s], 0, g, off, pid, policy);
+          tma_load_4d(stage + C::HALF_BYTES + so, &tmK, &full_bar[s], 64, g, off, pid, policy);
+          tma_load_4d(stage + 2 * C::HALF_BYTES + so, &tmV, &full_bar[s], 0, g, off, pid, policy);
+          tma_load_4d(stage + 3 * C::HALF_BYTES + so, &tmV, &full_bar[s], 64, g, off, pid, policy);
+        }
       }
     }
   };
@@ -187,10 +277,11 @@ __global__ void __launch_bounds__(W * 32, 1)
     }
   }
 
-  // ---- query fragments (B operand of S^T = K . Q^T): B[k = dim][n = head]
-  // lane holds dims 2(lane%4)+{0,1} and +8 of head (lane/4) of each n-tile.
+  // ---- raw query loads (fp32 bit patterns), turned into MMA fragments below.
+  // (Issuing them ahead of the ring's first copies was measured: it delays
+  // the copies and gains nothing.)
   const int G = p.G;
-  uint32_t qf[NPW][8][2];
+  uint32_t qraw[NPW][8][4];
 #pragma unroll
   for (int j = 0; j < NPW; ++j) {
     const int hl = (wn * NPW + j) * 8 + (lane >> 2);          // head within the group
@@ -198,15 +289,90 @@ __global__ void __launch_bounds__(W * 32, 1)
     const int h = g * G + (real ? hl : 0);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      const int d0 = ks * 16 + 2 * (lane & 3);
-      uint32_t lo = 0u, hi = 0u;
-      if (real) {
-        const uint16_t* qp = reinterpret_cast<const uint16_t*>(p.q) + b * p.q_sb + h * p.q_sh;
-        lo = uint32_t(qp[d0]) | (uint32_t(qp[d0 + 1]) << 16);
-        hi = uint32_t(qp[d0 + 8]) | (uint32_t(qp[d0 + 9]) << 16);
+      // bf16 cache: dims ks*16 + 2(lane%4) + {0, 1, 8, 9}; 8-bit cache: dims
+      // 16(2(lane%4) + ks/4) + 4(ks%4) + {0, 1, 2, 3} (see the fragments below)
+      const int d0 = C::Q8 ? 16 * (2 * (lane & 3) + (ks >> 2)) + 4 * (ks & 3)
+                           : ks * 16 + 2 * (lane & 3);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int d = C::Q8 ? d0 + i : d0 + (i & 1) + (i >> 1) * 8;
+        uint32_t x = 0u;
+        if (real) {
+          const int64_t o = b * p.q_sb + h * p.q_sh + d;
+          x = p.q_bf16 ? uint32_t(reinterpret_cast<const uint16_t*>(p.q)[o]) << 16
+                       : __float_as_uint(reinterpret_cast<const float*>(p.q)[o]);
+        }
+        qraw[j][ks][i] = x;                    // fp32 bit pattern of the query
       }
-      qf[j][ks][0] = lo;
-      qf[j][ks][1] = hi;
+    }
+  }
+  const float ks_g = C::Q8 ? p.k_scale[g] : 1.f;
+
+  // ---- query fragments (B operand of S^T = K . Q^T): B[k = dim][n = head]
+  // lane holds dims 2(lane%4)+{0,1} and +8 of head (lane/4) of each n-tile.
+  uint32_t qf[NPW][8][2];
+  // 8-bit caches: per-lane score multipliers of heads hA = 2(lane%4) and
+  // hB = hA + 1 of each n-tile (score scale x K scale x 2^-e of the head's
+  // query rescale, below).
+  float sl2h[NPW][2];
+  float shift[NPW][2];   // int8: sl2h * kI8Bias * sum_d q_d (f16 values) per head
+  if constexpr (!C::Q8) {
+    // bf16 queries: the top halves of the fp32 patterns are the bf16 values.
+#pragma unroll
+    for (int j = 0; j < NPW; ++j) {
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qf[j][ks][0] = (qraw[j][ks][0] >> 16) | (qraw[j][ks][1] & 0xffff0000u);
+        qf[j][ks][1] = (qraw[j][ks][2] >> 16) | (qraw[j][ks][3] & 0xffff0000u);
+      }
+      sl2h[j][0] = sl2h[j][1] = p.scale_log2;
+      shift[j][0] = shift[j][1] = 0.f;
+    }
+  } else {
+    // The contraction over head dims may take the dims in any order, as long
+    // as the K and Q fragments agree.  Lane (n = lane/4, t = lane%4) reads
+    // whole words of a K row, so in k-step ks its k positions 2t, 2t+1 are
+    // dims 16c + 4w + {0, 1} and positions 2t+8, 2t+9 dims 16c + 4w + {2, 3},
+    // with c = 2t + ks/4 (the row's 16-byte chunk) and w = ks % 4 (its word).
+    // The queries of each head are scaled by 2^e (e from the head's largest
+    // |q|, so that it lands in [2^14, 2^15)) and rounded to f16; the score
+    // multiplier takes 2^-e back.
+#pragma unroll
+    for (int j = 0; j < NPW; ++j) {
+      float qv[8][4];
+      float amax = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          qv[ks][i] = __uint_as_float(qraw[j][ks][i]);
+          amax = fmaxf(amax, fabsf(qv[ks][i]));
+        }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int E = int((__float_as_uint(amax) >> 23) & 0xffu);
+      const int e = (E == 0) ? 0 : min(100, max(-100, 141 - E));
+      const float up = __uint_as_float(uint32_t(127 + e) << 23);       // 2^e
+      const float down = __uint_as_float(uint32_t(127 - e) << 23);     // 2^-e
+      float qsum = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        qf[j][ks][0] = pack_f16x2(qv[ks][0] * up, qv[ks][1] * up);
+        qf[j][ks][1] = pack_f16x2(qv[ks][2] * up, qv[ks][3] * up);
+        if constexpr (KVQ == 1) {
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&qf[j][ks][0]));
+          const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&qf[j][ks][1]));
+          qsum += (a.x + a.y) + (c.x + c.y);
+        }
+      }
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+      qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+      const float mine = p.scale_log2 * ks_g * down;                  // head lane/4
+      const float mshift = (KVQ == 1) ? mine * (kI8Bias * qsum) : 0.f;
+      sl2h[j][0] = __shfl_sync(0xffffffffu, mine, 8 * (lane & 3));     // head 2(lane%4)
+      sl2h[j][1] = __shfl_sync(0xffffffffu, mine, 8 * (lane & 3) + 4); // head 2(lane%4)+1
+      shift[j][0] = __shfl_sync(0xffffffffu, mshift, 8 * (lane & 3));
+      shift[j][1] = __shfl_sync(0xffffffffu, mshift, 8 * (lane & 3) + 4);
     }
   }
 
@@ -228,7 +394,7 @@ __global__ void __launch_bounds__(W * 32, 1)
     const int s = t % C::NSTAGE;
     if (!mbar_wait_or_abort(&full_bar[s], (t / C::NSTAGE) & 1, abort_s)) break;
     const uint32_t kbase = smem_u32(smem + s * C::STAGE_BYTES);
-    const uint32_t vbase = kbase + 2 * C::HALF_BYTES;
+    const uint32_t vbase = kbase + (C::Q8 ? 1 : 2) * C::HALF_BYTES;   // V box(es) after K
     const int nvalid = min(C::T, end - (begin + t * C::T));
 #pragma unroll 1
     for (int bb = 0; bb < C::BPW; ++bb) {
@@ -239,7 +405,7 @@ __global__ void __launch_bounds__(W * 32, 1)
       for (int j = 0; j < NPW; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
-      {
+      if constexpr (!C::Q8) {
         const int arow = row0 + r8 + ((lane >> 3) & 1) * 8;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
@@ -250,6 +416,25 @@ __global__ void __launch_bounds__(W * 32, 1)
           ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
           for (int j = 0; j < NPW; ++j) mma_bf16_16816(sacc[j], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
+        }
+      } else {
+        // A = K rows row0 + lane/4 (a0, a2) and + 8 (a1, a3); chunks 2t and
+        // 2t + 1 of each (the dims order of the query fragments).  Rows of
+        // one parity read even chunks, the others odd ones after the
+        // swizzle, so the 16-byte loads are bank-conflict free.
+        const int ra = row0 + (lane >> 2);
+        const int c0 = 2 * (lane & 3);
+        const uint4 kA0 = lds128_q8<KVQ>(kbase + swz128(ra, c0));
+        const uint4 kA1 = lds128_q8<KVQ>(kbase + swz128(ra, c0 + 1));
+        const uint4 kB0 = lds128_q8<KVQ>(kbase + swz128(ra + 8, c0));
+        const uint4 kB1 = lds128_q8<KVQ>(kbase + swz128(ra + 8, c0 + 1));
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          q8_to_f16x2x2<KVQ>(u4_word(ks < 4 ? kA0 : kA1, ks & 3), a0, a2);
+          q8_to_f16x2x2<KVQ>(u4_word(ks < 4 ? kB0 : kB1, ks & 3), a1, a3);
+#pragma unroll
+          for (int j = 0; j < NPW; ++j) mma_f16_16816(sacc[j], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
         }
       }
       // ---- online softmax; lane holds tokens tA = lane/4, tB = tA + 8 and
@@ -262,10 +447,14 @@ __global__ void __launch_bounds__(W * 32, 1)
       float alpha[NPW][2];
 #pragma unroll
       for (int j = 0; j < NPW; ++j) {
-        float sA0 = vA ? sacc[j][0] * sl2 : kNegInf;   // (tA, hA)
-        float sA1 = vA ? sacc[j][1] * sl2 : kNegInf;   // (tA, hB)
-        float sB0 = vB ? sacc[j][2] * sl2 : kNegInf;   // (tB, hA)
-        float sB1 = vB ? sacc[j][3] * sl2 : kNegInf;   // (tB, hB)
+        const float f0 = C::Q8 ? sl2h[j][0] : sl2;
+        const float f1 = C::Q8 ? sl2h[j][1] : sl2;
+        // (int8: one fused multiply-add also removes the code bias's share
+        // of the score, exactly rounded once.)
+        float sA0 = vA ? fmaf(sacc[j][0], f0, -shift[j][0]) : kNegInf;   // (tA, hA)
+        float sA1 = vA ? fmaf(sacc[j][1], f1, -shift[j][1]) : kNegInf;   // (tA, hB)
+        float sB0 = vB ? fmaf(sacc[j][2], f0, -shift[j][0]) : kNegInf;   // (tB, hA)
+        float sB1 = vB ? fmaf(sacc[j][3], f1, -shift[j][1]) : kNegInf;   // (tB, hB)
         float mx0 = fmaxf(sA0, sB0), mx1 = fmaxf(sA1, sB1);
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) {
@@ -287,18 +476,38 @@ __global__ void __launch_bounds__(W * 32, 1)
         // Probabilities as hi + lo bf16 pairs (hi = RNE(p), lo = RNE(p - hi)):
         // two PV products carry ~16 mantissa bits, so the bf16 operand adds
         // no visible error; the running sum keeps the fp32 values.
-        const uint32_t XA = pack_bf16x2(pA0, pA1);      // token tA, heads hA hB
-        const uint32_t XB = pack_bf16x2(pB0, pB1);      // token tB
-        const uint32_t XAl = pack_bf16x2(pA0 - __uint_as_float(XA << 16),
-                                         pA1 - __uint_as_float(XA & 0xffff0000u));
-        const uint32_t XBl = pack_bf16x2(pB0 - __uint_as_float(XB << 16),
-                                         pB1 - __uint_as_float(XB & 0xffff0000u));
-        l_run[j][0] = l_run[j][0] * alpha[j][0] + (pA0 + pB0);
-        l_run[j][1] = l_run[j][1] * alpha[j][1] + (pA1 + pB1);
-        pb[j][0] = movmatrix_trans(XA);                 // B[k = tokens 0-7][n = head]
-        pb[j][1] = movmatrix_trans(XB);                 // B[k = tokens 8-15][n = head]
-        pbl[j][0] = movmatrix_trans(XAl);
-        pbl[j][1] = movmatrix_trans(XBl);
+        if constexpr (KVQ == 1) {
+          // The normaliser sums the f16 probabilities the PV product uses,
+          // so that the epilogue's bias removal is exact.
+          const uint32_t XA = pack_f16x2(pA0, pA1);
+          const uint32_t XB = pack_f16x2(pB0, pB1);
+          const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&XA));
+          const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&XB));
+          l_run[j][0] = l_run[j][0] * alpha[j][0] + (a.x + c.x);
+          l_run[j][1] = l_run[j][1] * alpha[j][1] + (a.y + c.y);
+          pb[j][0] = movmatrix_trans(XA);
+          pb[j][1] = movmatrix_trans(XB);
+        } else {
+          l_run[j][0] = l_run[j][0] * alpha[j][0] + (pA0 + pB0);
+          l_run[j][1] = l_run[j][1] * alpha[j][1] + (pA1 + pB1);
+        }
+        if constexpr (!C::Q8) {
+          const uint32_t XA = pack_bf16x2(pA0, pA1);      // token tA, heads hA hB
+          const uint32_t XB = pack_bf16x2(pB0, pB1);      // token tB
+          const uint32_t XAl = pack_bf16x2(pA0 - __uint_as_float(XA << 16),
+                                           pA1 - __uint_as_float(XA & 0xffff0000u));
+          const uint32_t XBl = pack_bf16x2(pB0 - __uint_as_float(XB << 16),
+                                           pB1 - __uint_as_float(XB & 0xffff0000u));
+          pb[j][0] = movmatrix_trans(XA);                 // B[k = tokens 0-7][n = head]
+          pb[j][1] = movmatrix_trans(XB);                 // B[k = tokens 8-15][n = head]
+          pbl[j][0] = movmatrix_trans(XAl);
+          pbl[j][1] = movmatrix_trans(XBl);
+        } else if constexpr (KVQ == 2) {
+          // f16 keeps 11 significant bits of p (<= 256 under the lazy
+          // rescale): one PV product suffices.
+          pb[j][0] = movmatrix_trans(pack_f16x2(pA0, pA1));
+          pb[j][1] = movmatrix_trans(pack_f16x2(pB0, pB1));
+        }
       }
       if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll
@@ -323,22 +532,54 @@ __global__ void __launch_bounds__(W * 32, 1)
           keep01 = (tk < nvalid ? 0x0000ffffu : 0u) | (tk + 1 < nvalid ? 0xffff0000u : 0u);
           keep23 = (tk + 8 < nvalid ? 0x0000ffffu : 0u) | (tk + 9 < nvalid ? 0xffff0000u : 0u);
         }
-        const int vrow = row0 + r8 + (lane >> 4) * 8;
+        if constexpr (!C::Q8) {
+          const int vrow = row0 + r8 + (lane >> 4) * 8;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int col = mt * 16 + ((lane >> 3) & 1) * 8;
-          const uint32_t addr =
-              vbase + (col >> 6) * C::HALF_BYTES + swz128(vrow, (col & 63) >> 3);
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(addr, a0, a1, a2, a3);
-          a0 &= keep01;
-          a1 &= keep01;
-          a2 &= keep23;
-          a3 &= keep23;
+          for (int mt = 0; mt < 8; ++mt) {
+            const int col = mt * 16 + ((lane >> 3) & 1) * 8;
+            const uint32_t addr =
+                vbase + (col >> 6) * C::HALF_BYTES + swz128(vrow, (col & 63) >> 3);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(addr, a0, a1, a2, a3);
+            a0 &= keep01;
+            a1 &= keep01;
+            a2 &= keep23;
+            a3 &= keep23;
 #pragma unroll
-          for (int j = 0; j < NPW; ++j) {
-            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
-            mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pbl[j][0], pbl[j][1]);
+            for (int j = 0; j < NPW; ++j) {
+              mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+              mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pbl[j][0], pbl[j][1]);
+            }
+          }
+        } else {
+          // A = V^T with the dims reordered so that a lane reads whole
+          // 16-byte chunks: lane (r = lane/4, t = lane%4) reads chunk r of
+          // token rows 2t, 2t+1, 2t+8, 2t+9; row r of m-tile mt is dim
+          // 16r + 2mt and row r + 8 is dim 16r + 2mt + 1.  A byte permute
+          // pairs the two tokens of each f16x2 operand.  Row parities split
+          // the even and odd chunks, so the loads are conflict free.
+          const int vr = row0 + 2 * (lane & 3);
+          const int ch = lane >> 2;
+          const uint4 vA = lds128_q8<KVQ>(vbase + swz128(vr, ch));
+          const uint4 vB = lds128_q8<KVQ>(vbase + swz128(vr + 1, ch));
+          const uint4 vC = lds128_q8<KVQ>(vbase + swz128(vr + 8, ch));
+          const uint4 vD = lds128_q8<KVQ>(vbase + swz128(vr + 9, ch));
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+            const uint32_t iAB = __byte_perm(u4_word(vA, mt >> 1), u4_word(vB, mt >> 1), sel);
+            const uint32_t iCD = __byte_perm(u4_word(vC, mt >> 1), u4_word(vD, mt >> 1), sel);
+            uint32_t a0, a1, a2, a3;
+            q8_to_f16x2x2<KVQ>(iAB, a0, a1);
+            q8_to_f16x2x2<KVQ>(iCD, a2, a3);
+            if constexpr (KVQ == 2) {      // e4m3 codes past the split may be NaN
+              a0 &= keep01;
+              a1 &= keep01;
+              a2 &= keep23;
+              a3 &= keep23;
+            }
+#pragma unroll
+            for (int j = 0; j < NPW; ++j) mma_f16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
           }
         }
       }
@@ -385,11 +626,14 @@ __global__ void __launch_bounds__(W * 32, 1)
     const int hA = hbase + 2 * (lane & 3);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
-      const int d = mt * 16 + (lane >> 2);
+      // Accumulator rows r = lane/4 and r + 8 of m-tile mt are dims
+      // mt*16 + r and + 8 (bf16), or 16r + 2mt and 16r + 2mt + 1 (8-bit).
+      const int d = C::Q8 ? 16 * (lane >> 2) + 2 * mt : mt * 16 + (lane >> 2);
+      const int d2 = C::Q8 ? d + 1 : d + 8;
       ACC_s[(wt * C::GP + hA) * C::D + d] = acc[j][mt][0];
       ACC_s[(wt * C::GP + hA + 1) * C::D + d] = acc[j][mt][1];
-      ACC_s[(wt * C::GP + hA) * C::D + d + 8] = acc[j][mt][2];
-      ACC_s[(wt * C::GP + hA + 1) * C::D + d + 8] = acc[j][mt][3];
+      ACC_s[(wt * C::GP + hA) * C::D + d2] = acc[j][mt][2];
+      ACC_s[(wt * C::GP + hA + 1) * C::D + d2] = acc[j][mt][3];
     }
   }
   __syncthreads();
@@ -397,6 +641,7 @@ __global__ void __launch_bounds__(W * 32, 1)
   // (into SF_s) and the log-sum-exp; then every output element is a short
   // weighted sum over the token groups, four elements per thread at a time.
   float* SF_s = ACC_s + C::WT * C::GP * C::D;                // [WT][GP]
+  float* SB_s = SF_s + C::WT * C::GP;                         // [GP]
   for (int h = threadIdx.x; h < G; h += C::THREADS) {
     float M = kNegInf;
 #pragma unroll
@@ -409,9 +654,13 @@ __global__ void __launch_bounds__(W * 32, 1)
       f[w] = (ms == kNegInf) ? 0.f : fast_exp2(ms - M);
       lt += f[w] * ML_s[(w * C::GP + h) * 2 + 1];
     }
-    const float inv = lt > 0.f ? 1.f / lt : 0.f;
+    // 8-bit caches: the kv head's V scale joins the normalisation; int8
+    // subtracts the code bias (times the V scale) from the normalised sum.
+    const float vsc = C::Q8 ? p.v_scale[g] : 1.f;
+    const float inv = lt > 0.f ? vsc / lt : 0.f;
 #pragma unroll
     for (int w = 0; w < C::WT; ++w) SF_s[w * C::GP + h] = f[w] * inv;
+    SB_s[h] = (KVQ == 1 && lt > 0.f) ? vsc * kI8Bias : 0.f;
     const int hq = g * G + h;
     if (p.lse != nullptr)
       p.lse[b * p.l_sb + hq * p.l_sh + split * p.l_ss] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
@@ -420,7 +669,8 @@ __global__ void __launch_bounds__(W * 32, 1)
   for (int idx = threadIdx.x; idx < G * (C::D / 4); idx += C::THREADS) {
     const int h = idx / (C::D / 4);
     const int d = (idx - h * (C::D / 4)) * 4;
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float bias = SB_s[h];
+    float4 o = make_float4(-bias, -bias, -bias, -bias);
 #pragma unroll
     for (int w = 0; w < C::WT; ++w) {
       const float sf = SF_s[w * C::GP + h];

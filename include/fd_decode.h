@@ -81,12 +81,15 @@ enum {
   FD_ERR_DEVICE_TIMEOUT = 10/* a bounded on-device wait gave up                    */
 };
 
-/* Element types. */
-enum { FD_F32 = 0, FD_BF16 = 1, FD_I32 = 2 };
+/* Element types.  FD_I8 is a signed 8-bit integer code, FD_E4M3 the 8-bit
+ * float with 1 sign, 4 exponent (bias 7) and 3 mantissa bits (no infinity;
+ * codes 0x7F / 0xFF are NaN; largest finite 448).  Both appear only as the
+ * cache of fd_decode_attention_quant. */
+enum { FD_F32 = 0, FD_BF16 = 1, FD_I32 = 2, FD_I8 = 3, FD_E4M3 = 4 };
 
 typedef struct fd_tensor {
   void* data;                    /* device pointer (host pointer only where stated) */
-  int32_t dtype;                 /* FD_F32, FD_BF16 or FD_I32                      */
+  int32_t dtype;                 /* FD_F32, FD_BF16, FD_I32, FD_I8 or FD_E4M3      */
   int32_t ndim;                  /* 1..4                                           */
   int64_t shape[FD_MAX_DIMS];    /* extents, outermost first                        */
   int64_t stride[FD_MAX_DIMS];   /* strides in elements, outermost first            */
@@ -117,6 +120,32 @@ FD_API fd_status fd_decode_attention(const fd_tensor* q, const fd_tensor* k_cach
                               const fd_tensor* v_cache, const fd_tensor* seqlens,
                               int32_t num_splits, float scale, fd_tensor* out,
                               fd_tensor* lse, fd_stream stream);
+
+/*
+ * fd_decode_attention_quant — split-KV decode attention over an 8-bit KV
+ * cache with one dequantisation scale per kv head (the bandwidth lever of
+ * quantisation: 8-bit codes instead of 16-bit floats halve the bytes that
+ * cross the memory bus; memory-bound decoding explainer, section on fighting
+ * the memory wall).
+ *   q        [B, Hq, D]            FD_BF16 or FD_F32
+ *   k_cache  [B, Lcap, Hkv, D]     FD_I8 or FD_E4M3 (same dtype as v_cache)
+ *   v_cache  [B, Lcap, Hkv, D]
+ *   k_scale  [Hkv] FD_F32 device tensor: K[b,j,g,:] = k_scale[g] * k_cache[b,j,g,:]
+ *   v_scale  [Hkv] FD_F32 device tensor: V[b,j,g,:] = v_scale[g] * v_cache[b,j,g,:]
+ *   seqlens, num_splits, scale, out, lse: as fd_decode_attention.
+ * The result is the definition above evaluated on the dequantised K and V
+ * (codes times scales, exact).  Non-finite scales, or NaN codes of an E4M3
+ * cache inside len_b, give non-finite outputs; codes past len_b are never
+ * used.  D must be 64 or 128 and Hq a multiple of Hkv; base pointers and the
+ * strides of the caches must be 16-byte aligned.  Queries are taken to f16
+ * inside the kernel after a per-head power-of-two rescale, so |q| up to
+ * 2^100 is represented without overflow.
+ */
+FD_API fd_status fd_decode_attention_quant(const fd_tensor* q, const fd_tensor* k_cache,
+                                           const fd_tensor* v_cache, const fd_tensor* k_scale,
+                                           const fd_tensor* v_scale, const fd_tensor* seqlens,
+                                           int32_t num_splits, float scale, fd_tensor* out,
+                                           fd_tensor* lse, fd_stream stream);
 
 /*
  * fd_decode_attention_paged — split-KV decode attention over a paged KV

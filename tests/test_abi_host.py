@@ -230,3 +230,34 @@ def test_paged_validation(L):
     import torch
     if not torch.cuda.is_available():
         assert call() == 8                                          # valid: no device here
+
+
+def test_quant_validation(L):
+    """fd_decode_attention_quant refuses bad descriptors on the host (the
+    pointers below are never dereferenced), and the plain entry point
+    refuses 8-bit caches."""
+    from decode_attention_20_b300._lib import FD_E4M3, FD_I8
+    r = lambda x: ctypes.byref(x) if x is not None else None
+    q = _t([2, 8, 128])
+    k = _t([2, 256, 2, 128], FD_I8)
+    ks = _t([2], FD_F32)
+    o = _t([2, 8, 128], FD_F32)
+    call = lambda q_=q, k_=k, v_=k, ks_=ks, vs_=ks, sl=None, ns=0, scale=0.1, o_=o: \
+        L.fd_decode_attention_quant(r(q_), r(k_), r(v_), r(ks_), r(vs_), r(sl), ns, scale, r(o_),
+                                    None, None)
+    assert call(k_=_t([2, 256, 2, 128])) == 3                          # bf16 cache
+    assert call(v_=_t([2, 256, 2, 128], FD_E4M3)) == 3                 # K / V kinds differ
+    assert call(ks_=None) == 1
+    assert call(vs_=_t([2], FD_BF16)) == 3                              # scale dtype
+    assert call(ks_=_t([3], FD_F32)) == 2                               # one scale per kv head
+    assert call(ks_=_t([2, 1], FD_F32)) == 2                            # scale rank
+    assert call(ns=-1) == 5
+    assert call(scale=math.inf) == 5
+    assert call(q_=_t([2, 8, 96])) == 2                                 # head dims differ
+    assert L.fd_last_error()
+    # the plain entry point takes bf16 / f32 caches only
+    assert _decode(L, q, k, k, None, 0, 0.1, o, None) == 3
+    import torch
+    if not torch.cuda.is_available():
+        assert call() == 8                                              # valid: no device here
+        assert call(k_=_t([2, 256, 2, 128], FD_E4M3), v_=_t([2, 256, 2, 128], FD_E4M3)) == 8
