@@ -120,6 +120,48 @@ class QuantCase:
         return [int(x) for x in self.seqlens.tolist()]
 
 
+@dataclass
+class MultiCase:
+    """Several new query positions per sequence (speculative verification):
+    q [B,Tq,Hq,D]; k/v cache [B,Lcap,Hkv,D] holding the history including the
+    Tq new tokens; seqlens [B] int32 (CPU) or None for "all Lcap"."""
+    name: str
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    seqlens: Optional[torch.Tensor]
+    scale: float
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def lens(self):
+        B, Lcap = self.k.shape[0], self.k.shape[1]
+        if self.seqlens is None:
+            return [Lcap] * B
+        return [int(x) for x in self.seqlens.tolist()]
+
+
+def multi_token_case(batch, tq, hq, hkv, d, lcap, dtype=torch.bfloat16, seed=0, seqlens=None,
+                     ragged=None, q_dtype=None, device="cpu", scale=None, name="multi"):
+    """Multi-token decode workload: like decode_case with Tq query positions
+    per sequence (q drawn first, [B, Tq, Hq, D])."""
+    q_dtype = dtype if q_dtype is None else q_dtype
+    g = _gen(seed, device)
+    q = _randn((batch, tq, hq, d), q_dtype, g, device)
+    k = _randn((batch, lcap, hkv, d), dtype, g, device)
+    v = _randn((batch, lcap, hkv, d), dtype, g, device)
+    extra = _gen(seed + 1, "cpu")
+    lens_t = None
+    if ragged is not None:
+        lo, hi = ragged
+        lens_t = torch.randint(lo, hi + 1, (batch,), generator=extra, dtype=torch.int64).to(torch.int32)
+    elif seqlens is not None:
+        lens_t = torch.tensor(list(seqlens), dtype=torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return MultiCase(name=name, q=q, k=k, v=v, seqlens=lens_t, scale=scale, meta={"seed": seed})
+
+
 def _int8_codes(shape, sigma, gen, device):
     """Integer codes drawn from a normal of standard deviation ``sigma``,
     rounded and clipped to [-127, 127] (a symmetric 8-bit code range), in
@@ -363,3 +405,10 @@ def quant_flash_decoding_b1(L=65536, kind="int8", seed=0, device="cpu"):
     head dim 128) over an 8-bit cache of L tokens."""
     return quant_case(1, 64, 8, 128, L, kind=kind, seed=seed, device=device,
                       name=f"b1_h64_kv8_d128_{kind}_L{L}")
+
+
+def speculative_b1(L=65536, tq=4, seed=0, device="cpu"):
+    """The batch-1 CodeLlama-34B-shaped layer (64 query heads, 8 kv heads,
+    head dim 128, bf16) verifying tq new tokens against an L-token cache."""
+    return multi_token_case(1, tq, 64, 8, 128, L, seed=seed, device=device,
+                            name=f"verify{tq}_b1_h64_kv8_d128_bf16_L{L}")

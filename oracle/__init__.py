@@ -47,13 +47,15 @@ from .attention import (  # noqa: F401
     bifurcated_attention_ref,
     paged_gather_ref,
     paged_decode_attention_ref,
+    causal_lengths_ref,
+    multi_token_decode_ref,
     required_bytes_ref,
     SPLIT_ALIGN,
     MAX_SPLITS,
     MIN_CHUNK,
     SPLIT_OVERHEAD_TOKENS,
 )
-from .bruteforce import attention_bruteforce, paged_attention_bruteforce  # noqa: F401
+from .bruteforce import attention_bruteforce, paged_attention_bruteforce, multi_token_bruteforce  # noqa: F401
 from .quant import (  # noqa: F401
     e4m3_to_f64,
     int8_to_f64,

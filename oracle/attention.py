@@ -292,6 +292,40 @@ def bifurcated_attention_ref(q, k_ctx, v_ctx, k_dec, v_dec, dec_lens, scale):
     return O, LSE
 
 
+def causal_lengths_ref(length: int, tq: int):
+    """Keys visible to each of the tq new query positions of a sequence whose
+    cached history (the new positions included, at its end) is ``length``
+    tokens long: query t sits at position length - tq + t and sees positions
+    0 .. length - tq + t, i.e. max(0, length - tq + t + 1) keys."""
+    return [max(0, int(length) - int(tq) + t + 1) for t in range(int(tq))]
+
+
+def multi_token_decode_ref(q, k, v, seqlens, scale):
+    """Decode attention with several new query positions per sequence
+    (speculative verification): q [B, Tq, Hq, D]; k, v [B, Lcap, Hkv, D];
+    seqlens [B] or None (= Lcap) counts the cached tokens including the Tq
+    new ones.  Query t of sequence b is decode_attention_ref over the first
+    causal_lengths_ref(len_b, Tq)[t] keys.  Returns (O [B, Tq, Hq, D],
+    LSE [B, Tq, Hq]).
+
+    The Flash-Decoding page contrasts prefill, which processes many query
+    positions at once, with usual decoding, one new position per sequence
+    (section "Why decoding needs different scheduling"); a verification step
+    sits in between, and each new position attends causally to the history
+    up to itself."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    B, Tq, Hq, D = q.shape
+    Lcap = k.shape[1]
+    lens = _lens(seqlens, B, Lcap)
+    O = np.zeros((B, Tq, Hq, D))
+    LSE = np.full((B, Tq, Hq), -np.inf)
+    for t in range(Tq):
+        lt = [causal_lengths_ref(n, Tq)[t] for n in lens]
+        O[:, t], LSE[:, t] = decode_attention_ref(q[:, t], k, v, lt, scale)
+    return O, LSE
+
+
 def paged_gather_ref(pages, block_table, page_size: int, length: int, b: int):
     """The first ``length`` cached tokens of sequence b from a paged cache.
 

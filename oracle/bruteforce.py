@@ -72,3 +72,33 @@ def paged_attention_bruteforce(q, k_pages, v_pages, block_table, seqlens, page_s
             for d in range(D):
                 O[b][h][d] = math.fsum(e[j] * vv[j][d] for j in range(n)) / z
     return O, LSE
+
+
+def multi_token_bruteforce(q, k, v, seqlens, scale):
+    """Multi-token decode by definition: q nested [B][Tq][Hq][D]; query t of
+    sequence b attends over the keys at positions j <= len_b - Tq + t (a
+    causal mask written out per key); k, v [B][Lcap][Hkv][D].  Returns
+    (O [B][Tq][Hq][D], LSE [B][Tq][Hq])."""
+    B = len(q)
+    Tq = len(q[0])
+    Lcap = len(k[0])
+    O, LSE = [], []
+    for b in range(B):
+        n = Lcap if seqlens is None else int(seqlens[b])
+        Ob, Lb = [], []
+        for t in range(Tq):
+            pos = n - Tq + t                       # this query's own position
+            keys = [j for j in range(n) if j <= pos]
+            kk = [[k[b][j] for j in keys]]
+            vv = [[v[b][j] for j in keys]]
+            o, l = attention_bruteforce([q[b][t]], kk, vv, [len(keys)], scale) if keys else (None, None)
+            if o is None:
+                Hq, D = len(q[b][t]), len(q[b][t][0])
+                Ob.append([[0.0] * D for _ in range(Hq)])
+                Lb.append([-math.inf] * Hq)
+            else:
+                Ob.append(o[0])
+                Lb.append(l[0])
+        O.append(Ob)
+        LSE.append(Lb)
+    return O, LSE

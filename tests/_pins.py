@@ -292,3 +292,50 @@ def quant_closed_forms_ok(quant_fn):
             if not (np.all(np.isfinite(Oa)) and _close(Oa, Ob) and _close(La, Lb)):
                 return False
     return True
+
+
+# ------------------------------------------------------- multi-token decode
+
+def golden_multi_ok(multi_fn):
+    """The hand-derived multi-token examples (tests/golden, "multi")."""
+    for case in load_golden()["multi"]:
+        O, L = multi_fn(_arr(case["q"]), _arr(case["k"]), _arr(case["v"]), case["seqlens"],
+                        case["scale"])
+        if not (_close(O, _arr(case["O"])) and _close(L, _arr(case["LSE"]))):
+            return False
+    return True
+
+
+def multi_bruteforce_ok(multi_fn, brute_fn, trials=8, seed=3):
+    """Vectorised multi-token oracle == the loop oracle with a per-key causal
+    mask, on tiny shapes with GQA groups and histories shorter than, equal
+    to and longer than the number of new positions."""
+    rng = np.random.default_rng(seed)
+    for _ in range(trials):
+        B, Tq, Hkv, G, D, L = 2, int(rng.integers(1, 5)), 2, int(rng.integers(1, 3)), 4, 6
+        q = rng.standard_normal((B, Tq, Hkv * G, D))
+        k = rng.standard_normal((B, L, Hkv, D))
+        v = rng.standard_normal((B, L, Hkv, D))
+        seqlens = [int(rng.integers(0, L + 1)), L]
+        O, LSE = multi_fn(q, k, v, seqlens, 0.7)
+        Ob, Lb = brute_fn(q.tolist(), k.tolist(), v.tolist(), seqlens, 0.7)
+        if not (_close(O, Ob, 1e-11) and _close(LSE, Lb, 1e-11)):
+            return False
+    return True
+
+
+def multi_last_query_is_plain_decode_ok(multi_fn, decode_fn, seed=4):
+    """The newest query position sees the whole history: its row equals
+    single-query decode; with one new position the two definitions agree."""
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((3, 4, 4, 8))
+    k = rng.standard_normal((3, 20, 2, 8))
+    v = rng.standard_normal((3, 20, 2, 8))
+    lens = [20, 7, 2]
+    O, L = multi_fn(q, k, v, lens, 0.3)
+    O1, L1 = decode_fn(q[:, -1], k, v, lens, 0.3)
+    if not (_close(O[:, -1], O1) and _close(L[:, -1], L1)):
+        return False
+    O2, L2 = multi_fn(q[:, :1], k, v, lens, 0.3)
+    O3, L3 = decode_fn(q[:, 0], k, v, lens, 0.3)
+    return _close(O2[:, 0], O3) and _close(L2[:, 0], L3)
