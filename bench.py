@@ -220,7 +220,10 @@ class DecodeWorkload(Workload):
         self.case = builder(device)
         c = self.case
         self.name = c.name
-        self.B, self.Hq, self.D = c.q.shape
+        if c.q.dim() == 4:                     # multi-token decode: q [B, Tq, Hq, D]
+            self.B, self.Tq, self.Hq, self.D = c.q.shape
+        else:
+            (self.B, self.Hq, self.D), self.Tq = c.q.shape, 1
         self.Lcap, self.Hkv = c.k.shape[1], c.k.shape[2]
         self.lens = c.lens
         self.seqlens_dev = c.seqlens.to(device) if c.seqlens is not None else None
@@ -228,8 +231,9 @@ class DecodeWorkload(Workload):
         self.nbuf = max(1, min(8, math.ceil(2 * L2_BYTES / kv_bytes) + (1 if kv_bytes < 4 * L2_BYTES else 0)))
         self.ks = [c.k] + [c.k.clone() for _ in range(self.nbuf - 1)]
         self.vs = [c.v] + [c.v.clone() for _ in range(self.nbuf - 1)]
-        self.out = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=device)
-        self.lse = torch.empty((self.B, self.Hq), dtype=torch.float32, device=device)
+        tok = (self.Tq,) if self.Tq > 1 else ()
+        self.out = torch.empty((self.B,) + tok + (self.Hq, self.D), dtype=torch.float32, device=device)
+        self.lse = torch.empty((self.B,) + tok + (self.Hq,), dtype=torch.float32, device=device)
         esz = c.k.element_size()
         tokens = sum(self.lens)
         self.kv_req = tokens * self.Hkv * self.D * esz * 2
@@ -275,26 +279,28 @@ class DecodeWorkload(Workload):
         c = self.case
         hq = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
         hq.copy_(c.q.cpu())
-        hk = torch.empty((self.B, self.Hkv, self.D), dtype=c.k.dtype).pin_memory()
+        # the Tq newest rows of every sequence (positions len_b - Tq .. len_b - 1)
+        pos = [(b, j) for b, n in enumerate(self.lens) for j in range(max(0, n - self.Tq), max(n, 1))]
+        nr = len(pos)
+        hk = torch.empty((nr, self.Hkv, self.D), dtype=c.k.dtype).pin_memory()
         hv = torch.empty_like(hk).pin_memory()
-        pos = [max(0, n - 1) for n in self.lens]
-        for b in range(self.B):
-            hk[b].copy_(c.k[b, pos[b]].cpu())
-            hv[b].copy_(c.v[b, pos[b]].cpu())
+        for i, (b, j) in enumerate(pos):
+            hk[i].copy_(c.k[b, j].cpu())
+            hv[i].copy_(c.v[b, j].cpu())
         hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
         hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
-        rows = torch.tensor([b * self.Lcap + pos[b] for b in range(self.B)], dtype=torch.int64,
+        rows = torch.tensor([b * self.Lcap + j for b, j in pos], dtype=torch.int64,
                             device=c.q.device)
-        dk = torch.empty((self.B, self.Hkv * self.D), dtype=c.k.dtype, device=c.q.device)
+        dk = torch.empty((nr, self.Hkv * self.D), dtype=c.k.dtype, device=c.q.device)
         dv = torch.empty_like(dk)
 
         def step(i):
             kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
             c.q.copy_(hq, non_blocking=True)
-            dk.copy_(hk.view(self.B, -1), non_blocking=True)
-            dv.copy_(hv.view(self.B, -1), non_blocking=True)
-            _rows(kb, self.B * self.Lcap).index_copy_(0, rows, _rows(dk, self.B))
-            _rows(vb, self.B * self.Lcap).index_copy_(0, rows, _rows(dv, self.B))
+            dk.copy_(hk.view(nr, -1), non_blocking=True)
+            dv.copy_(hv.view(nr, -1), non_blocking=True)
+            _rows(kb, self.B * self.Lcap).index_copy_(0, rows, _rows(dk, nr))
+            _rows(vb, self.B * self.Lcap).index_copy_(0, rows, _rows(dv, nr))
             self.api_call(c.q, kb, vb, stream)
             hout.copy_(self.out, non_blocking=True)
             hlse.copy_(self.lse, non_blocking=True)
@@ -573,6 +579,39 @@ class PagedWorkload(DecodeWorkload):
         return us, hq.numel() * 2 + hk.numel() * 2 * 2, hout.numel() * 4 + hlse.numel() * 4
 
 
+class MultiWorkload(DecodeWorkload):
+    """The batch-1 64K-token layer verifying Tq new tokens at once
+    (fd_decode_attention_multi)."""
+
+    def __init__(self, short, tq, device):
+        from decode_attention_20_b300 import inputs
+        super().__init__(short, lambda d: inputs.speculative_b1(65536, tq=tq, device=d), device)
+
+    def config(self, ns):
+        cfg = super().config(ns)
+        cfg["query_tokens"] = self.Tq
+        return cfg
+
+    def call(self, i):
+        r = ctypes.byref
+        st = self.L.fd_decode_attention_multi(r(self.dq), r(self.dks[i % self.nbuf]),
+                                              r(self.dvs[i % self.nbuf]),
+                                              r(self.ds) if self.ds is not None else None, self.ns,
+                                              ctypes.c_float(self.case.scale), r(self.do),
+                                              r(self.dl), self.sptr)
+        if st:
+            raise RuntimeError(self.L.fd_last_error().decode())
+
+    def api_call(self, q, k, v, stream):
+        import decode_attention_20_b300 as fd
+        fd.decode_attention_multi(q, k, v, self.seqlens_dev, self.ns, self.case.scale,
+                                  out=self.out, lse=self.lse, stream=stream)
+
+    def _oracle_call(self, q, k, v, T):
+        import oracle
+        oracle.multi_token_decode_ref(q, k[:, :T], v[:, :T], None, self.case.scale)
+
+
 class QuantWorkload(DecodeWorkload):
     """The batch-1 64K-token layer over an 8-bit cache (int8 or e4m3 codes,
     one scale per kv head): fd_decode_attention_quant."""
@@ -638,6 +677,8 @@ def make_workload(short, device):
         return BifWorkload(device)
     if short == "paged_b1_64k":
         return PagedWorkload(device)
+    if short == "verify4_b1_64k":
+        return MultiWorkload(short, 4, device)
     if short == "int8_b1_64k":
         return QuantWorkload(short, "int8", device)
     if short == "e4m3_b1_64k":
@@ -969,7 +1010,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="b1_64k",
                     choices=["b1_64k", "ragged_b32", "long_b4", "bif_mqa", "paged_b1_64k",
-                             "int8_b1_64k", "e4m3_b1_64k"])
+                             "int8_b1_64k", "e4m3_b1_64k", "verify4_b1_64k"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

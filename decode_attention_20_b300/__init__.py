@@ -14,6 +14,7 @@ from .api import (  # noqa: F401
     choose_num_splits,
     decode_attention,
     decode_attention_partials,
+    decode_attention_multi,
     decode_attention_paged,
     decode_attention_quant,
     lse_combine,

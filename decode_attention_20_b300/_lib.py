@@ -43,6 +43,7 @@ def _declare(lib):
         "fd_decode_attention": (st, [_T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_decode_attention_noalloc": (st, [_T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_decode_attention_paged": (st, [_T, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
+        "fd_decode_attention_multi": (st, [_T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_decode_attention_quant": (st, [_T, _T, _T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_decode_attention_partials": (st, [_T, _T, _T, _T, ctypes.c_int32, ctypes.c_float, _T, _T, ctypes.c_void_p]),
         "fd_lse_combine": (st, [_T, _T, _T, _T, ctypes.c_void_p]),

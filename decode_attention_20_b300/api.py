@@ -69,6 +69,26 @@ def decode_attention(q, k_cache, v_cache, seqlens=None, num_splits=0, scale=None
     return out, lse
 
 
+def decode_attention_multi(q, k_cache, v_cache, seqlens=None, num_splits=0, scale=None,
+                           out=None, lse=None, return_lse=True, stream=None):
+    """Multi-token decode attention (fd_decode_attention_multi): q [B, Tq,
+    Hq, D]; the cache holds the history including the Tq new tokens; query t
+    sees keys j < len_b - Tq + t + 1.  Returns (out [B, Tq, Hq, D] fp32,
+    lse [B, Tq, Hq] fp32 or None)."""
+    B, Tq, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((B, Tq, Hq, D), dtype=torch.float32, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Tq, Hq), dtype=torch.float32, device=q.device)
+    dq, dk, dv, ds = _desc(q, "q"), _desc(k_cache, "k_cache"), _desc(v_cache, "v_cache"), _desc(seqlens, "seqlens")
+    do, dl = _desc(out, "out"), _desc(lse, "lse")
+    check(lib().fd_decode_attention_multi(_ref(dq), _ref(dk), _ref(dv), _ref(ds), int(num_splits),
+                                          float(scale), _ref(do), _ref(dl), _stream(stream)))
+    return out, lse
+
+
 def decode_attention_quant(q, k_cache, v_cache, k_scale, v_scale, seqlens=None, num_splits=0,
                            scale=None, out=None, lse=None, return_lse=True, stream=None):
     """Split-KV decode attention over an 8-bit cache (fd_decode_attention_quant).

@@ -234,6 +234,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct DecodeDesc {
   int64_t B, Hq, Hkv, D, Lcap, G;
   int32_t q_dt, kv_dt;
+  int64_t tq = 1;                   // query positions per sequence (q is [B, tq, Hq, D] if > 1)
   const float* k_scale = nullptr;   // 8-bit caches: [Hkv] device
   const float* v_scale = nullptr;
 };
@@ -378,7 +379,8 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
                         const fd_tensor* v, const int32_t* seqlens, int ns, float scale,
                         float* o, int64_t o_sb, int64_t o_sh, int64_t o_ss, float* lse,
                         int64_t l_sb, int64_t l_sh, int64_t l_ss, bool kv_broadcast,
-                        cudaStream_t st, const PageDesc* pg = nullptr) {
+                        cudaStream_t st, const PageDesc* pg = nullptr, int64_t o_st = 0,
+                        int64_t l_st = 0) {
   SplitParams p = {};
   if (pg) {
     p.block_table = pg->table;
@@ -388,8 +390,12 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
     p.page_rows = pg->page_size < 64 ? pg->page_size : 64;
   }
   p.q = q->data;
+  p.tq = (int)d.tq;
   p.q_sb = q->stride[0];
-  p.q_sh = q->stride[1];
+  p.q_st = q->ndim == 4 ? q->stride[1] : 0;          // [B, tq, Hq, D] or [B, Hq, D]
+  p.q_sh = q->ndim == 4 ? q->stride[2] : q->stride[1];
+  p.o_st = o_st;
+  p.l_st = l_st;
   p.q_bf16 = d.q_dt == FD_BF16;
   p.k = k->data;
   p.v = v->data;
@@ -413,7 +419,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   p.o_sb = o_sb;
   p.o_sh = o_sh;
   p.o_ss = o_ss;
-  p.o_vec4 = aligned16(o) && o_sb % 4 == 0 && o_sh % 4 == 0 && o_ss % 4 == 0;
+  p.o_vec4 = aligned16(o) && o_sb % 4 == 0 && o_sh % 4 == 0 && o_ss % 4 == 0 && o_st % 4 == 0;
   p.lse = lse;
   p.l_sb = l_sb;
   p.l_sh = l_sh;
@@ -436,7 +442,9 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   // The tensor-core kernel takes bf16 queries over a bf16 cache, or bf16 /
   // f32 queries over an 8-bit cache (converted to f16 in the kernel).
   const int mtile = mma_tile_tokens(variant, p.kv_kind);
-  if (variant >= 0 && (d.q_dt == FD_BF16 || q8) && mma_group_ok(d.G) && d.Lcap >= mtile &&
+  // Multi-token decode puts tq * G rows on the n-tiles (up to 64).
+  const bool rows_ok = d.tq > 1 ? d.tq * d.G <= 64 : mma_group_ok(d.G);
+  if (variant >= 0 && (d.q_dt == FD_BF16 || q8) && rows_ok && d.Lcap >= mtile &&
       tma_ok(d, k->data, v->data, strides, kv_batch) &&
       (!pg || page_size_tma_ok(pg->page_size))) {
     fd_status gs = get_encoder();
@@ -460,7 +468,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
       if (e != cudaSuccess) return cuda_fail(e, "split kernel launch");
     }
   }
-  if (!launched && !pg && !q8 && tma_ok(d, k->data, v->data, strides, kv_batch)) {
+  if (!launched && !pg && !q8 && d.tq == 1 && tma_ok(d, k->data, v->data, strides, kv_batch)) {
     fd_status gs = get_encoder();
     if (gs) return gs;
     CUtensorMap tmK, tmV;
@@ -737,6 +745,118 @@ fd_status fd_decode_attention_quant(const fd_tensor* q, const fd_tensor* k_cache
   d.k_scale = reinterpret_cast<const float*>(k_scale->data);
   d.v_scale = reinterpret_cast<const float*>(v_scale->data);
   return run_decode(d, q, k_cache, v_cache, seqlens, num_splits, scale, out, lse, stream, nullptr);
+}
+
+fd_status fd_decode_attention_multi(const fd_tensor* q, const fd_tensor* k_cache,
+                                    const fd_tensor* v_cache, const fd_tensor* seqlens,
+                                    int32_t num_splits, float scale, fd_tensor* out,
+                                    fd_tensor* lse, fd_stream stream) {
+  fd_status st;
+  if ((st = check_tensor(q, "q", 4))) return st;
+  if ((st = check_tensor(k_cache, "k_cache", 4))) return st;
+  if ((st = check_tensor(v_cache, "v_cache", 4))) return st;
+  if ((st = check_tensor(out, "out", 4))) return st;
+  if (lse && (st = check_tensor(lse, "lse", 3))) return st;
+  if (seqlens && (st = check_tensor(seqlens, "seqlens", 1))) return st;
+  DecodeDesc d;
+  d.B = q->shape[0];
+  d.tq = q->shape[1];
+  d.Hq = q->shape[2];
+  d.D = q->shape[3];
+  d.Lcap = k_cache->shape[1];
+  d.Hkv = k_cache->shape[2];
+  for (int i = 0; i < 4; ++i)
+    if (k_cache->shape[i] != v_cache->shape[i])
+      return fail(FD_ERR_SHAPE, "k_cache and v_cache shapes differ");
+  if (k_cache->shape[0] != d.B) return fail(FD_ERR_SHAPE, "k_cache batch != q batch");
+  if (k_cache->shape[3] != d.D) return fail(FD_ERR_SHAPE, "k_cache head dim != q head dim");
+  if (d.tq < 1) return fail(FD_ERR_SHAPE, "q must hold at least one query token per sequence");
+  if (q->dtype != FD_BF16 && q->dtype != FD_F32) return fail(FD_ERR_DTYPE, "q must be bf16 or f32");
+  if (k_cache->dtype != v_cache->dtype) return fail(FD_ERR_DTYPE, "k_cache and v_cache dtypes differ");
+  if (k_cache->dtype != FD_BF16 && k_cache->dtype != FD_F32)
+    return fail(FD_ERR_DTYPE, "k_cache/v_cache must be bf16 or f32");
+  if (out->dtype != FD_F32 || (lse && lse->dtype != FD_F32))
+    return fail(FD_ERR_DTYPE, "out / lse must be f32");
+  for (int i = 0; i < 4; ++i)
+    if (out->shape[i] != q->shape[i]) return fail(FD_ERR_SHAPE, "out must be [B, Tq, Hq, D]");
+  if (lse && (lse->shape[0] != d.B || lse->shape[1] != d.tq || lse->shape[2] != d.Hq))
+    return fail(FD_ERR_SHAPE, "lse must be [B, Tq, Hq]");
+  if (seqlens) {
+    if (seqlens->dtype != FD_I32) return fail(FD_ERR_DTYPE, "seqlens must be int32");
+    if (seqlens->shape[0] != d.B) return fail(FD_ERR_SHAPE, "seqlens must have B entries");
+    if (seqlens->stride[0] != 1 && d.B > 1) return fail(FD_ERR_LAYOUT, "seqlens must be contiguous");
+  }
+  if (d.Hkv < 1 || d.Hq < 1 || d.Hq % d.Hkv != 0)
+    return fail(FD_ERR_UNSUPPORTED, "Hq must be a positive multiple of Hkv");
+  if (d.D != 64 && d.D != 128) return fail(FD_ERR_UNSUPPORTED, "head dim not in {64, 128}");
+  if (d.B > 65535 || d.tq * d.Hq > 65535)
+    return fail(FD_ERR_UNSUPPORTED, "batch and query tokens x heads must be <= 65535");
+  if (d.Lcap > (int64_t)INT32_MAX - 2 * kSplitAlign) return fail(FD_ERR_UNSUPPORTED, "cache length too large");
+  if (num_splits < 0 || num_splits > kMaxSplits)
+    return fail(FD_ERR_ARG, "num_splits %d outside [0, %d]", num_splits, kMaxSplits);
+  if (!std::isfinite(scale)) return fail(FD_ERR_ARG, "scale must be finite");
+  d.G = d.Hq / d.Hkv;
+  d.q_dt = q->dtype;
+  d.kv_dt = k_cache->dtype;
+
+  int dev;
+  DeviceInfo* info;
+  if ((st = current_device(&dev, &info))) return st;
+  if (d.B == 0) return FD_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const int ns = num_splits > 0 ? num_splits : choose_splits_host(d.B, d.Hkv, d.Lcap, info->sms);
+  const int32_t* sl = seqlens ? reinterpret_cast<const int32_t*>(seqlens->data) : nullptr;
+  float* o = reinterpret_cast<float*>(out->data);
+  float* l = lse ? reinterpret_cast<float*>(lse->data) : nullptr;
+  const int64_t l0 = lse ? lse->stride[0] : 0, l1 = lse ? lse->stride[1] : 0,
+                l2 = lse ? lse->stride[2] : 0;
+  if (ns == 1)
+    return enqueue_split(d, q, k_cache, v_cache, sl, 1, scale, o, out->stride[0], out->stride[2],
+                         0, l, l0, l2, 0, false, cs, nullptr, out->stride[1], l1);
+  // Partials [B, Tq, Hq, ns, D] and [B, Tq, Hq, ns], merged per (b, t, h).
+  const int64_t rows = d.B * d.tq;
+  const int64_t bytes = workspace_bytes(rows, d.Hq, d.D, ns);
+  void* ws = nullptr;
+  cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)bytes, info->pool, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace allocation");
+  float* po = reinterpret_cast<float*>(ws);
+  float* pl = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) +
+                                       ((rows * d.Hq * ns * d.D * 4 + 255) / 256) * 256);
+  const int64_t po_h = ns * d.D, po_t = d.Hq * po_h, po_b = d.tq * po_t;
+  const int64_t pl_h = ns, pl_t = d.Hq * pl_h, pl_b = d.tq * pl_t;
+  st = enqueue_split(d, q, k_cache, v_cache, sl, ns, scale, po, po_b, po_h, d.D, pl, pl_b, pl_h, 1,
+                     false, cs, nullptr, po_t, pl_t);
+  if (st == FD_OK) {
+    CombineParams cp = {};
+    cp.part_o = po;
+    cp.po_r1 = po_b;
+    cp.po_rm = po_t;
+    cp.po_r2 = po_h;
+    cp.po_s = d.D;
+    cp.part_lse = pl;
+    cp.pl_r1 = pl_b;
+    cp.pl_rm = pl_t;
+    cp.pl_r2 = pl_h;
+    cp.pl_s = 1;
+    cp.out = o;
+    cp.out_r1 = out->stride[0];
+    cp.out_rm = out->stride[1];
+    cp.out_r2 = out->stride[2];
+    cp.lse = l;
+    cp.lse_r1 = l0;
+    cp.lse_rm = l1;
+    cp.lse_r2 = l2;
+    cp.R1 = (int)d.B;
+    cp.Rm = (int)d.tq;
+    cp.R2 = (int)d.Hq;
+    cp.S = ns;
+    cp.D = (int)d.D;
+    st = enqueue_combine(cp, cs, true);
+  }
+  e = cudaFreeAsync(ws, cs);
+  if (st) return st;
+  if (e != cudaSuccess) return cuda_fail(e, "workspace release");
+  return FD_OK;
 }
 
 fd_status fd_decode_attention_paged(const fd_tensor* q, const fd_tensor* k_pages,

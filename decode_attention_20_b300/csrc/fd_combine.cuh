@@ -1,6 +1,7 @@
 // Log-sum-exp combine kernel.
 //
-// For every output row r (a (sequence, query head) pair) with S partial
+// For every output row r (a (sequence, query head) pair, or a (sequence,
+// query token, query head) triple for multi-token decode) with S partial
 // results (O_i, lse_i):
 //   LSE = ln sum_i e^(lse_i)   (evaluated as M + ln sum_i e^(lse_i - M))
 //   O   = sum_i e^(lse_i - LSE) * O_i
@@ -46,11 +47,14 @@ __global__ void __launch_bounds__(kCombineThreads)
   // with PDL) may start now: it waits for this grid before touching memory.
   pdl_launch_dependents();
   pdl_wait_prerequisites();
-  if (row >= p.R1 * p.R2) return;
-  const int r1 = row / p.R2;
-  const int r2 = row - r1 * p.R2;
-  const float* pl = p.part_lse + r1 * p.pl_r1 + r2 * p.pl_r2;
-  const float* po = p.part_o + r1 * p.po_r1 + r2 * p.po_r2;
+  const int Rm = p.Rm > 0 ? p.Rm : 1;
+  if (row >= p.R1 * Rm * p.R2) return;
+  const int r1 = row / (Rm * p.R2);
+  const int rr = row - r1 * (Rm * p.R2);
+  const int rm = rr / p.R2;
+  const int r2 = rr - rm * p.R2;
+  const float* pl = p.part_lse + r1 * p.pl_r1 + rm * p.pl_rm + r2 * p.pl_r2;
+  const float* po = p.part_o + r1 * p.po_r1 + rm * p.po_rm + r2 * p.po_r2;
 
   // ---- pass 1: M = max_i lse_i, tot = sum_i e^(lse_i - M)
   float M = kNegInfC;
@@ -108,14 +112,14 @@ __global__ void __launch_bounds__(kCombineThreads)
       o.z += a.z;
       o.w += a.w;
     }
-    float* out = p.out + r1 * p.out_r1 + r2 * p.out_r2 + tid * 4;
+    float* out = p.out + r1 * p.out_r1 + rm * p.out_rm + r2 * p.out_r2 + tid * 4;
     out[0] = o.x;
     out[1] = o.y;
     out[2] = o.z;
     out[3] = o.w;
   }
   if (tid == 0 && p.lse != nullptr)
-    p.lse[r1 * p.lse_r1 + r2 * p.lse_r2] = empty ? M : M + __logf(tot);
+    p.lse[r1 * p.lse_r1 + rm * p.lse_rm + r2 * p.lse_r2] = empty ? M : M + __logf(tot);
 }
 
 }  // namespace fd

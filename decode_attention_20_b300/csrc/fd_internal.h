@@ -25,8 +25,11 @@ constexpr int kKvI8 = 2;
 constexpr int kKvE4m3 = 3;
 
 struct SplitParams {
-  const void* q;              // [B, Hq, D]
+  const void* q;              // [B, Hq, D], or [B, tq, Hq, D] with tq > 1
   int64_t q_sb, q_sh;         // element strides
+  int64_t q_st;               // stride over the query tokens (tq > 1)
+  int tq;                     // new query positions per sequence (1: plain decode);
+                              // query t sees keys j < len - tq + t + 1
   int q_bf16;                 // 1: bf16, 0: fp32
   const void* k;              // [B, Lcap, Hkv, D] (generic kernel only; the TMA
   const void* v;              //  kernel reads through tensor maps)
@@ -37,6 +40,7 @@ struct SplitParams {
   float scale_log2;           // scale * log2(e): scores are kept in base 2
   float* o;                   // partial (or final, ns == 1) output, fp32
   int64_t o_sb, o_sh, o_ss;   // strides over (b, q head, split)
+  int64_t o_st, l_st;         // strides over the query tokens (tq > 1)
   int o_vec4;                 // 1: o and its strides allow 16-byte stores
   float* lse;                 // natural-log lse, or nullptr
   int64_t l_sb, l_sh, l_ss;
@@ -58,7 +62,7 @@ struct SplitParams {
 // Arguments of the log-sum-exp combine kernel.
 struct CombineParams {
   const float* part_o;        // rows x splits x D
-  int64_t po_r1, po_r2, po_s; // row index r = r1 * R2 + r2 (two row dims) ; split stride
+  int64_t po_r1, po_r2, po_s; // row index r = (r1 * Rm + rm) * R2 + r2 ; split stride
   const float* part_lse;
   int64_t pl_r1, pl_r2, pl_s;
   float* out;
@@ -66,6 +70,8 @@ struct CombineParams {
   float* lse;                 // may be nullptr
   int64_t lse_r1, lse_r2;
   int R1, R2, S, D;
+  int Rm;                     // middle row dimension (query tokens), 1 if none
+  int64_t po_rm, pl_rm, out_rm, lse_rm;
 };
 
 // Arguments of the bifurcated context kernel (one CTA per (128-row M-tile,

@@ -163,6 +163,10 @@ static cudaError_t launch_split_mma_kind(const SplitParams& p, const CUtensorMap
 
 cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              int G, int variant, cudaStream_t st, bool* launched, bool pdl) {
+  // The n-tiles hold the kv head's rows: its G query heads, times the query
+  // tokens for multi-token decode; round up to an instantiated row count.
+  const int rows = G * (p.tq > 1 ? p.tq : 1);
+  if (p.tq > 1) G = rows <= 8 ? 8 : rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 0;
   switch (p.kv_kind) {
     case kKvBf16: return launch_split_mma_kind<0>(p, tmK, tmV, G, variant, st, launched, pdl);
     case kKvI8: return launch_split_mma_kind<1>(p, tmK, tmV, G, variant, st, launched, pdl);
@@ -173,7 +177,7 @@ cudaError_t launch_split_mma(const SplitParams& p, const CUtensorMap& tmK, const
 
 template <int D>
 static cudaError_t launch_generic_d(const SplitParams& p, cudaStream_t st, bool pdl) {
-  const dim3 grid(p.ns, p.Hq, p.B);
+  const dim3 grid(p.ns, p.Hq * (p.tq > 1 ? p.tq : 1), p.B);
   switch (p.kv_kind) {
     case kKvF32: return launch_ex(split_generic_kernel<D, kKvF32>, grid, dim3(128), 0, st, pdl, p);
     case kKvBf16: return launch_ex(split_generic_kernel<D, kKvBf16>, grid, dim3(128), 0, st, pdl, p);
@@ -190,7 +194,8 @@ cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, b
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
-  return launch_ex(lse_combine_kernel, dim3(p.R1 * p.R2), dim3(kCombineThreads), 0, st, pdl, p);
+  return launch_ex(lse_combine_kernel, dim3(p.R1 * (p.Rm > 0 ? p.Rm : 1) * p.R2),
+                   dim3(kCombineThreads), 0, st, pdl, p);
 }
 
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,

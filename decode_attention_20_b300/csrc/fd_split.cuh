@@ -449,7 +449,9 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
   __shared__ float ml_s[NW][2];
   __shared__ float acc_s[NW][D];
   const int split = blockIdx.x;
-  const int h = blockIdx.y;
+  const int TQ = p.tq > 1 ? p.tq : 1;
+  const int tqi = blockIdx.y / p.Hq;          // query token (grid.y = tq * Hq)
+  const int h = blockIdx.y - tqi * p.Hq;
   const int b = blockIdx.z;
   const int g = h / p.G;
   const int warp = threadIdx.x >> 5;
@@ -457,6 +459,7 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
   const int len = resolve_len(p.seqlens, b, p.Lcap);
   int begin, end;
   split_range(len, p.ns, split, begin, end);
+  end = min(end, max(begin, len - TQ + tqi + 1));   // causal limit of query token tqi
 
   // 8-bit caches: the K scale joins the score scale, the V scale multiplies
   // the normalised output.
@@ -469,9 +472,9 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
     const int d = lane * EPL + e;
     float x;
     if (p.q_bf16)
-      x = __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.q)[b * p.q_sb + h * p.q_sh + d]) << 16);
+      x = __uint_as_float(uint32_t(reinterpret_cast<const uint16_t*>(p.q)[b * p.q_sb + tqi * p.q_st + h * p.q_sh + d]) << 16);
     else
-      x = reinterpret_cast<const float*>(p.q)[b * p.q_sb + h * p.q_sh + d];
+      x = reinterpret_cast<const float*>(p.q)[b * p.q_sb + tqi * p.q_st + h * p.q_sh + d];
     q[e] = x * qs;
   }
   float acc[EPL];
@@ -531,9 +534,10 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
         o += f * acc_s[w][d];
       }
     }
-    p.o[b * p.o_sb + h * p.o_sh + split * p.o_ss + d] = lt > 0.f ? vs * (o / lt) : 0.f;
+    p.o[b * p.o_sb + tqi * p.o_st + h * p.o_sh + split * p.o_ss + d] = lt > 0.f ? vs * (o / lt) : 0.f;
     if (d == 0 && p.lse != nullptr)
-      p.lse[b * p.l_sb + h * p.l_sh + split * p.l_ss] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
+      p.lse[b * p.l_sb + tqi * p.l_st + h * p.l_sh + split * p.l_ss] =
+          lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
   }
 }
 

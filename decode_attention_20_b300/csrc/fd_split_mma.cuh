@@ -280,13 +280,18 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   // ---- raw query loads (fp32 bit patterns), turned into MMA fragments below.
   // (Issuing them ahead of the ring's first copies was measured: it delays
   // the copies and gains nothing.)
+  // Rows of the kv head: (query token t, head in group hl), row = t * G + hl
+  // (plain decode: tq = 1, rows = heads).
   const int G = p.G;
+  const int TQ = p.tq > 1 ? p.tq : 1;
+  const int R = TQ * G;
   uint32_t qraw[NPW][8][4];
 #pragma unroll
   for (int j = 0; j < NPW; ++j) {
-    const int hl = (wn * NPW + j) * 8 + (lane >> 2);          // head within the group
-    const bool real = hl < G;
-    const int h = g * G + (real ? hl : 0);
+    const int r = (wn * NPW + j) * 8 + (lane >> 2);           // row of this lane's query
+    const bool real = r < R;
+    const int tqi = real ? r / G : 0;
+    const int h = g * G + (real ? r - tqi * G : 0);
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       // bf16 cache: dims ks*16 + 2(lane%4) + {0, 1, 8, 9}; 8-bit cache: dims
@@ -298,7 +303,7 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
         const int d = C::Q8 ? d0 + i : d0 + (i & 1) + (i >> 1) * 8;
         uint32_t x = 0u;
         if (real) {
-          const int64_t o = b * p.q_sb + h * p.q_sh + d;
+          const int64_t o = b * p.q_sb + tqi * p.q_st + h * p.q_sh + d;
           x = p.q_bf16 ? uint32_t(reinterpret_cast<const uint16_t*>(p.q)[o]) << 16
                        : __float_as_uint(reinterpret_cast<const float*>(p.q)[o]);
         }
@@ -389,6 +394,16 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   }
   const float sl2 = p.scale_log2;
   const int r8 = lane & 7;
+  // Causal limit of this lane's two score columns (rows hA, hB of each
+  // n-tile): query token t sees tokens j < len - tq + t + 1.  For tq = 1 the
+  // limit is len, which the split range already enforces.
+  int limA[NPW], limB[NPW];
+#pragma unroll
+  for (int j = 0; j < NPW; ++j) {
+    const int rA = (wn * NPW + j) * 8 + 2 * (lane & 3);
+    limA[j] = len - TQ + min(rA, R - 1) / G + 1;
+    limB[j] = len - TQ + min(rA + 1, R - 1) / G + 1;
+  }
 
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % C::NSTAGE;
@@ -442,6 +457,7 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
       const int tokA = row0 + (lane >> 2);
       const bool vA = tokA < nvalid;
       const bool vB = tokA + 8 < nvalid;
+      const int absA = begin + t * C::T + tokA;                  // absolute token index
       uint32_t pb[NPW][2], pbl[NPW][2];
       bool moved = false;
       float alpha[NPW][2];
@@ -451,10 +467,10 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
         const float f1 = C::Q8 ? sl2h[j][1] : sl2;
         // (int8: one fused multiply-add also removes the code bias's share
         // of the score, exactly rounded once.)
-        float sA0 = vA ? fmaf(sacc[j][0], f0, -shift[j][0]) : kNegInf;   // (tA, hA)
-        float sA1 = vA ? fmaf(sacc[j][1], f1, -shift[j][1]) : kNegInf;   // (tA, hB)
-        float sB0 = vB ? fmaf(sacc[j][2], f0, -shift[j][0]) : kNegInf;   // (tB, hA)
-        float sB1 = vB ? fmaf(sacc[j][3], f1, -shift[j][1]) : kNegInf;   // (tB, hB)
+        float sA0 = (vA && absA < limA[j]) ? fmaf(sacc[j][0], f0, -shift[j][0]) : kNegInf;      // (tA, hA)
+        float sA1 = (vA && absA < limB[j]) ? fmaf(sacc[j][1], f1, -shift[j][1]) : kNegInf;      // (tA, hB)
+        float sB0 = (vB && absA + 8 < limA[j]) ? fmaf(sacc[j][2], f0, -shift[j][0]) : kNegInf;  // (tB, hA)
+        float sB1 = (vB && absA + 8 < limB[j]) ? fmaf(sacc[j][3], f1, -shift[j][1]) : kNegInf;  // (tB, hB)
         float mx0 = fmaxf(sA0, sB0), mx1 = fmaxf(sA1, sB1);
 #pragma unroll
         for (int o = 4; o <= 16; o <<= 1) {
@@ -642,7 +658,7 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   // weighted sum over the token groups, four elements per thread at a time.
   float* SF_s = ACC_s + C::WT * C::GP * C::D;                // [WT][GP]
   float* SB_s = SF_s + C::WT * C::GP;                         // [GP]
-  for (int h = threadIdx.x; h < G; h += C::THREADS) {
+  for (int h = threadIdx.x; h < R; h += C::THREADS) {         // h: row (t * G + head)
     float M = kNegInf;
 #pragma unroll
     for (int w = 0; w < C::WT; ++w) M = fmaxf(M, ML_s[(w * C::GP + h) * 2]);
@@ -661,12 +677,14 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
 #pragma unroll
     for (int w = 0; w < C::WT; ++w) SF_s[w * C::GP + h] = f[w] * inv;
     SB_s[h] = (KVQ == 1 && lt > 0.f) ? vsc * kI8Bias : 0.f;
-    const int hq = g * G + h;
+    const int tqi = h / G;
+    const int hq = g * G + (h - tqi * G);
     if (p.lse != nullptr)
-      p.lse[b * p.l_sb + hq * p.l_sh + split * p.l_ss] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
+      p.lse[b * p.l_sb + tqi * p.l_st + hq * p.l_sh + split * p.l_ss] =
+          lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * (C::D / 4); idx += C::THREADS) {
+  for (int idx = threadIdx.x; idx < R * (C::D / 4); idx += C::THREADS) {
     const int h = idx / (C::D / 4);
     const int d = (idx - h * (C::D / 4)) * 4;
     const float bias = SB_s[h];
@@ -680,8 +698,9 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
       o.z = fmaf(sf, a.z, o.z);
       o.w = fmaf(sf, a.w, o.w);
     }
-    const int hq = g * G + h;
-    float* dst = p.o + b * p.o_sb + hq * p.o_sh + split * p.o_ss + d;
+    const int tqi = h / G;
+    const int hq = g * G + (h - tqi * G);
+    float* dst = p.o + b * p.o_sb + tqi * p.o_st + hq * p.o_sh + split * p.o_ss + d;
     if (p.o_vec4) {
       *reinterpret_cast<float4*>(dst) = o;
     } else {

@@ -148,6 +148,32 @@ FD_API fd_status fd_decode_attention_quant(const fd_tensor* q, const fd_tensor* 
                                            fd_tensor* lse, fd_stream stream);
 
 /*
+ * fd_decode_attention_multi — split-KV decode attention with several new
+ * query positions per sequence (the verification step of speculative
+ * decoding: between prefill, which processes many query positions at once,
+ * and usual decoding, one new position per sequence; Flash-Decoding page,
+ * section "Why decoding needs different scheduling").
+ *   q        [B, Tq, Hq, D]        FD_BF16 or FD_F32; Tq >= 1 new positions
+ *   k_cache  [B, Lcap, Hkv, D]     FD_BF16 or FD_F32 (same dtype as v_cache),
+ *   v_cache  [B, Lcap, Hkv, D]     holding the history INCLUDING the Tq new
+ *                                  tokens at its end
+ *   seqlens  [B] FD_I32 or NULL: len_b cached tokens, new ones included.
+ *            Query t of sequence b sits at position len_b - Tq + t and sees
+ *            the keys j < len_b - Tq + t + 1 (causal among the new tokens);
+ *            a query with no visible key gets O = 0, LSE = -inf.
+ *   out      [B, Tq, Hq, D] FD_F32; lse [B, Tq, Hq] FD_F32 or NULL.
+ *   num_splits, scale: as fd_decode_attention.
+ * Tq = 1 is fd_decode_attention with q viewed as [B, 1, Hq, D].
+ * Tq * Hq <= 65535.  The tensor-core kernel takes Tq * G <= 64 rows per kv
+ * head (bf16 queries and cache, head dim 128); other shapes use the
+ * CUDA-core kernel.
+ */
+FD_API fd_status fd_decode_attention_multi(const fd_tensor* q, const fd_tensor* k_cache,
+                                           const fd_tensor* v_cache, const fd_tensor* seqlens,
+                                           int32_t num_splits, float scale, fd_tensor* out,
+                                           fd_tensor* lse, fd_stream stream);
+
+/*
  * fd_decode_attention_paged — split-KV decode attention over a paged KV
  * cache: fixed-size pages of tokens, each sequence's pages listed in a block
  * table (the indirection-table storage named among the memory-wall

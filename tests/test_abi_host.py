@@ -261,3 +261,26 @@ def test_quant_validation(L):
     if not torch.cuda.is_available():
         assert call() == 8                                              # valid: no device here
         assert call(k_=_t([2, 256, 2, 128], FD_E4M3), v_=_t([2, 256, 2, 128], FD_E4M3)) == 8
+
+
+def test_multi_validation(L):
+    """fd_decode_attention_multi refuses bad descriptors on the host."""
+    r = lambda x: ctypes.byref(x) if x is not None else None
+    q = _t([2, 3, 8, 128])
+    k = _t([2, 256, 2, 128])
+    o = _t([2, 3, 8, 128], FD_F32)
+    call = lambda q_=q, k_=k, v_=k, sl=None, ns=0, scale=0.1, o_=o, l_=None: \
+        L.fd_decode_attention_multi(r(q_), r(k_), r(v_), r(sl), ns, scale, r(o_), r(l_), None)
+    assert call(q_=_t([2, 8, 128])) == 2                            # q rank
+    assert call(o_=_t([2, 2, 8, 128], FD_F32)) == 2                 # out tokens
+    assert call(l_=_t([2, 8], FD_F32)) == 2                         # lse rank
+    assert call(l_=_t([2, 2, 8], FD_F32)) == 2                      # lse tokens
+    assert call(k_=_t([2, 256, 3, 128]), v_=_t([2, 256, 3, 128])) == 6
+    assert call(q_=_t([2, 0, 8, 128]), o_=_t([2, 0, 8, 128], FD_F32)) == 2
+    assert call(q_=_t([2, 9000, 8, 128]), o_=_t([2, 9000, 8, 128], FD_F32)) == 6
+    assert call(o_=_t([2, 3, 8, 128])) == 3                          # out dtype
+    assert call(ns=257) == 5
+    import torch
+    if not torch.cuda.is_available():
+        assert call() == 8
+        assert call(l_=_t([2, 3, 8], FD_F32)) == 8
