@@ -34,6 +34,9 @@ namespace fd {
 constexpr int kCombineThreads = 128;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// MULTI: rows carry a middle (query token) index; compiled separately so
+// the single-token path keeps its shorter index arithmetic.
+template <bool MULTI>
 __global__ void __launch_bounds__(kCombineThreads)
     lse_combine_kernel(const __grid_constant__ CombineParams p) {
   constexpr float kNegInfC = -__builtin_huge_valf();
@@ -47,14 +50,20 @@ __global__ void __launch_bounds__(kCombineThreads)
   // with PDL) may start now: it waits for this grid before touching memory.
   pdl_launch_dependents();
   pdl_wait_prerequisites();
-  const int Rm = p.Rm > 0 ? p.Rm : 1;
-  if (row >= p.R1 * Rm * p.R2) return;
-  const int r1 = row / (Rm * p.R2);
-  const int rr = row - r1 * (Rm * p.R2);
-  const int rm = rr / p.R2;
-  const int r2 = rr - rm * p.R2;
-  const float* pl = p.part_lse + r1 * p.pl_r1 + rm * p.pl_rm + r2 * p.pl_r2;
-  const float* po = p.part_o + r1 * p.po_r1 + rm * p.po_rm + r2 * p.po_r2;
+  int r1, rm = 0, r2;
+  if constexpr (MULTI) {                 // (sequence, query token, head) rows
+    if (row >= p.R1 * p.Rm * p.R2) return;
+    r1 = row / (p.Rm * p.R2);
+    const int rr = row - r1 * (p.Rm * p.R2);
+    rm = rr / p.R2;
+    r2 = rr - rm * p.R2;
+  } else {
+    if (row >= p.R1 * p.R2) return;
+    r1 = row / p.R2;
+    r2 = row - r1 * p.R2;
+  }
+  const float* pl = p.part_lse + r1 * p.pl_r1 + r2 * p.pl_r2 + (MULTI ? rm * p.pl_rm : 0);
+  const float* po = p.part_o + r1 * p.po_r1 + r2 * p.po_r2 + (MULTI ? rm * p.po_rm : 0);
 
   // ---- pass 1: M = max_i lse_i, tot = sum_i e^(lse_i - M)
   float M = kNegInfC;
@@ -112,14 +121,14 @@ __global__ void __launch_bounds__(kCombineThreads)
       o.z += a.z;
       o.w += a.w;
     }
-    float* out = p.out + r1 * p.out_r1 + rm * p.out_rm + r2 * p.out_r2 + tid * 4;
+    float* out = p.out + r1 * p.out_r1 + r2 * p.out_r2 + (MULTI ? rm * p.out_rm : 0) + tid * 4;
     out[0] = o.x;
     out[1] = o.y;
     out[2] = o.z;
     out[3] = o.w;
   }
   if (tid == 0 && p.lse != nullptr)
-    p.lse[r1 * p.lse_r1 + rm * p.lse_rm + r2 * p.lse_r2] = empty ? M : M + __logf(tot);
+    p.lse[r1 * p.lse_r1 + r2 * p.lse_r2 + (MULTI ? rm * p.lse_rm : 0)] = empty ? M : M + __logf(tot);
 }
 
 }  // namespace fd

@@ -194,8 +194,11 @@ cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, b
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
-  return launch_ex(lse_combine_kernel, dim3(p.R1 * (p.Rm > 0 ? p.Rm : 1) * p.R2),
-                   dim3(kCombineThreads), 0, st, pdl, p);
+  if (p.Rm > 1)
+    return launch_ex(lse_combine_kernel<true>, dim3(p.R1 * p.Rm * p.R2), dim3(kCombineThreads), 0,
+                     st, pdl, p);
+  return launch_ex(lse_combine_kernel<false>, dim3(p.R1 * p.R2), dim3(kCombineThreads), 0, st,
+                   pdl, p);
 }
 
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
