@@ -380,8 +380,9 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
                         float* o, int64_t o_sb, int64_t o_sh, int64_t o_ss, float* lse,
                         int64_t l_sb, int64_t l_sh, int64_t l_ss, bool kv_broadcast,
                         cudaStream_t st, const PageDesc* pg = nullptr, int64_t o_st = 0,
-                        int64_t l_st = 0) {
+                        int64_t l_st = 0, bool late_wait = false) {
   SplitParams p = {};
+  p.late_wait = late_wait ? 1 : 0;
   if (pg) {
     p.block_table = pg->table;
     p.bt_stride = pg->stride;
@@ -396,6 +397,8 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   p.q_sh = q->ndim == 4 ? q->stride[2] : q->stride[1];
   p.o_st = o_st;
   p.l_st = l_st;
+  p.q_vec16 = d.q_dt == FD_BF16 && aligned16(q->data) && p.q_sb % 8 == 0 && p.q_sh % 8 == 0 &&
+              p.q_st % 8 == 0;
   p.q_bf16 = d.q_dt == FD_BF16;
   p.k = k->data;
   p.v = v->data;
@@ -1124,6 +1127,10 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   int ns_dec = 0;
   if (Ld > 0) {
     int64_t want = (2 * (int64_t)info->sms) / (n * Hkv);
+    // Tuning knob, read on every call: FD_BIF_DEC_SPLITS fixes the count.
+    if (const char* e = getenv("FD_BIF_DEC_SPLITS")) {
+      if (atoi(e) > 0) want = atoi(e);
+    }
     const int64_t cap = (Ld + 63) / 64;
     if (want > cap) want = cap;
     if (want > kMaxSplits) want = kMaxSplits;
@@ -1213,7 +1220,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
                        dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr,
                        ns_dec, scale, po + (int64_t)(ns_ctx / csize) * n * Hq * D, Hq * D, D,
                        n * Hq * D, pl + (int64_t)(ns_ctx / csize) * n * Hq, Hq, 1, n * Hq, false,
-                       cs);
+                       cs, nullptr, 0, 0, /*late_wait=*/ctx_done && csize == 1);
   }
   if (st == FD_OK) {
     CombineParams cp = {};

@@ -107,6 +107,9 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
                    const __grid_constant__ CUtensorMap tmV) {
   using C = BifCfg;
   pdl_wait_prerequisites();   // launched with PDL: no memory access before this
+  // Every earlier grid has now finished: the decode part (which reads none of
+  // this kernel's output) may start on the SMs this grid leaves free.
+  pdl_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));

@@ -45,6 +45,15 @@ struct SplitParams {
   float* lse;                 // natural-log lse, or nullptr
   int64_t l_sb, l_sh, l_ss;
   int kv_batch_broadcast;     // 1: every sequence reads kv batch row 0
+  // 1: do not wait for the preceding grid before reading the inputs, only
+  // before exiting.  Set only when the preceding kernel is one of this
+  // library's, which triggers its dependents after its own launch wait (so
+  // every earlier grid has finished) and writes nothing this kernel reads:
+  // the split kernel then overlaps it, and still completes after it.
+  int late_wait;
+  // 1: q rows are 16-byte aligned (base and strides), so the tensor-core
+  // kernel stages its query block through shared memory with vector loads.
+  int q_vec16;
   // Element type of the cache (kKvF32, kKvBf16, kKvI8, kKvE4m3); the 8-bit
   // kinds carry one dequantisation scale per kv head for K and for V.
   int kv_kind;

@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
   using C = TmaCfg<GH, HC>;
-  pdl_wait_prerequisites();   // launched with PDL: no memory access before this
+  if (!p.late_wait) pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -422,6 +422,7 @@ __global__ void __launch_bounds__(TmaCfg<GH, HC>::THREADS, 1)
     if (d == 0 && p.lse != nullptr)
       p.lse[b * p.l_sb + hq * p.l_sh + split * p.l_ss] = lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
   }
+  if (p.late_wait) pdl_wait_prerequisites();   // complete only after the preceding grid
 }
 
 // ------------------------------------------------------------------ generic
@@ -443,7 +444,7 @@ __device__ __forceinline__ float kv_elem(const void* base, int64_t i) {
 
 template <int D, int KVK>
 __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constant__ SplitParams p) {
-  pdl_wait_prerequisites();   // launched with PDL: no memory access before this
+  if (!p.late_wait) pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   constexpr int NW = 4;
   constexpr int EPL = D / 32;
   __shared__ float ml_s[NW][2];
@@ -539,6 +540,7 @@ __global__ void __launch_bounds__(128) split_generic_kernel(const __grid_constan
       p.lse[b * p.l_sb + tqi * p.l_st + h * p.l_sh + split * p.l_ss] =
           lt > 0.f ? (M + __log2f(lt)) * kLn2 : kNegInf;
   }
+  if (p.late_wait) pdl_wait_prerequisites();   // complete only after the preceding grid
 }
 
 }  // namespace fd

@@ -180,10 +180,17 @@ struct MmaCfg {
   static constexpr int STAGE_BYTES = (Q8 ? 2 : 4) * HALF_BYTES;
   static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
   static constexpr int GP = NT * 8;            // padded heads
-  static constexpr int SMEM_BYTES = 1024 + RING_BYTES + 2 * NSTAGE * 8 + 16;
+  // Query staging (bf16 queries, up to 32 rows): rows of D bf16 padded by 16
+  // bytes so that the fragment reads of 8 rows hit distinct banks.
+  static constexpr bool STAGE_Q = GP <= 32;
+  static constexpr int QROW_BYTES = D * 2 + 16;
+  static constexpr int OFF_Q = ((RING_BYTES + 2 * NSTAGE * 8 + 16) + 127) / 128 * 128;
+  static constexpr int Q_BYTES = STAGE_Q ? GP * QROW_BYTES : 0;
+  static constexpr int SMEM_BYTES = 1024 + OFF_Q + Q_BYTES;
   static_assert(NT % WN == 0, "n-tiles split evenly over warps");
   static_assert(W % WN == 0 && BLK % WT == 0 && BPW >= 1, "blocks split evenly over warps");
   static_assert(WT * GP * (D + 3) * 4 + GP * 4 <= RING_BYTES, "epilogue fits the ring");
+  static_assert(Q_BYTES == 0 || OFF_Q % 16 == 0, "staged query rows are 16-byte aligned");
   static_assert(HALF_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
 };
 
@@ -193,7 +200,7 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
   using C = MmaCfg<KVQ, NT, WN, W, T, NSTAGE>;
-  pdl_wait_prerequisites();   // launched with PDL: no memory access before this
+  if (!p.late_wait) pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   constexpr int NPW = C::NPW;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -223,6 +230,36 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     }
     *abort_s = 0;
     fence_barrier_init();
+  }
+
+  // Rows of the kv head: (query token t, head in group hl), row = t * G + hl
+  // (plain decode: tq = 1, rows = heads).
+  const int G = p.G;
+  const int TQ = p.tq > 1 ? p.tq : 1;
+  const int R = TQ * G;
+  // ---- bf16 query block: one coalesced 16-byte load per chunk per thread,
+  // issued before the ring's first copies (scalar fragment loads issued
+  // after them queued behind every CTA's ring fill for several
+  // microseconds while the full ring waited); stored to shared memory
+  // after the copies are issued.
+  constexpr int QCH = C::GP * (C::D / 8);                    // 16-byte chunks
+  constexpr int QPT = C::STAGE_Q ? (QCH + C::THREADS - 1) / C::THREADS : 1;
+  const bool stage_q = C::STAGE_Q && p.q_bf16 && p.q_vec16;
+  uint4 qv16[QPT];
+  if (stage_q) {
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int c = threadIdx.x + k * C::THREADS;
+      const int r = c / (C::D / 8);
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (c < QCH && r < R) {
+        const int tqi = r / G;
+        const int64_t o = b * p.q_sb + tqi * p.q_st + (g * G + r - tqi * G) * p.q_sh +
+                          (c - r * (C::D / 8)) * 8;
+        x = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + o);
+      }
+      qv16[k] = x;
+    }
   }
 
   __syncthreads();
@@ -277,15 +314,38 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     }
   }
 
-  // ---- raw query loads (fp32 bit patterns), turned into MMA fragments below.
-  // (Issuing them ahead of the ring's first copies was measured: it delays
-  // the copies and gains nothing.)
-  // Rows of the kv head: (query token t, head in group hl), row = t * G + hl
-  // (plain decode: tq = 1, rows = heads).
-  const int G = p.G;
-  const int TQ = p.tq > 1 ? p.tq : 1;
-  const int R = TQ * G;
+  // ---- raw query values (fp32 bit patterns), turned into MMA fragments below.
   uint32_t qraw[NPW][8][4];
+  unsigned char* q_s = smem + C::OFF_Q;
+  if (stage_q) {
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) {
+      const int c = threadIdx.x + k * C::THREADS;
+      if (c < QCH) {
+        const int r = c / (C::D / 8);
+        *reinterpret_cast<uint4*>(q_s + r * C::QROW_BYTES + (c - r * (C::D / 8)) * 16) = qv16[k];
+      }
+    }
+    __syncthreads();
+    // Word pairs: bf16 cache dims (d0, d0+1) and (d0+8, d0+9); 8-bit cache
+    // dims (d0, d0+1) and (d0+2, d0+3) (the fragment orders below).
+#pragma unroll
+    for (int j = 0; j < NPW; ++j) {
+      const int r = (wn * NPW + j) * 8 + (lane >> 2);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int d0 = C::Q8 ? 16 * (2 * (lane & 3) + (ks >> 2)) + 4 * (ks & 3)
+                             : ks * 16 + 2 * (lane & 3);
+        const uint32_t* rowp = reinterpret_cast<const uint32_t*>(q_s + r * C::QROW_BYTES);
+        const uint32_t w0 = rowp[d0 >> 1];
+        const uint32_t w1 = rowp[(d0 + (C::Q8 ? 2 : 8)) >> 1];
+        qraw[j][ks][0] = w0 << 16;
+        qraw[j][ks][1] = w0 & 0xffff0000u;
+        qraw[j][ks][2] = w1 << 16;
+        qraw[j][ks][3] = w1 & 0xffff0000u;
+      }
+    }
+  }
   // One uniform branch on the query type outside the unrolled loads (a
   // per-element select here measured 2-4 us slower per launch).
   auto load_q = [&](auto as_bits) {
@@ -310,10 +370,12 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
       }
     }
   };
-  if (C::Q8 && !p.q_bf16)
+  if (stage_q) {
+  } else if (C::Q8 && !p.q_bf16) {
     load_q([&](int64_t o) { return __float_as_uint(reinterpret_cast<const float*>(p.q)[o]); });
-  else
+  } else {
     load_q([&](int64_t o) { return uint32_t(reinterpret_cast<const uint16_t*>(p.q)[o]) << 16; });
+  }
   const float ks_g = C::Q8 ? p.k_scale[g] : 1.f;
 
   // ---- query fragments (B operand of S^T = K . Q^T): B[k = dim][n = head]
@@ -713,6 +775,7 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
       dst[3] = o.w;
     }
   }
+  if (p.late_wait) pdl_wait_prerequisites();   // complete only after the preceding grid
 }
 
 }  // namespace fd
