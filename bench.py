@@ -721,6 +721,17 @@ def run_reference(args, rank):
 
 # ------------------------------------------------------------------ GPU arm
 
+def max_over_ranks(vals, world):
+    """Element-wise maximum of a tensor of timings over all ranks: every
+    replica runs the same calls independently, and the slowest one sets the
+    job's time.  One all-reduce of the (already measured) timings; no data of
+    the attention path crosses ranks."""
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    return vals
+
+
 def run_fd(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -841,8 +852,7 @@ def run_fd(args, rank, world):
     fd.check_device_error(stream)
 
     vals = torch.tensor([us_per_call, e2e_us, dom_us], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    vals = max_over_ranks(vals, world)
     us_per_call, e2e_us, dom_us = [float(x) for x in vals.tolist()]
     if rank != 0:
         return 0

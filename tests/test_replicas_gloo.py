@@ -1,0 +1,68 @@
+"""Host logic of the multi-replica benchmark on the CPU (gloo, world size 2):
+the timings reduce to their maximum over ranks, and only rank 0 of the
+reference arm does any work.  The data path has no collective (replicas
+only), so this is the whole multi-process surface."""
+
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import torch
+    import torch.distributed as dist
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        v = torch.tensor([10.0 + rank, 5.0 - rank, 1.5], dtype=torch.float64)
+        out = bench.max_over_ranks(v, world)
+        q.put((rank, [float(x) for x in out.tolist()]))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_timings_reduce_to_the_slowest_rank():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = {}
+    for _ in range(2):
+        rank, vals = q.get(timeout=120)
+        got[rank] = vals
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got[0] == got[1] == [11.0, 5.0, 1.5]
+
+
+def test_single_rank_reduction_is_identity():
+    sys.path.insert(0, ROOT)
+    import torch
+    import bench
+    v = torch.tensor([3.0, 4.0], dtype=torch.float64)
+    assert bench.max_over_ranks(v, 1) is v
+
+
+def test_reference_arm_runs_on_rank_zero_only(capsys):
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.argparse.Namespace(workload="b1_64k", steps=1, warmup=0, gpus=2, num_splits=0)
+    assert bench.run_reference(args, rank=1) == 0
+    assert capsys.readouterr().out == ""
