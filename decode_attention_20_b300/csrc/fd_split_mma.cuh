@@ -480,11 +480,13 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     for (int bb = 0; bb < C::BPW; ++bb) {
       const int row0 = (bb * C::WT + wt) * 16;       // first token row of this block
       // ---- S^T = K . Q^T
-      float sacc[NPW][4];
+      // Two accumulators per n-tile (even and odd head-dim steps) halve the
+      // chain of dependent MMAs; they are summed once below.
+      float sacc2[NPW][2][4];
 #pragma unroll
       for (int j = 0; j < NPW; ++j)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
+        for (int e = 0; e < 4; ++e) sacc2[j][0][e] = sacc2[j][1][e] = 0.f;
       if constexpr (!C::Q8) {
         const int arow = row0 + r8 + ((lane >> 3) & 1) * 8;
 #pragma unroll
@@ -495,7 +497,8 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
           uint32_t a0, a1, a2, a3;
           ldsm_x4(addr, a0, a1, a2, a3);
 #pragma unroll
-          for (int j = 0; j < NPW; ++j) mma_bf16_16816(sacc[j], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
+          for (int j = 0; j < NPW; ++j)
+            mma_bf16_16816(sacc2[j][ks & 1], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
         }
       } else {
         // A = K rows row0 + lane/4 (a0, a2) and + 8 (a1, a3); chunks 2t and
@@ -514,9 +517,15 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
           q8_to_f16x2x2<KVQ>(u4_word(ks < 4 ? kA0 : kA1, ks & 3), a0, a2);
           q8_to_f16x2x2<KVQ>(u4_word(ks < 4 ? kB0 : kB1, ks & 3), a1, a3);
 #pragma unroll
-          for (int j = 0; j < NPW; ++j) mma_f16_16816(sacc[j], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
+          for (int j = 0; j < NPW; ++j)
+            mma_f16_16816(sacc2[j][ks & 1], a0, a1, a2, a3, qf[j][ks][0], qf[j][ks][1]);
         }
       }
+      float sacc[NPW][4];
+#pragma unroll
+      for (int j = 0; j < NPW; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[j][e] = sacc2[j][0][e] + sacc2[j][1][e];
       // ---- online softmax; lane holds tokens tA = lane/4, tB = tA + 8 and
       // heads hA = 2(lane%4), hB = hA + 1 of each n-tile
       const int tokA = row0 + (lane >> 2);
