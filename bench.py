@@ -365,7 +365,10 @@ class BifWorkload(Workload):
         kv_ctx = c.k_ctx.numel() * 2 * 2
         kv_dec = sum(self.case.lens) * self.Hkv * self.D * 2 * 2
         self.required = kv_ctx + kv_dec + c.q.numel() * 2 + self.out.numel() * 4 + self.lse.numel() * 4
-        self.dominant_units = 4.0 * self.n * self.Hq * self.Lc * self.D     # context FLOPs
+        # The context kernel also streams every sample's own decode tokens
+        # (folded into it for groups of 16+ query heads), so its FLOPs are
+        # QK^T and PV over the context plus each sample's decode history.
+        self.dominant_units = 4.0 * self.Hq * self.D * (self.n * self.Lc + sum(self.case.lens))
         self.bound, self.unit = "tensor", "TFLOP/s"
 
     def config(self, ns):

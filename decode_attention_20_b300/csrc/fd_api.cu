@@ -1155,6 +1155,25 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
       for (int d = 8; d >= 2; d /= 2)
         if (d <= cmax && ns_ctx % d == 0) { csize = d; break; }
   }
+  // Decode part folded into the context kernel: one extra split index whose
+  // CTAs stream the decode K / V of their tile's samples, masked per sample.
+  // Used when a 128-row tile spans few samples (G >= 16) and the decode
+  // caches can be streamed by TMA; FD_BIF_FOLD = 0 turns it off (tuning and
+  // test knob, read on every call).
+  CUtensorMap tmKd, tmVd;
+  bool fold = false;
+  if (tc_ok && csize == 1 && G >= 16 && Ld > 0) {
+    const char* fe = getenv("FD_BIF_FOLD");
+    fold = !(fe && fe[0] == '0') && aligned16(k_dec->data) && aligned16(v_dec->data);
+    for (int i = 0; fold && i < 3; ++i)
+      fold = (k_dec->stride[i] * 2) % 16 == 0 && (v_dec->stride[i] * 2) % 16 == 0 &&
+             k_dec->stride[i] > 0 && v_dec->stride[i] > 0;
+    fold = fold && make_kv_map(&tmKd, k_dec->data, n, Ld, Hkv, D, k_dec->stride[0],
+                               k_dec->stride[1], k_dec->stride[2], kBifTileTokens, 64) &&
+           make_kv_map(&tmVd, v_dec->data, n, Ld, Hkv, D, v_dec->stride[0], v_dec->stride[1],
+                       v_dec->stride[2], kBifTileTokens, 64);
+    if (fold) ns_dec = 1;
+  }
   const int S = ns_ctx / csize + ns_dec;
   const int64_t bytes = workspace_bytes(n, Hq, D, S);
   void* ws = nullptr;
@@ -1198,7 +1217,11 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         bp.l_ss = n * Hq;
         ProfRecord rec;
         const bool prof = prof_begin(FD_KERNEL_BIF_CTX, cs, &rec);
-        e = launch_bif_ctx(bp, tmK, tmV, (int)mtiles, cs, !prof);
+        bp.dec_split = fold ? ns_ctx : -1;
+        bp.dec_lens = dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr;
+        bp.Ld = (int)Ld;
+        e = launch_bif_ctx(bp, tmK, tmV, fold ? tmKd : tmK, fold ? tmVd : tmV, (int)mtiles, cs,
+                           !prof);
         prof_end(FD_KERNEL_BIF_CTX, cs, prof, rec);
         if (e != cudaSuccess) st = cuda_fail(e, "bifurcated context kernel launch");
         ctx_done = true;
@@ -1214,7 +1237,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   }
   // Decode part: each sample's own tokens, ns_dec splits, written after
   // the context splits.
-  if (st == FD_OK && ns_dec) {
+  if (st == FD_OK && ns_dec && !(fold && ctx_done)) {
     DecodeDesc dd = {n, Hq, Hkv, D, Ld, Hq / Hkv, FD_BF16, FD_BF16};
     st = enqueue_split(dd, q, k_dec, v_dec,
                        dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr,

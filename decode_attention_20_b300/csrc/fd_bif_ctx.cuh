@@ -104,7 +104,9 @@ __device__ __forceinline__ void bif_split_range(int Lc, int ns, int i, int& begi
 
 __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     bif_ctx_kernel(const __grid_constant__ BifCtxParams p, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV) {
+                   const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmKd,
+                   const __grid_constant__ CUtensorMap tmVd) {
   using C = BifCfg;
   pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   // Every earlier grid has now finished: the decode part (which reads none of
@@ -132,9 +134,51 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   const int g = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  int begin, end;
-  bif_split_range(p.Lc, p.ns, split, begin, end);
-  const int ntiles = (end - begin + C::TN - 1) / C::TN;
+  // Context CTA: tiles [begin, end) of the shared context.  Decode CTA
+  // (split == dec_split): the decode tokens of the tile's samples s_first ..
+  // s_first + nsamp - 1, sample after sample, dlen[k] tokens each.
+  const bool dec = split == p.dec_split;
+  int begin = 0, end = 0, ntiles = 0, s_first = 0, nsamp = 0;
+  int dlen[kBifFoldMaxSamples];
+#pragma unroll
+  for (int k = 0; k < kBifFoldMaxSamples; ++k) dlen[k] = 0;
+  if (!dec) {
+    bif_split_range(p.Lc, p.ns, split, begin, end);
+    ntiles = (end - begin + C::TN - 1) / C::TN;
+  } else {
+    const int m0 = mtile * C::MT;
+    s_first = m0 / p.G;
+    nsamp = (min(m0 + C::MT, p.rows) - 1) / p.G - s_first + 1;
+#pragma unroll
+    for (int k = 0; k < kBifFoldMaxSamples; ++k)
+      if (k < nsamp) {
+        dlen[k] = resolve_len(p.dec_lens, s_first + k, p.Ld);
+        ntiles += (dlen[k] + C::TN - 1) / C::TN;
+      }
+  }
+  // Decode tile j (< ntiles) -> (sample index k within the tile, its first
+  // token, the valid tokens of the tile).  Unrolled so dlen stays in
+  // registers.
+  auto dec_tile = [&](int j, int& k_out, int& tok, int& nv) {
+    int kk = 0, len = 0;
+    bool found = false;
+#pragma unroll
+    for (int k = 0; k < kBifFoldMaxSamples; ++k) {
+      const int nt = (dlen[k] + C::TN - 1) / C::TN;
+      if (!found && k < nsamp) {
+        if (j < nt) {
+          kk = k;
+          len = dlen[k];
+          found = true;
+        } else {
+          j -= nt;
+        }
+      }
+    }
+    k_out = kk;
+    tok = j * C::TN;
+    nv = min(C::TN, len - tok);
+  };
 
   if (ntiles == 0 && p.cs == 1) {
     // Empty split: O = 0, lse = -inf for every valid row.  (In a cluster an
@@ -174,8 +218,14 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
+      if (dec) {
+        prefetch_tensormap(&tmKd);
+        prefetch_tensormap(&tmVd);
+      } else {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+      }
+      const uint64_t policy = l2_policy_evict_first();
       int kt = 0, vt = 0;                           // next K / V tile to issue
       bool ok = true;
       while (ok && (kt < ntiles || vt < ntiles)) {
@@ -186,9 +236,16 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           if (!ok) break;
           unsigned char* dst = smem + C::OFF_K + st * C::KV_BYTES;
           mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
-          const int tok = begin + kt * C::TN;
-          tma_load_3d(dst, &tmK, &k_full[st], 0, g, tok);
-          tma_load_3d(dst + C::KV_CHUNK, &tmK, &k_full[st], 64, g, tok);
+          if (dec) {
+            int k, tok, nv;
+            dec_tile(kt, k, tok, nv);
+            tma_load_4d(dst, &tmKd, &k_full[st], 0, g, tok, s_first + k, policy);
+            tma_load_4d(dst + C::KV_CHUNK, &tmKd, &k_full[st], 64, g, tok, s_first + k, policy);
+          } else {
+            const int tok = begin + kt * C::TN;
+            tma_load_3d(dst, &tmK, &k_full[st], 0, g, tok);
+            tma_load_3d(dst + C::KV_CHUNK, &tmK, &k_full[st], 64, g, tok);
+          }
           ++kt;
         }
         if (vt < ntiles && vt < kt) {
@@ -197,9 +254,16 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           if (!ok) break;
           unsigned char* dst = smem + C::OFF_V + st * C::KV_BYTES;
           mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
-          const int tok = begin + vt * C::TN;
-          tma_load_3d(dst, &tmV, &v_full[st], 0, g, tok);
-          tma_load_3d(dst + C::KV_CHUNK, &tmV, &v_full[st], 64, g, tok);
+          if (dec) {
+            int k, tok, nv;
+            dec_tile(vt, k, tok, nv);
+            tma_load_4d(dst, &tmVd, &v_full[st], 0, g, tok, s_first + k, policy);
+            tma_load_4d(dst + C::KV_CHUNK, &tmVd, &v_full[st], 64, g, tok, s_first + k, policy);
+          } else {
+            const int tok = begin + vt * C::TN;
+            tma_load_3d(dst, &tmV, &v_full[st], 0, g, tok);
+            tma_load_3d(dst + C::KV_CHUNK, &tmV, &v_full[st], 64, g, tok);
+          }
           ++vt;
         }
       }
@@ -273,6 +337,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     const uint32_t q_tmem = tmem + lane_base + C::COL_Q;
     const uint32_t o_tmem = tmem + lane_base + C::COL_O;
     const int m0 = mtile * C::MT;                 // first row of this tile
+    const int row_s = (m0 + r) / p.G;             // sample of this row
     {
       // Query row -> Q (bf16 pairs, dim 2c in the low half of column c).
       // Rows past n * G load zeros.  A negative scale is folded in here (the
@@ -315,8 +380,17 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, sr[c]);
       tc::tmem_wait_ld();
-      const int nvalid = min(C::TN, end - (begin + j * C::TN));
-      if (nvalid < C::TN) {                        // tail tile only (uniform branch)
+      // Context tile: the split's tail; decode tile: its sample's tail, and
+      // nothing at all for rows of the tile's other samples.
+      int nvalid, tile_valid = C::TN;
+      if (dec) {
+        int k, tok;
+        dec_tile(j, k, tok, tile_valid);
+        nvalid = (row_s == s_first + k) ? tile_valid : 0;
+      } else {
+        nvalid = min(C::TN, end - (begin + j * C::TN));
+      }
+      if (nvalid < C::TN) {                        // tail tiles (and other samples' decode tiles)
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -370,6 +444,22 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           tc::tmem_wait_st();
         }
       }
+      if (dec && tile_valid < C::TN) {
+        // V rows past the sample's length hold whatever the cache holds
+        // there: zero them before O += P V reads the tile (P is 0 on those
+        // rows, but 0 times a non-finite value is not 0).
+        const bool got_v = mbar_wait_or_abort(&v_full[j % C::NV], (j / C::NV) & 1, abort_s);
+        if (!__all_sync(0xffffffffu, got_v)) { ok = false; break; }
+        if (r >= tile_valid) {
+          unsigned char* vrow = smem + C::OFF_V + (j % C::NV) * C::KV_BYTES + r * 128;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            reinterpret_cast<uint4*>(vrow)[i] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(vrow + C::KV_CHUNK)[i] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        tc::fence_proxy_async_smem();
+      }
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(&p_full[j & 1]);
@@ -389,7 +479,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     if (done) {
       tc::fence_after_sync();
       const int m = m0 + r;
-      const float inv_l = 1.f / l_run;
+      const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;   // a decode row may see no token
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t orr[32];

@@ -99,7 +99,18 @@ struct BifCtxParams {
   int64_t o_sb, o_sh, o_ss;   // strides over (sample, q head, split)
   float* lse;                 // natural-log partial lse
   int64_t l_sb, l_sh, l_ss;
+  // Decode part folded into this kernel (G >= 16, so a 128-row query tile
+  // spans at most 9 samples): the CTAs of split index dec_split (= ns, one
+  // past the context splits; -1 when not folded) stream the decode K / V of
+  // the tile's samples, dec_lens[s] tokens each (nullptr: all Ld), each
+  // 128-token tile masked to the rows of its own sample.
+  int dec_split;
+  const int32_t* dec_lens;
+  int Ld;
 };
+
+// Most samples a 128-row query tile can span when the decode part is folded.
+constexpr int kBifFoldMaxSamples = 9;
 
 // Tokens per tile, and 128-row query tiles per CTA, of the bifurcated
 // context kernel.
@@ -118,6 +129,7 @@ int mma_tile_tokens(int variant, int kv_kind);
 cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, bool pdl);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                           const CUtensorMap& tmKd, const CUtensorMap& tmVd,
                            int mtiles, cudaStream_t st, bool pdl);
 
 // Tile height (tokens) of the TMA split kernel; the tensor-map box uses it.

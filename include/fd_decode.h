@@ -276,8 +276,16 @@ FD_API fd_status fd_lse_combine(const fd_tensor* part_o, const fd_tensor* part_l
  * Sample i attends over concat(context, its first dec_lens[i] decode tokens).
  * The context part runs as a tensor-core contraction whose rows are all
  * (sample, query head) pairs of a kv-head group, so the context KV is read
- * once for all samples; the decode part runs on the split kernel; partials
- * are merged by the log-sum-exp reduction.
+ * once for all samples; partials are merged by the log-sum-exp reduction.
+ * The decode part runs inside the same tensor-core kernel when a group holds
+ * 16 or more query heads (each sample's decode tiles as extra tiles of the
+ * query tile that holds its rows), else on the split kernel.  Decode tokens
+ * past dec_lens[i] are never used, whatever they hold.  With the decode part
+ * inside the tensor-core kernel, a NaN or infinity inside sample i's first
+ * dec_lens[i] values of v_dec also reaches the other samples whose rows share
+ * its 128-row query tile (their zero weights times the value); finite caches
+ * are unaffected.  Environment FD_BIF_FOLD=0 keeps the decode part on the
+ * split kernel, which isolates samples also for non-finite caches.
  * Source: bifurcated-attention summary, section "Tiivistelmä" (two GEMMs,
  * one over the prefill KV and one over the decode KV; exact result).
  */

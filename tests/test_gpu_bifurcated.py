@@ -76,14 +76,16 @@ def test_bifurcated_mqa_sampling_workload(cuda_device):
 # oracle, across M-tile tails, context tails, split counts and a peaked
 # softmax that makes the running max jump (accumulator rescaling).
 
-@pytest.fixture(params=["tc", "tc_cluster", "split"])
+@pytest.fixture(params=["tc", "tc_nofold", "tc_cluster", "split"])
 def ctx_path(request, monkeypatch):
-    """tc: tensor-core context kernel, one partial per split (default);
-    tc_cluster: the same kernel with its splits merged in thread-block
-    clusters of up to 8 CTAs where they divide evenly; split: the split
-    kernel over a broadcast view of the context."""
+    """tc: tensor-core context kernel, one partial per split, with the decode
+    part folded into it where G >= 16 (default); tc_nofold: the same with the
+    decode part on the split kernel; tc_cluster: splits merged in
+    thread-block clusters of up to 8 CTAs where they divide evenly; split:
+    the split kernel over a broadcast view of the context."""
     monkeypatch.setenv("FD_BIF_CTX", "split" if request.param == "split" else "tc")
     monkeypatch.setenv("FD_BIF_CLUSTER", "8" if request.param == "tc_cluster" else "1")
+    monkeypatch.setenv("FD_BIF_FOLD", "0" if request.param == "tc_nofold" else "1")
     return request.param
 
 
@@ -131,3 +133,27 @@ def test_bifurcated_scale_sign_and_zero(cuda_device, ctx_path, scale):
     O, L = _run(case)
     O_ref, L_ref = _ref(case)
     assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16, f"{ctx_path} scale={scale}")
+
+
+@pytest.mark.parametrize("n,G,ld,dec_lens", [
+    (8, 16, 300, [300, 0, 129, 128, 127, 1, 256, 299]),   # 8 samples per tile, every tail kind
+    (7, 24, 260, [260, 3, 0, 131, 200, 259, 64]),          # samples straddle query tiles
+    (5, 48, 400, [0, 0, 0, 0, 0]),                         # no decode token anywhere
+    (3, 32, 130, None),                                    # all Ld
+    (11, 64, 200, [5, 199, 128, 0, 77, 200, 1, 2, 150, 129, 64]),
+])
+def test_decode_folded_into_context_kernel(cuda_device, monkeypatch, n, G, ld, dec_lens):
+    """The decode part streamed by the context kernel: decode tiles of every
+    length, samples spanning two query tiles, empty decode histories, and
+    NaN left in the caches past each sample's length (never used)."""
+    monkeypatch.setenv("FD_BIF_CTX", "tc")
+    monkeypatch.setenv("FD_BIF_CLUSTER", "1")
+    monkeypatch.setenv("FD_BIF_FOLD", "1")
+    case = inputs.bifurcated_case(n, G, 1, 128, 700, ld, seed=n * 13 + G, dec_lens=dec_lens)
+    lens = [ld] * n if dec_lens is None else dec_lens
+    for i, L in enumerate(lens):
+        case.k_dec[i, L:] = float("nan")
+        case.v_dec[i, L:] = float("nan")
+    O, L = _run(case)
+    O_ref, L_ref = _ref(case)
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16, f"fold n={n} G={G} ld={ld}")
