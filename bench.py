@@ -24,7 +24,8 @@ Prints ONE JSON line (rank 0):
                host memory of the step's new inputs (query, one new K/V row per
                sequence), the call, D2H of out (+ lse), synchronised per step
   roofline     the dominant kernel's algorithmic bytes (or FLOPs) per launch /
-               its mean CUDA-event duration, against the measured peak
+               its mean CUDA-event duration (launches queued back to back,
+               without programmatic dependent launch), against the peak
   cpu_baseline the fp64 CPU oracle timed on a bounded sample of the same
                workload on the host cores (rank 0, N = 1)
 With --gpus N > 1 (torchrun), every rank runs an independent replica (the
@@ -59,6 +60,10 @@ KERNEL_NAMES = {FD_KERNEL_SPLIT: "split_mma_kernel (mma.sync bf16, TMA ring)",
 # Source files each roofline kernel is built from: a DRAM-traffic figure in
 # profiles/traffic.json is used only while these files hash to the value it
 # was captured with (otherwise the kernel has changed and traffic is null).
+# Cycles of torch.cuda._sleep per microsecond: the maximum SM clock of a
+# B300 (2032 MHz), rounded up, so a delay is at least as long as asked.
+SLEEP_CYCLES_PER_US = 2100
+
 KERNEL_SOURCES = {
     FD_KERNEL_SPLIT: ["fd_split_mma.cuh", "fd_split.cuh", "fd_device.cuh"],
     FD_KERNEL_BIF_CTX: ["fd_bif_ctx.cuh", "fd_tcgen05.cuh", "fd_split.cuh", "fd_device.cuh"],
@@ -823,9 +828,16 @@ def run_fd(args, rank, world):
     us_direct = e0.elapsed_time(e1) * 1e3 / dsteps
 
     # Per-kernel durations (CUDA events around each launch on its stream).
+    # The calls are queued behind a device-side delay longer than the host
+    # takes to issue them, so the GPU runs them back to back and each event
+    # pair brackets its kernel, not the host's time to issue the next call
+    # (short calls are host-bound when issued one by one).
+    psteps = min(dsteps, 128)
+    delay_us = 2.0 * psteps * us_direct + 5000.0
     fd.profile_enable(True)
     with torch.cuda.stream(stream):
-        for i in range(dsteps):
+        torch.cuda._sleep(int(delay_us * SLEEP_CYCLES_PER_US))
+        for i in range(psteps):
             w.call(i)
     stream.synchronize()
     kern = {}
@@ -836,9 +848,9 @@ def run_fd(args, rank, world):
         launches += n
         if n:
             kern[label + "_us"] = round(ms * 1e3 / n, 3)
-            kern[label + "_launches_per_call"] = n / dsteps
+            kern[label + "_launches_per_call"] = n / psteps
     fd.profile_enable(False)
-    launches_per_call = launches / dsteps
+    launches_per_call = launches / psteps
     dom_label = {FD_KERNEL_SPLIT: "split", FD_KERNEL_BIF_CTX: "bif_ctx"}[w.dominant]
     dom_us = kern[dom_label + "_us"]
 

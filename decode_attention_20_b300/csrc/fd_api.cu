@@ -1119,13 +1119,48 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
                         kBifTileTokens);
   }
   const int64_t mtiles = (n * G + 128 * kBifQueryTiles - 1) / (128 * kBifQueryTiles);
+  // Optional thread-block clusters (see below).  Tuning knob, read on every
+  // call.
+  const char* ce = getenv("FD_BIF_CLUSTER");
+  const int cmax = ce ? atoi(ce) : 1;
+  // Decode part folded into the context kernel: each query tile's decode
+  // tiles join its list of context tiles, masked per sample, and the list is
+  // shared out evenly over the splits.  Used when a 128-row tile spans few
+  // samples (G >= 16), no clusters are asked for and the decode caches can
+  // be streamed by TMA; FD_BIF_FOLD = 0 turns it off (tuning and test knob,
+  // read on every call).
+  CUtensorMap tmKd, tmVd;
+  bool fold = false;
+  if (tc_ok && cmax < 2 && G >= 16 && Ld > 0) {
+    const char* fe = getenv("FD_BIF_FOLD");
+    fold = !(fe && fe[0] == '0') && aligned16(k_dec->data) && aligned16(v_dec->data);
+    for (int i = 0; fold && i < 3; ++i)
+      fold = (k_dec->stride[i] * 2) % 16 == 0 && (v_dec->stride[i] * 2) % 16 == 0 &&
+             k_dec->stride[i] > 0 && v_dec->stride[i] > 0;
+    fold = fold && make_kv_map(&tmKd, k_dec->data, n, Ld, Hkv, D, k_dec->stride[0],
+                               k_dec->stride[1], k_dec->stride[2], kBifTileTokens, 64) &&
+           make_kv_map(&tmVd, v_dec->data, n, Ld, Hkv, D, v_dec->stride[0], v_dec->stride[1],
+                       v_dec->stride[2], kBifTileTokens, 64);
+  }
+  // Split count.  Folded: over the longest list a query tile can have (its
+  // context tiles plus full decode caches of the most samples a tile spans).
+  int64_t work_tokens = Lc;
+  if (fold) {
+    int64_t most = 1;
+    for (int64_t t = 0; t < mtiles; ++t) {
+      const int64_t m0 = t * 128, last = std::min<int64_t>(m0 + 128, n * G) - 1;
+      most = std::max<int64_t>(most, last / G - m0 / G + 1);
+    }
+    work_tokens = ((Lc + kBifTileTokens - 1) / kBifTileTokens +
+                   most * ((Ld + kBifTileTokens - 1) / kBifTileTokens)) * kBifTileTokens;
+  }
   const int ns_ctx = ctx_splits > 0 ? ctx_splits
-                     : tc_ok ? choose_ctx_splits(Lc, mtiles * Hkv, info->sms)
+                     : tc_ok ? choose_ctx_splits(work_tokens, mtiles * Hkv, info->sms)
                              : choose_splits_host(n, Hkv, Lc, info->sms);
-  // Decode part: about two CTAs per SM over (sample, kv head) units, at
-  // most one 64-token tile per split.
+  // Decode part on the split kernel (not folded): about two CTAs per SM over
+  // (sample, kv head) units, at most one 64-token tile per split.
   int ns_dec = 0;
-  if (Ld > 0) {
+  if (Ld > 0 && !fold) {
     int64_t want = (2 * (int64_t)info->sms) / (n * Hkv);
     // Tuning knob, read on every call: FD_BIF_DEC_SPLITS fixes the count.
     if (const char* e = getenv("FD_BIF_DEC_SPLITS")) {
@@ -1146,33 +1181,12 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   // when every split holds tokens.
   int csize = 1;
   if (tc_ok) {
-    const char* ce = getenv("FD_BIF_CLUSTER");
-    const int cmax = ce ? atoi(ce) : 1;
     const int64_t per = (Lc + ns_ctx - 1) / ns_ctx;
     const int64_t chunk = ((per + kBifTileTokens - 1) / kBifTileTokens) * kBifTileTokens;
     const bool all_full = (int64_t)(ns_ctx - 1) * chunk < Lc;
     if (cmax >= 2 && all_full)
       for (int d = 8; d >= 2; d /= 2)
         if (d <= cmax && ns_ctx % d == 0) { csize = d; break; }
-  }
-  // Decode part folded into the context kernel: one extra split index whose
-  // CTAs stream the decode K / V of their tile's samples, masked per sample.
-  // Used when a 128-row tile spans few samples (G >= 16) and the decode
-  // caches can be streamed by TMA; FD_BIF_FOLD = 0 turns it off (tuning and
-  // test knob, read on every call).
-  CUtensorMap tmKd, tmVd;
-  bool fold = false;
-  if (tc_ok && csize == 1 && G >= 16 && Ld > 0) {
-    const char* fe = getenv("FD_BIF_FOLD");
-    fold = !(fe && fe[0] == '0') && aligned16(k_dec->data) && aligned16(v_dec->data);
-    for (int i = 0; fold && i < 3; ++i)
-      fold = (k_dec->stride[i] * 2) % 16 == 0 && (v_dec->stride[i] * 2) % 16 == 0 &&
-             k_dec->stride[i] > 0 && v_dec->stride[i] > 0;
-    fold = fold && make_kv_map(&tmKd, k_dec->data, n, Ld, Hkv, D, k_dec->stride[0],
-                               k_dec->stride[1], k_dec->stride[2], kBifTileTokens, 64) &&
-           make_kv_map(&tmVd, v_dec->data, n, Ld, Hkv, D, v_dec->stride[0], v_dec->stride[1],
-                       v_dec->stride[2], kBifTileTokens, 64);
-    if (fold) ns_dec = 1;
   }
   const int S = ns_ctx / csize + ns_dec;
   const int64_t bytes = workspace_bytes(n, Hq, D, S);
@@ -1217,7 +1231,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         bp.l_ss = n * Hq;
         ProfRecord rec;
         const bool prof = prof_begin(FD_KERNEL_BIF_CTX, cs, &rec);
-        bp.dec_split = fold ? ns_ctx : -1;
+        bp.fold = fold ? 1 : 0;
         bp.dec_lens = dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr;
         bp.Ld = (int)Ld;
         e = launch_bif_ctx(bp, tmK, tmV, fold ? tmKd : tmK, fold ? tmVd : tmV, (int)mtiles, cs,
@@ -1237,7 +1251,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
   }
   // Decode part: each sample's own tokens, ns_dec splits, written after
   // the context splits.
-  if (st == FD_OK && ns_dec && !(fold && ctx_done)) {
+  if (st == FD_OK && ns_dec) {
     DecodeDesc dd = {n, Hq, Hkv, D, Ld, Hq / Hkv, FD_BF16, FD_BF16};
     st = enqueue_split(dd, q, k_dec, v_dec,
                        dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr,

@@ -17,6 +17,16 @@
 // "How does Flash Attention reduce memory traffic during local inference?",
 // section on online softmax.
 //
+// With 16 or more query heads per kv head, a 128-row query tile spans at
+// most 9 samples, and the kernel also takes the decode part ("fold"): each
+// decode tile (128 tokens of one sample's own cache, 4-D tensor map over
+// [n, Ld, Hkv, D]) joins the tile's list of work with the scores of the
+// other samples' rows masked to -inf, and the V rows past the sample's
+// length zeroed in shared memory.  The list, context tiles then decode
+// tiles, is cut into equal runs, one per split, so every CTA streams about
+// the same number of tiles; the log-sum-exp reduction then needs no separate
+// decode partial.
+//
 // CTA = one 128-row query tile x one context split x one kv head; 6 warps:
 //   warp 0      TMA producer: K and V tiles of 128 tokens into separate
 //               3-stage rings, 128-byte swizzle (two 64-column boxes per
@@ -134,49 +144,74 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   const int g = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Context CTA: tiles [begin, end) of the shared context.  Decode CTA
-  // (split == dec_split): the decode tokens of the tile's samples s_first ..
-  // s_first + nsamp - 1, sample after sample, dlen[k] tokens each.
-  const bool dec = split == p.dec_split;
-  int begin = 0, end = 0, ntiles = 0, s_first = 0, nsamp = 0;
+  // Without the fold: context tiles [begin, end) of this split.  With it:
+  // the query tile's work is the list of the nct context tiles followed by
+  // the decode tiles of its samples s_first .. s_first + nsamp - 1 (sample
+  // after sample, dlen[k] tokens each), and this split takes the run
+  // [t0, t0 + ntiles) of that list.
+  const bool fold = p.fold != 0;
+  const int nct = (p.Lc + C::TN - 1) / C::TN;
+  int begin = 0, end = 0, ntiles = 0, t0 = 0, s_first = 0, nsamp = 0;
   int dlen[kBifFoldMaxSamples];
 #pragma unroll
   for (int k = 0; k < kBifFoldMaxSamples; ++k) dlen[k] = 0;
-  if (!dec) {
+  if (!fold) {
     bif_split_range(p.Lc, p.ns, split, begin, end);
     ntiles = (end - begin + C::TN - 1) / C::TN;
   } else {
     const int m0 = mtile * C::MT;
     s_first = m0 / p.G;
     nsamp = (min(m0 + C::MT, p.rows) - 1) / p.G - s_first + 1;
+    int total = nct;
 #pragma unroll
     for (int k = 0; k < kBifFoldMaxSamples; ++k)
       if (k < nsamp) {
         dlen[k] = resolve_len(p.dec_lens, s_first + k, p.Ld);
-        ntiles += (dlen[k] + C::TN - 1) / C::TN;
+        total += (dlen[k] + C::TN - 1) / C::TN;
       }
+    const int per = (total + p.ns - 1) / p.ns;
+    t0 = min(split * per, total);
+    ntiles = min(t0 + per, total) - t0;
   }
-  // Decode tile j (< ntiles) -> (sample index k within the tile, its first
-  // token, the valid tokens of the tile).  Unrolled so dlen stays in
-  // registers.
-  auto dec_tile = [&](int j, int& k_out, int& tok, int& nv) {
+  // Tile j (< ntiles) of this CTA -> whether it is a decode tile, its sample
+  // index k within the query tile (decode tiles), its first token (in the
+  // context, or in sample k's decode cache) and its valid tokens.  Unrolled
+  // so dlen stays in registers.
+  auto tile_of = [&](int j, bool& is_dec, int& k_out, int& tok, int& nv) {
+    if (!fold) {
+      is_dec = false;
+      k_out = 0;
+      tok = begin + j * C::TN;
+      nv = min(C::TN, end - tok);
+      return;
+    }
+    int f = t0 + j;
+    if (f < nct) {
+      is_dec = false;
+      k_out = 0;
+      tok = f * C::TN;
+      nv = min(C::TN, p.Lc - tok);
+      return;
+    }
+    f -= nct;
     int kk = 0, len = 0;
     bool found = false;
 #pragma unroll
     for (int k = 0; k < kBifFoldMaxSamples; ++k) {
       const int nt = (dlen[k] + C::TN - 1) / C::TN;
       if (!found && k < nsamp) {
-        if (j < nt) {
+        if (f < nt) {
           kk = k;
           len = dlen[k];
           found = true;
         } else {
-          j -= nt;
+          f -= nt;
         }
       }
     }
+    is_dec = true;
     k_out = kk;
-    tok = j * C::TN;
+    tok = f * C::TN;
     nv = min(C::TN, len - tok);
   };
 
@@ -218,12 +253,11 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      if (dec) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      if (fold) {
         prefetch_tensormap(&tmKd);
         prefetch_tensormap(&tmVd);
-      } else {
-        prefetch_tensormap(&tmK);
-        prefetch_tensormap(&tmV);
       }
       const uint64_t policy = l2_policy_evict_first();
       int kt = 0, vt = 0;                           // next K / V tile to issue
@@ -236,13 +270,13 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           if (!ok) break;
           unsigned char* dst = smem + C::OFF_K + st * C::KV_BYTES;
           mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
-          if (dec) {
-            int k, tok, nv;
-            dec_tile(kt, k, tok, nv);
+          bool is_dec;
+          int k, tok, nv;
+          tile_of(kt, is_dec, k, tok, nv);
+          if (is_dec) {
             tma_load_4d(dst, &tmKd, &k_full[st], 0, g, tok, s_first + k, policy);
             tma_load_4d(dst + C::KV_CHUNK, &tmKd, &k_full[st], 64, g, tok, s_first + k, policy);
           } else {
-            const int tok = begin + kt * C::TN;
             tma_load_3d(dst, &tmK, &k_full[st], 0, g, tok);
             tma_load_3d(dst + C::KV_CHUNK, &tmK, &k_full[st], 64, g, tok);
           }
@@ -254,13 +288,13 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           if (!ok) break;
           unsigned char* dst = smem + C::OFF_V + st * C::KV_BYTES;
           mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
-          if (dec) {
-            int k, tok, nv;
-            dec_tile(vt, k, tok, nv);
+          bool is_dec;
+          int k, tok, nv;
+          tile_of(vt, is_dec, k, tok, nv);
+          if (is_dec) {
             tma_load_4d(dst, &tmVd, &v_full[st], 0, g, tok, s_first + k, policy);
             tma_load_4d(dst + C::KV_CHUNK, &tmVd, &v_full[st], 64, g, tok, s_first + k, policy);
           } else {
-            const int tok = begin + vt * C::TN;
             tma_load_3d(dst, &tmV, &v_full[st], 0, g, tok);
             tma_load_3d(dst + C::KV_CHUNK, &tmV, &v_full[st], 64, g, tok);
           }
@@ -380,16 +414,12 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, sr[c]);
       tc::tmem_wait_ld();
-      // Context tile: the split's tail; decode tile: its sample's tail, and
-      // nothing at all for rows of the tile's other samples.
-      int nvalid, tile_valid = C::TN;
-      if (dec) {
-        int k, tok;
-        dec_tile(j, k, tok, tile_valid);
-        nvalid = (row_s == s_first + k) ? tile_valid : 0;
-      } else {
-        nvalid = min(C::TN, end - (begin + j * C::TN));
-      }
+      // Context tile: the context's tail; decode tile: its sample's tail,
+      // and nothing at all for rows of the tile's other samples.
+      bool is_dec;
+      int ks, tok, tile_valid;
+      tile_of(j, is_dec, ks, tok, tile_valid);
+      const int nvalid = (!is_dec || row_s == s_first + ks) ? tile_valid : 0;
       if (nvalid < C::TN) {                        // tail tiles (and other samples' decode tiles)
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -444,7 +474,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
           tc::tmem_wait_st();
         }
       }
-      if (dec && tile_valid < C::TN) {
+      if (is_dec && tile_valid < C::TN) {
         // V rows past the sample's length hold whatever the cache holds
         // there: zero them before O += P V reads the tile (P is 0 on those
         // rows, but 0 times a non-finite value is not 0).

@@ -99,12 +99,13 @@ struct BifCtxParams {
   int64_t o_sb, o_sh, o_ss;   // strides over (sample, q head, split)
   float* lse;                 // natural-log partial lse
   int64_t l_sb, l_sh, l_ss;
-  // Decode part folded into this kernel (G >= 16, so a 128-row query tile
-  // spans at most 9 samples): the CTAs of split index dec_split (= ns, one
-  // past the context splits; -1 when not folded) stream the decode K / V of
-  // the tile's samples, dec_lens[s] tokens each (nullptr: all Ld), each
-  // 128-token tile masked to the rows of its own sample.
-  int dec_split;
+  // Decode part folded into this kernel (fold = 1; needs G >= 16, so a
+  // 128-row query tile spans at most 9 samples).  A query tile's work is
+  // then one list of 128-token tiles, the context's followed by the decode
+  // tiles of the tile's samples (dec_lens[s] tokens each, nullptr: all Ld;
+  // each masked to the rows of its own sample), cut into ns equal runs, one
+  // per split.
+  int fold;
   const int32_t* dec_lens;
   int Ld;
 };

@@ -204,8 +204,6 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmKd, const CUtensorMap& tmVd,
                            int mtiles, cudaStream_t st, bool pdl) {
-  // One more split index when the decode part is folded in.
-  const int ny = p.ns + (p.dec_split >= 0 ? 1 : 0);
   static unsigned long long attr_set = 0ull;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -218,7 +216,7 @@ cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const 
     attr_set |= bit;
   }
   if (p.cs <= 1)
-    return launch_ex(bif_ctx_kernel, dim3(mtiles, ny, p.Hkv), dim3(BifCfg::THREADS),
+    return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
                      BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV, tmKd, tmVd);
   // Clusters of cs CTAs along the splits (grid.y is a multiple of cs).
   cudaLaunchConfig_t cfg = {};

@@ -142,10 +142,13 @@ def test_bifurcated_scale_sign_and_zero(cuda_device, ctx_path, scale):
     (3, 32, 130, None),                                    # all Ld
     (11, 64, 200, [5, 199, 128, 0, 77, 200, 1, 2, 150, 129, 64]),
 ])
-def test_decode_folded_into_context_kernel(cuda_device, monkeypatch, n, G, ld, dec_lens):
+@pytest.mark.parametrize("ctx_splits", [0, 1, 4, 40])
+def test_decode_folded_into_context_kernel(cuda_device, monkeypatch, n, G, ld, dec_lens, ctx_splits):
     """The decode part streamed by the context kernel: decode tiles of every
-    length, samples spanning two query tiles, empty decode histories, and
-    NaN left in the caches past each sample's length (never used)."""
+    length, samples spanning two query tiles, empty decode histories, NaN
+    left in the caches past each sample's length (never used), and the
+    tile list of a query tile cut into 1, 4 or 40 runs (40: some splits get
+    nothing) or the library's count."""
     monkeypatch.setenv("FD_BIF_CTX", "tc")
     monkeypatch.setenv("FD_BIF_CLUSTER", "1")
     monkeypatch.setenv("FD_BIF_FOLD", "1")
@@ -154,6 +157,7 @@ def test_decode_folded_into_context_kernel(cuda_device, monkeypatch, n, G, ld, d
     for i, L in enumerate(lens):
         case.k_dec[i, L:] = float("nan")
         case.v_dec[i, L:] = float("nan")
-    O, L = _run(case)
+    O, L = _run(case, ctx_splits)
     O_ref, L_ref = _ref(case)
-    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16, f"fold n={n} G={G} ld={ld}")
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16,
+                  f"fold n={n} G={G} ld={ld} ns={ctx_splits}")
