@@ -297,7 +297,9 @@ FD_API fd_status fd_bifurcated_attention(const fd_tensor* q, const fd_tensor* k_
 /*
  * fd_bifurcated_attention_lse — fd_bifurcated_attention that also writes
  * lse [n, Hq] FD_F32 (may be NULL) and takes an explicit context split count
- * (0 = library choice).
+ * (0 = library choice; 1..FD_MAX_SPLITS, else FD_ERR_ARG).  With the decode
+ * part inside the tensor-core kernel, the count is the number of equal runs
+ * a query tile's context and decode tiles are cut into.
  */
 FD_API fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx,
                                       const fd_tensor* v_ctx, const fd_tensor* k_dec,
