@@ -194,11 +194,15 @@ cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, b
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
-  if (p.Rm > 1)
-    return launch_ex(lse_combine_kernel<true>, dim3(p.R1 * p.Rm * p.R2), dim3(kCombineThreads), 0,
-                     st, pdl, p);
-  return launch_ex(lse_combine_kernel<false>, dim3(p.R1 * p.R2), dim3(kCombineThreads), 0, st,
-                   pdl, p);
+  const int rows = p.R1 * (p.Rm > 1 ? p.Rm : 1) * p.R2;   // Rm is 0 or 1 without query tokens
+  if (rows > kCombineFewRows)
+    return p.Rm > 1 ? launch_ex(lse_combine_many_kernel<true>, dim3(rows),
+                                dim3(kCombineManyThreads), 0, st, pdl, p)
+                    : launch_ex(lse_combine_many_kernel<false>, dim3(rows),
+                                dim3(kCombineManyThreads), 0, st, pdl, p);
+  const int threads = combine_threads(p.S, p.D);
+  return p.Rm > 1 ? launch_ex(lse_combine_kernel<true>, dim3(rows), dim3(threads), 0, st, pdl, p)
+                  : launch_ex(lse_combine_kernel<false>, dim3(rows), dim3(threads), 0, st, pdl, p);
 }
 
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,

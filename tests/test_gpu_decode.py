@@ -197,6 +197,32 @@ def test_lse_combine_standalone(cuda_device):
     assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.float32, "combine")
 
 
+@pytest.mark.parametrize("R,S,D", [
+    (1, 1, 128), (64, 37, 128), (5, 100, 128), (3, 300, 64),      # one and several load batches
+    (2, 4096, 512), (4, 33, 4), (7, 20, 12), (3, 17, 512),         # widest rows, 1 and 3 chunks per row
+    (1500, 9, 128), (1100, 70, 64),                                # grids of many rows
+])
+def test_lse_combine_shapes(cuda_device, R, S, D):
+    """Split counts and head dims across the combine's thread layouts: one
+    or several batches of partial rows per thread, rows of 1 to 128 float4
+    chunks (threads left over when the chunks do not divide the block),
+    grids of few and many rows; empty splits hold NaN, which must not reach
+    the result."""
+    g = torch.Generator().manual_seed(R * 7 + S * 3 + D)
+    po = torch.randn((R, S, D), generator=g)
+    pl = torch.randn((R, S), generator=g) * 8
+    pl[0, ::3] = -float("inf")
+    po[0, ::3] = float("nan")
+    if R > 2:
+        pl[2, :] = -float("inf")                        # every split empty
+        po[2, :] = float("nan")
+    O, L = fd.lse_combine(po.cuda(), pl.cuda())
+    # An empty split's row is undefined; the oracle gets zeros there.
+    po_def = torch.where(torch.isneginf(pl)[..., None], torch.zeros_like(po), po)
+    O_ref, L_ref = oracle.lse_combine_ref(to_f64(po_def), to_f64(pl))
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.float32, f"combine R={R} S={S} D={D}")
+
+
 def test_stream_ordering_on_side_stream(cuda_device):
     case = inputs.flash_decoding_b1(2048, seed=20)
     s = torch.cuda.Stream()
