@@ -1,8 +1,9 @@
 """Benchmark of the decode-attention hot path on one B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fd|reference]
-                    [--workload b1_64k|ragged_b32|long_b4|bif_mqa|paged_b1_64k]
-                    [--num-splits S]
+                    [--workload b1_64k|ragged_b32|long_b4|bif_mqa|paged_b1_64k|
+                                int8_b1_64k|e4m3_b1_64k|verify4_b1_64k]
+                    [--num-splits S] [--bif-sweep]
 
 Default workload: split-KV decode attention at batch 1 over a 65536-token
 history of a CodeLlama-34B-shaped layer (64 query heads, 8 kv heads, head
@@ -16,6 +17,14 @@ kernel + log-sum-exp combine) over the whole history.  Other workloads:
               line also carries the replicated-context decode time
   paged_b1_64k the batch-1 64K layer with its history in 64-token pages
               scattered by a seeded permutation (paged KV cache)
+  int8_b1_64k, e4m3_b1_64k
+              the batch-1 64K layer over an 8-bit cache (int8 or e4m3 codes,
+              one fp32 scale per kv head for K and for V)
+  verify4_b1_64k
+              the batch-1 64K layer verifying 4 new query positions per
+              sequence (causal among them)
+  --bif-sweep bifurcated vs replicated-context timings over samples,
+              context lengths and kv heads (a measurement aid, not a line)
 Prints ONE JSON line (rank 0):
   value        device-timed microseconds per call: CUDA events around K calls
                replayed from a CUDA graph, inputs resident in HBM and rotated
