@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -105,14 +106,14 @@ struct ProfRecord {
   cudaEvent_t start, stop;
 };
 struct ProfState {
-  bool on = false;
+  std::atomic<bool> on{false};   // read without the lock on every launch
   std::vector<ProfRecord> rec[FD_KERNEL_KINDS];
   std::vector<ProfRecord> pool;
 } g_prof;
 std::mutex g_prof_mu;
 
 bool prof_begin(int kind, cudaStream_t st, ProfRecord* r) {
-  if (!g_prof.on) return false;
+  if (!g_prof.on.load(std::memory_order_relaxed)) return false;
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (!g_prof.pool.empty()) {
     *r = g_prof.pool.back();
@@ -135,18 +136,26 @@ void prof_end(int kind, cudaStream_t st, bool active, const ProfRecord& r) {
 
 // ------------------------------------------------------------------ TMA maps
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+// The driver's tensor-map encoder, looked up once (atomic: calls may come
+// from several host threads; two lookups store the same pointer).
+std::atomic<PFN_cuTensorMapEncodeTiled_v12000> g_encode_fn{nullptr};
 
 fd_status get_encoder() {
-  if (g_encode) return FD_OK;
+  if (g_encode_fn.load(std::memory_order_acquire)) return FD_OK;
   void* fn = nullptr;
   cudaDriverEntryPointQueryResult q;
   cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
                                                    cudaEnableDefault, &q);
   if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
     return fail(FD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  g_encode_fn.store(reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn),
+                    std::memory_order_release);
   return FD_OK;
+}
+
+// Callers run get_encoder() first.
+inline PFN_cuTensorMapEncodeTiled_v12000 g_encode() {
+  return g_encode_fn.load(std::memory_order_acquire);
 }
 
 // 4-D map over a [B, L, Hkv, D] cache of bf16 (esz 2) or 8-bit codes (esz
@@ -168,7 +177,7 @@ bool make_kv_map(CUtensorMap* map, const void* base, int64_t B, int64_t L, int64
       (box_d * esz == 128) ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
   const CUtensorMapDataType dt =
       esz == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUresult r = g_encode(map, dt, 4, const_cast<void*>(base), dims,
+  CUresult r = g_encode()(map, dt, 4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -185,7 +194,7 @@ bool make_3d_map(CUtensorMap* map, const void* base, int64_t D, int64_t n1, int6
   cuuint64_t strides[2] = {(cuuint64_t)(s1_elems * esz), (cuuint64_t)(s2_eff * esz)};
   cuuint32_t box[3] = {64u, (cuuint32_t)box1, (cuuint32_t)box2};
   cuuint32_t estr[3] = {1u, 1u, 1u};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = g_encode()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1310,7 +1319,7 @@ fd_status fd_profile_enable(int32_t on) {
     for (auto& r : g_prof.rec[k]) g_prof.pool.push_back(r);
     g_prof.rec[k].clear();
   }
-  g_prof.on = on != 0;
+  g_prof.on.store(on != 0, std::memory_order_relaxed);
   return FD_OK;
 }
 

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <utility>
 
 #include "fd_combine.cuh"
@@ -34,6 +35,22 @@ static cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
+// The dynamic shared-memory opt-in of a kernel is per (function, device).
+// `done` keeps one bit per device index below 64 (higher indices set the
+// attribute on every call).  Atomic, since calls may come from several host
+// threads; two threads that both set the attribute do no harm.
+template <typename K>
+static cudaError_t smem_optin(K kern, int bytes, std::atomic<unsigned long long>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 cudaError_t read_and_clear_device_error(unsigned int* bits, cudaStream_t st) {
   unsigned int zero = 0u;
   cudaError_t e = cudaMemcpyFromSymbolAsync(bits, g_device_error, sizeof(unsigned int), 0,
@@ -52,17 +69,9 @@ static cudaError_t launch_tma_variant(const SplitParams& p, const CUtensorMap& t
                                       const CUtensorMap& tmV, cudaStream_t st, bool pdl) {
   using C = TmaCfg<GH, HC>;
   auto kern = split_tma_kernel<GH, HC>;
-  // The shared-memory opt-in is per (function, device): remember it per device.
-  static unsigned long long attr_set = 0ull;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<unsigned long long> optin{0ull};
+  const cudaError_t e = smem_optin(kern, C::SMEM_BYTES, optin);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_set & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set |= bit;
-  }
   return launch_ex(kern, dim3(p.ns, p.Hkv, p.B), dim3(C::THREADS), C::SMEM_BYTES, st, pdl, p,
                    tmK, tmV);
 }
@@ -90,16 +99,9 @@ static cudaError_t launch_mma_variant(const SplitParams& p, const CUtensorMap& t
                                       const CUtensorMap& tmV, cudaStream_t st, bool pdl) {
   using C = MmaCfg<KVQ, NT, WN, W, T, NSTAGE>;
   auto kern = split_mma_kernel<KVQ, NT, WN, W, T, NSTAGE>;
-  static unsigned long long attr_set = 0ull;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<unsigned long long> optin{0ull};
+  const cudaError_t e = smem_optin(kern, C::SMEM_BYTES, optin);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_set & bit)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set |= bit;
-  }
   return launch_ex(kern, dim3(p.ns, p.Hkv, p.B), dim3(C::THREADS), C::SMEM_BYTES, st, pdl, p,
                    tmK, tmV);
 }
@@ -208,17 +210,9 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmKd, const CUtensorMap& tmVd,
                            int mtiles, cudaStream_t st, bool pdl) {
-  static unsigned long long attr_set = 0ull;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<unsigned long long> optin{0ull};
+  const cudaError_t e = smem_optin(bif_ctx_kernel, BifCfg::SMEM_BYTES, optin);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_set & bit)) {
-    e = cudaFuncSetAttribute(bif_ctx_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             BifCfg::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set |= bit;
-  }
   if (p.cs <= 1)
     return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
                      BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV, tmKd, tmVd);
