@@ -844,8 +844,10 @@ def run_fd(args, rank, world):
     psteps = min(dsteps, 128)
     delay_us = 2.0 * psteps * us_direct + 5000.0
     fd.profile_enable(True)
+    sleep = getattr(torch.cuda, "_sleep", None)       # a device-side spin of N clock cycles
     with torch.cuda.stream(stream):
-        torch.cuda._sleep(int(delay_us * SLEEP_CYCLES_PER_US))
+        if sleep is not None:
+            sleep(int(delay_us * SLEEP_CYCLES_PER_US))
         for i in range(psteps):
             w.call(i)
     stream.synchronize()
