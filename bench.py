@@ -66,25 +66,40 @@ KERNEL_NAMES = {FD_KERNEL_SPLIT: "split_mma_kernel (mma.sync bf16, TMA ring)",
                 FD_KERNEL_BIF_CTX: "bif_ctx_kernel (tcgen05.mma, TMEM accumulators)"}
 
 
-# Source files each roofline kernel is built from: a DRAM-traffic figure in
-# profiles/traffic.json is used only while these files hash to the value it
-# was captured with (otherwise the kernel has changed and traffic is null).
 # Cycles of torch.cuda._sleep per microsecond: the maximum SM clock of a
 # B300 (2032 MHz), rounded up, so a delay is at least as long as asked.
 SLEEP_CYCLES_PER_US = 2100
 
+# Source files each roofline kernel is built from: a DRAM-traffic figure in
+# profiles/traffic.json is used only while their code (comments and
+# whitespace aside) hashes to the value it was captured with; otherwise the
+# kernel has changed and traffic is null.
 KERNEL_SOURCES = {
     FD_KERNEL_SPLIT: ["fd_split_mma.cuh", "fd_split.cuh", "fd_device.cuh"],
     FD_KERNEL_BIF_CTX: ["fd_bif_ctx.cuh", "fd_tcgen05.cuh", "fd_split.cuh", "fd_device.cuh"],
 }
 
 
-def kernel_source_hash(kind):
+def _code_only(text):
+    """Source text without its comments and with whitespace runs collapsed,
+    so that editing a comment does not count as changing the kernel."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(kind, read=None):
+    """Hash of the code of the kind's source files; `read(name)` returns a
+    file's text (default: the files under csrc/)."""
     import hashlib
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "decode_attention_20_b300", "csrc", name)) as f:
+                return f.read()
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, "decode_attention_20_b300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        h.update(_code_only(read(name)).encode())
     return h.hexdigest()[:16]
 
 

@@ -26,13 +26,16 @@
 // K and V tiles arrive by TMA with the 128-byte swizzle (two 64-column boxes
 // per tile), so every ldmatrix is bank-conflict free.
 //
+// With a bf16 cache the probabilities enter the PV product as a hi + lo pair
+// of bf16 values (two MMAs), which keeps ~16 mantissa bits; the running sum
+// l stays in fp32.
+//
 // 8-bit caches (int8 or e4m3 codes with one scale per kv head for K and for
 // V): one 128-byte box per row, codes turned into exact f16 values in
 // registers, f16 mma.sync with the queries in f16 (per-head power-of-two
 // rescale); the K scale joins the score scale and the V scale the final
-// normalisation.  Half the bytes per token of the bf16 cache.  The probabilities
-// enter the PV product as a hi + lo pair of bf16 values (two MMAs), which
-// keeps ~16 mantissa bits; the running sum l stays in fp32.
+// normalisation.  Half the bytes per token of the bf16 cache.  P enters the
+// PV product as one f16 value (11 significant bits), one MMA.
 #pragma once
 
 #include "fd_split.cuh"
