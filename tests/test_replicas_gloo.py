@@ -1,7 +1,8 @@
-"""Host logic of the multi-replica benchmark on the CPU (gloo, world size 2):
-the timings reduce to their maximum over ranks, and only rank 0 of the
-reference arm does any work.  The data path has no collective (replicas
-only), so this is the whole multi-process surface."""
+"""Host logic of the benchmark on the CPU.  Multi-replica (gloo, world size
+2): the timings reduce to their maximum over ranks, and only rank 0 of the
+reference arm does any work; the data path has no collective (replicas
+only), so this is the whole multi-process surface.  Also the source hash
+that decides whether a committed DRAM-traffic record still applies."""
 
 import os
 import socket
@@ -66,3 +67,16 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     args = bench.argparse.Namespace(workload="b1_64k", steps=1, warmup=0, gpus=2, num_splits=0)
     assert bench.run_reference(args, rank=1) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_traffic_hash_ignores_comments_not_code():
+    """The DRAM-traffic records stay valid across comment edits of a kernel's
+    sources and lapse on any code edit."""
+    import bench
+    src = {n: "int a = 1;  // one\n/* block\n comment */ int b = 2;\n" for n in
+           bench.KERNEL_SOURCES[bench.FD_KERNEL_SPLIT]}
+    h0 = bench.kernel_source_hash(bench.FD_KERNEL_SPLIT, src.__getitem__)
+    recommented = {n: "int a = 1;   // another comment\nint b = 2;  /* x */\n" for n in src}
+    assert bench.kernel_source_hash(bench.FD_KERNEL_SPLIT, recommented.__getitem__) == h0
+    changed = {n: "int a = 1;\nint b = 3;\n" for n in src}
+    assert bench.kernel_source_hash(bench.FD_KERNEL_SPLIT, changed.__getitem__) != h0
