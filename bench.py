@@ -7,8 +7,9 @@
 
 Default workload: split-KV decode attention at batch 1 over a 65536-token
 history of a CodeLlama-34B-shaped layer (64 query heads, 8 kv heads, head
-dim 128, bf16 K/V, fp32 out + LSE).  One step = one library call (split
-kernel + log-sum-exp combine) over the whole history.  Other workloads:
+dim 128, bf16 K/V, fp32 out + LSE).  One call = split kernel + log-sum-exp
+combine over the whole history; a timed step replays a graph of such calls.
+Other workloads:
   ragged_b32  batch 32, 32/8 heads, padded [32, 32768, 8, 128] cache, lengths
               uniform in [1024, 32768]
   long_b4     batch 4, 131072 tokens, 32/8 heads, 1% of keys scaled by 8
@@ -26,22 +27,31 @@ kernel + log-sum-exp combine) over the whole history.  Other workloads:
   --bif-sweep bifurcated vs replicated-context timings over samples,
               context lengths and kv heads (a measurement aid, not a line)
 Prints ONE JSON line (rank 0):
-  value        device-timed microseconds per call: CUDA events around K calls
-               replayed from a CUDA graph, inputs resident in HBM and rotated
-               over enough copies that every call reads past L2
+  value        device-timed microseconds per call.  Exactly --steps timed
+               steps (after --warmup untimed ones); a step is one replay of a
+               CUDA graph of C back-to-back calls over rotating input copies
+               that together exceed L2 (C sized so that the steps span about
+               --window-ms); CUDA events on the launching stream, a barrier
+               and a synchronise on both sides.  ms_per_step is one step.
   e2e          microseconds per step through the Python API: H2D from pinned
                host memory of the step's new inputs (query, one new K/V row per
                sequence), the call, D2H of out (+ lse), synchronised per step
   roofline     the dominant kernel's algorithmic bytes (or FLOPs) per launch /
                its mean CUDA-event duration (launches queued back to back,
                without programmatic dependent launch), against the peak
-  cpu_baseline the fp64 CPU oracle timed on a bounded sample of the same
-               workload on the host cores (rank 0, N = 1)
+  configs      (default workload, one GPU) the other workloads measured the
+               same way: the tiny fp32 case, the batch-1 layer at 512..32K
+               tokens (graph and direct-call microseconds), the ragged batch,
+               bifurcated sampling with its replicated-context comparison, and
+               the long peaked context
+  cpu_baseline the fp64 CPU oracle, best of 3 timings of a fixed sample of
+               the same workload on the host cores (rank 0, N = 1)
 With --gpus N > 1 (torchrun), every rank runs an independent replica (the
 method has no cross-GPU exchange); value is the max over ranks.
 
---impl reference times the fp64 CPU oracle instead (each step a bounded
-sample of the same workload, extrapolated to one full call).
+--impl reference times the fp64 CPU oracle instead (each step one timing of
+the same fixed sample, extrapolated to one full call; value the best step),
+with the same config object.
 """
 
 from __future__ import annotations
@@ -69,6 +79,16 @@ KERNEL_NAMES = {FD_KERNEL_SPLIT: "split_mma_kernel (mma.sync bf16, TMA ring)",
 # Cycles of torch.cuda._sleep per microsecond: the maximum SM clock of a
 # B300 (2032 MHz), rounded up, so a delay is at least as long as asked.
 SLEEP_CYCLES_PER_US = 2100
+
+
+def rotation_copies(per_copy_bytes):
+    """Input copies a timed loop rotates over so that no call finds its K/V
+    in L2: enough copies to cover twice the L2 size, plus one when a copy is
+    smaller than four times L2 (its tail may still be resident); at most 512
+    (a 512-token batch-1 layer is 2 MiB, so 127 copies)."""
+    n = math.ceil(2 * L2_BYTES / max(1, per_copy_bytes))
+    n += 1 if per_copy_bytes < 4 * L2_BYTES else 0
+    return max(1, min(512, n))
 
 # Source files each roofline kernel is built from: a DRAM-traffic figure in
 # profiles/traffic.json is used only while their code (comments and
@@ -146,7 +166,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50", "-i", str(self.gpu_id)],
+                 "-lms", "20", "-i", str(self.gpu_id)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -242,9 +262,8 @@ def _host_loop_us(stream, steps, step, warmup=5):
 class DecodeWorkload(Workload):
     dominant = FD_KERNEL_SPLIT
 
-    def __init__(self, short, builder, device):
+    def __init__(self, short, builder, device, copies=True):
         import torch
-        from decode_attention_20_b300 import inputs
         self.short = short
         self.case = builder(device)
         c = self.case
@@ -257,9 +276,10 @@ class DecodeWorkload(Workload):
         self.lens = c.lens
         self.seqlens_dev = c.seqlens.to(device) if c.seqlens is not None else None
         kv_bytes = c.k.numel() * c.k.element_size() * 2
-        self.nbuf = max(1, min(8, math.ceil(2 * L2_BYTES / kv_bytes) + (1 if kv_bytes < 4 * L2_BYTES else 0)))
-        self.ks = [c.k] + [c.k.clone() for _ in range(self.nbuf - 1)]
-        self.vs = [c.v] + [c.v.clone() for _ in range(self.nbuf - 1)]
+        self.nbuf = rotation_copies(kv_bytes)
+        extra = self.nbuf - 1 if copies else 0
+        self.ks = [c.k] + [c.k.clone() for _ in range(extra)]
+        self.vs = [c.v] + [c.v.clone() for _ in range(extra)]
         tok = (self.Tq,) if self.Tq > 1 else ()
         self.out = torch.empty((self.B,) + tok + (self.Hq, self.D), dtype=torch.float32, device=device)
         self.lse = torch.empty((self.B,) + tok + (self.Hq,), dtype=torch.float32, device=device)
@@ -348,33 +368,31 @@ class DecodeWorkload(Workload):
         import oracle
         oracle.decode_attention_ref(q, k[:, :T], v[:, :T], None, self.case.scale)
 
-    def oracle_sample(self, target_s):
-        """Time the oracle on the first T tokens of sequence 0 (all kv
-        heads), T sized for about target_s seconds (at least 64 tokens);
-        returns (us per full call extrapolated by tokens, sample text,
-        seconds of the sample)."""
+    def oracle_sample(self):
+        """Time the oracle once on a fixed sample: sequence 0's whole history
+        with all its kv heads (the whole call at batch 1).  Returns (us per
+        full call, extrapolated linearly by tokens when the batch holds more
+        than sequence 0; sample text; seconds of the sample).  The inputs'
+        float64 conversion is done once and not timed."""
+        T = max(self.lens[0], 1)
         if not hasattr(self, "_of"):
-            n0 = max(self.lens[0], 1)
-            self._of = self._oracle_inputs(n0)
-            q, k, v = self._of
-            T0 = min(n0, 2048)
-            t0 = time.perf_counter()
-            self._oracle_call(q, k, v, T0)
-            self._per_tok = (time.perf_counter() - t0) / T0
+            self._of = self._oracle_inputs(T)
         q, k, v = self._of
-        T = int(max(min(64, self.lens[0]), min(self.lens[0], target_s / self._per_tok)))
         t0 = time.perf_counter()
         self._oracle_call(q, k, v, T)
         dt = time.perf_counter() - t0
-        full = dt * (sum(self.lens) / T)
-        return full * 1e6, (f"sequence 0, first {T} tokens x all {self.Hkv} kv heads per call, "
-                            f"extrapolated linearly to {sum(self.lens)} tokens x {self.B} sequences"), dt
+        total = sum(self.lens)
+        full = dt * (total / T)
+        text = f"sequence 0: {T} tokens x all {self.Hkv} kv heads"
+        if total != T:
+            text += f", extrapolated linearly to {total} tokens x {self.B} sequences"
+        return full * 1e6, text, dt
 
 
 class BifWorkload(Workload):
     dominant = FD_KERNEL_BIF_CTX
 
-    def __init__(self, device):
+    def __init__(self, device, copies=True):
         import torch
         from decode_attention_20_b300 import inputs
         self.short = "bif_mqa"
@@ -385,10 +403,10 @@ class BifWorkload(Workload):
         self.Ld = c.k_dec.shape[1]
         self.dec_dev = c.dec_lens.to(device) if c.dec_lens is not None else None
         per_copy = sum(x.numel() * 2 for x in [c.k_ctx, c.v_ctx, c.k_dec, c.v_dec, c.q])
-        self.nbuf = max(1, math.ceil(2 * L2_BYTES / per_copy))
+        self.nbuf = rotation_copies(per_copy)
         self.bufs = [(c.q, c.k_ctx, c.v_ctx, c.k_dec, c.v_dec)] + [
             tuple(x.clone() for x in (c.q, c.k_ctx, c.v_ctx, c.k_dec, c.v_dec))
-            for _ in range(self.nbuf - 1)]
+            for _ in range(self.nbuf - 1 if copies else 0)]
         self.out = torch.empty((self.n, self.Hq, self.D), dtype=torch.float32, device=device)
         self.lse = torch.empty((self.n, self.Hq), dtype=torch.float32, device=device)
         kv_ctx = c.k_ctx.numel() * 2 * 2
@@ -493,37 +511,30 @@ class BifWorkload(Workload):
         d2h = hout.numel() * 4 + hlse.numel() * 4
         return us, h2d, d2h
 
-    def oracle_sample(self, target_s):
-        """Time the oracle on sample 0 with the first T context tokens (and
-        its own decode tokens), T sized for about target_s seconds (at least
-        64); returns (us per full call extrapolated by tokens and samples,
-        sample text, seconds of the sample)."""
+    def oracle_sample(self):
+        """Time the oracle once on a fixed sample: sample 0 over the whole
+        context and its own decode tokens.  Returns (us per full call,
+        extrapolated linearly to all samples; sample text; seconds)."""
         import oracle
         c = self.case
         lens = c.lens
         if not hasattr(self, "_of"):
             self._of = (f64(c.q[:1]), f64(c.k_ctx), f64(c.v_ctx), f64(c.k_dec[:1]), f64(c.v_dec[:1]))
-            q, kc, vc, kd, vd = self._of
-            T0 = min(self.Lc, 2048)
-            t0 = time.perf_counter()
-            oracle.bifurcated_attention_ref(q, kc[:T0], vc[:T0], kd, vd, [lens[0]], c.scale)
-            self._per_tok = (time.perf_counter() - t0) / (T0 + lens[0])
         q, kc, vc, kd, vd = self._of
-        T = int(max(64, min(self.Lc, target_s / self._per_tok - lens[0])))
         t0 = time.perf_counter()
-        oracle.bifurcated_attention_ref(q, kc[:T], vc[:T], kd, vd, [lens[0]], c.scale)
+        oracle.bifurcated_attention_ref(q, kc, vc, kd, vd, [lens[0]], c.scale)
         dt = time.perf_counter() - t0
         full_tokens = sum(self.Lc + x for x in lens)
-        return dt * full_tokens / (T + lens[0]) * 1e6, (
-            f"sample 0 with the first {T} of {self.Lc} context tokens and its {lens[0]} decode "
-            f"tokens per call, extrapolated linearly to {self.n} samples"), dt
+        return dt * full_tokens / (self.Lc + lens[0]) * 1e6, (
+            f"sample 0: {self.Lc} context tokens and its {lens[0]} decode tokens, "
+            f"extrapolated linearly to {self.n} samples"), dt
 
 
 class PagedWorkload(DecodeWorkload):
     """The batch-1 64K layer with its history in scattered 64-token pages
     (fd_decode_attention_paged)."""
 
-    def __init__(self, device):
+    def __init__(self, device, copies=True):
         import torch
         from decode_attention_20_b300 import inputs
         self.short = "paged_b1_64k"
@@ -537,9 +548,9 @@ class PagedWorkload(DecodeWorkload):
         self.seqlens_dev = None
         self.bt_dev = c.block_table.to(device)
         kv_bytes = c.k_pages.numel() * c.k_pages.element_size() * 2
-        self.nbuf = max(1, min(8, math.ceil(2 * L2_BYTES / kv_bytes) + (1 if kv_bytes < 4 * L2_BYTES else 0)))
-        self.ks = [c.k_pages] + [c.k_pages.clone() for _ in range(self.nbuf - 1)]
-        self.vs = [c.v_pages] + [c.v_pages.clone() for _ in range(self.nbuf - 1)]
+        self.nbuf = rotation_copies(kv_bytes)
+        self.ks = [c.k_pages] + [c.k_pages.clone() for _ in range(self.nbuf - 1 if copies else 0)]
+        self.vs = [c.v_pages] + [c.v_pages.clone() for _ in range(self.nbuf - 1 if copies else 0)]
         self.out = torch.empty((self.B, self.Hq, self.D), dtype=torch.float32, device=device)
         self.lse = torch.empty((self.B, self.Hq), dtype=torch.float32, device=device)
         self.kv_req = sum(self.lens) * self.Hkv * self.D * 2 * 2
@@ -615,9 +626,10 @@ class MultiWorkload(DecodeWorkload):
     """The batch-1 64K-token layer verifying Tq new tokens at once
     (fd_decode_attention_multi)."""
 
-    def __init__(self, short, tq, device):
+    def __init__(self, short, tq, device, copies=True):
         from decode_attention_20_b300 import inputs
-        super().__init__(short, lambda d: inputs.speculative_b1(65536, tq=tq, device=d), device)
+        super().__init__(short, lambda d: inputs.speculative_b1(65536, tq=tq, device=d), device,
+                         copies)
 
     def config(self, ns):
         cfg = super().config(ns)
@@ -650,10 +662,10 @@ class QuantWorkload(DecodeWorkload):
     dtype = "f16"
     kernel_name = "split_mma_kernel (mma.sync f16 over 8-bit codes, TMA ring)"
 
-    def __init__(self, short, kind, device):
+    def __init__(self, short, kind, device, copies=True):
         from decode_attention_20_b300 import inputs
         super().__init__(short, lambda d: inputs.quant_flash_decoding_b1(65536, kind=kind, device=d),
-                         device)
+                         device, copies)
         self.kind = kind
 
     def config(self, ns):
@@ -697,52 +709,108 @@ class QuantWorkload(DecodeWorkload):
                                           c.v_scale.cpu().numpy(), self.kind, None, c.scale)
 
 
-def make_workload(short, device):
+def make_workload(short, device, copies=True):
+    """The named workload on `device`; copies=False keeps one copy of the
+    inputs (the CPU oracle arm rotates nothing)."""
     from decode_attention_20_b300 import inputs
     if short == "b1_64k":
-        return DecodeWorkload(short, lambda d: inputs.flash_decoding_b1(65536, seed=0, device=d), device)
+        return DecodeWorkload(short, lambda d: inputs.flash_decoding_b1(65536, seed=0, device=d),
+                              device, copies)
+    if short.startswith("b1_L"):                      # the batch-1 layer at another length
+        L = int(short[4:])
+        return DecodeWorkload(short, lambda d: inputs.flash_decoding_b1(L, seed=0, device=d),
+                              device, copies)
+    if short == "tiny_fp32":
+        return DecodeWorkload(short, lambda d: inputs.tiny_mha(device=d), device, copies)
     if short == "ragged_b32":
-        return DecodeWorkload(short, lambda d: inputs.ragged_batch(device=d), device)
+        return DecodeWorkload(short, lambda d: inputs.ragged_batch(device=d), device, copies)
     if short == "long_b4":
-        return DecodeWorkload(short, lambda d: inputs.long_context_peaked(device=d), device)
+        return DecodeWorkload(short, lambda d: inputs.long_context_peaked(device=d), device, copies)
     if short == "bif_mqa":
-        return BifWorkload(device)
+        return BifWorkload(device, copies)
     if short == "paged_b1_64k":
-        return PagedWorkload(device)
+        return PagedWorkload(device, copies)
     if short == "verify4_b1_64k":
-        return MultiWorkload(short, 4, device)
+        return MultiWorkload(short, 4, device, copies)
     if short == "int8_b1_64k":
-        return QuantWorkload(short, "int8", device)
+        return QuantWorkload(short, "int8", device, copies)
     if short == "e4m3_b1_64k":
-        return QuantWorkload(short, "e4m3", device)
+        return QuantWorkload(short, "e4m3", device, copies)
     raise SystemExit(f"unknown workload {short}")
+
+
+# ------------------------------------------------------------------ shared pieces
+
+def num_sms_for_config():
+    """SM count the split heuristic is given: the visible GPU's, else a
+    B300's 148 (the CPU oracle arm may run where no GPU is visible)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return torch.cuda.get_device_properties(0).multi_processor_count
+    except Exception:
+        pass
+    return 148
+
+
+def line_config(w, ns, world):
+    """The `config` object of a line: the same in the GPU arm and the oracle
+    arm (workload shapes, split count, parallelism, L2 handling)."""
+    return dict(w.config(ns), parallelism="replicas" if world > 1 else "single",
+                l2=f"inputs larger than L2: {w.nbuf} rotating input copies")
+
+
+def workload_splits(w, num_sms):
+    """Split count the line reports: the library heuristic's for the decode
+    workloads (its host mirror in the oracle, equal bit for bit), 0 for the
+    bifurcated call (the library chooses its context splits itself)."""
+    import oracle
+    if isinstance(w, DecodeWorkload):
+        return int(oracle.choose_num_splits_ref(w.B, w.Hkv, w.Lcap, num_sms))
+    return 0
+
+
+def cpu_baseline(w, reps=3):
+    """Best of `reps` timings of the fp64 oracle on the workload's fixed
+    sample, on the host cores."""
+    best = None
+    sample = ""
+    for _ in range(reps):
+        us, sample, _dt = w.oracle_sample()
+        best = us if best is None else min(best, us)
+    return {"value": round(best, 1), "unit": "us/call", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{sample}; best of {reps}"}
 
 
 # ------------------------------------------------------------------ reference arm
 
-def run_reference(args, rank):
-    """--impl reference: the fp64 oracle on host cores, same workload."""
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 oracle on host cores, same workload and
+    config as the GPU arm; each step one timing of the fixed sample, value
+    the best step."""
     if rank != 0:
         return 0
-    w = make_workload(args.workload, "cpu")
-    budget = 100.0 / max(1, args.steps + args.warmup)
+    w = make_workload(args.workload, "cpu", copies=False)
+    ns = args.num_splits or workload_splits(w, num_sms_for_config())
     us = []
-    sample = ""
     step_s = []
+    sample = ""
     for i in range(args.warmup + args.steps):
-        u, sample, dt = w.oracle_sample(budget)
+        u, sample, dt = w.oracle_sample()
         if i >= args.warmup:
             us.append(u)
             step_s.append(dt)
-    value = statistics.median(us)
+    value = min(us)
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "us/call",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": statistics.median(step_s) * 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": w.config(args.num_splits),
+        "config": line_config(w, ns, world),
+        "timing": {"kind": "host wall clock of the fp64 oracle, one fixed sample per step",
+                   "reduction": f"best of {args.steps} steps"},
         "cpu_baseline": {"value": round(value, 1), "unit": "us/call", "cores": blas_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": f"{sample}; best of {args.steps}"},
         "e2e": {"value": round(value, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "achieved_gbs": round(w.required / (value * 1e-6) / 1e9, 3),
@@ -762,6 +830,194 @@ def max_over_ranks(vals, world):
         import torch.distributed as dist
         dist.all_reduce(vals, op=dist.ReduceOp.MAX)
     return vals
+
+
+def _events():
+    import torch
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def time_direct(w, stream, n):
+    """Device microseconds per call of n direct (not graph) calls issued back
+    to back on `stream`: host issue cost included where it exceeds the
+    device time."""
+    import torch
+    e0, e1 = _events()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(n):
+            w.call(i)
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / n
+
+
+def capture_calls(w, stream, ncalls):
+    """A CUDA graph of `ncalls` consecutive calls over the rotating input
+    copies, replayed once; None where capture fails."""
+    import torch
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(ncalls):
+                w.call(i)
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+    except Exception:
+        torch.cuda.synchronize()
+        return None
+
+
+def time_steps(w, stream, steps, warmup, window_s, barrier=None, sampler=None):
+    """Exactly `steps` timed steps after `warmup` untimed ones.  A step is
+    one replay of a CUDA graph of C back-to-back calls over the rotating
+    input copies (C a multiple of the copies, sized so that the steps span
+    about `window_s` seconds); CUDA events on the launching stream bracket
+    the steps, with a barrier and a device synchronise on both sides.
+    Returns microseconds per call, C, milliseconds per step, the timing
+    description and the clocks sampled during the steps."""
+    import torch
+    est = time_direct(w, stream, max(w.nbuf, 8))
+    cps = max(16, math.ceil(window_s * 1e6 / (steps * max(est, 1e-3))))
+    cps = min(max(w.nbuf, 4096), w.nbuf * math.ceil(cps / w.nbuf))
+    g = capture_calls(w, stream, cps)
+    if g is not None:
+        timing = f"each step one replay of a CUDA graph of {cps} calls"
+
+        def run():
+            g.replay()
+    else:
+        timing = f"each step {cps} direct calls (graph capture failed)"
+
+        def run():
+            for i in range(cps):
+                w.call(i)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            run()
+    stream.synchronize()
+    if sampler is not None:
+        sampler.start()
+    if barrier is not None:
+        barrier()
+    torch.cuda.synchronize()
+    e0, e1 = _events()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            run()
+        e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    if barrier is not None:
+        barrier()
+    clk = sampler.stop() if sampler is not None else None
+    ms = e0.elapsed_time(e1)
+    del g
+    return {"us_per_call": ms * 1e3 / (steps * cps), "calls_per_step": cps,
+            "ms_per_step": ms / steps, "timing": timing, "clocks": clk}
+
+
+KERNEL_LABELS = [(FD_KERNEL_SPLIT, "split"), (FD_KERNEL_COMBINE, "combine"),
+                 (FD_KERNEL_BIF_CTX, "bif_ctx")]
+
+
+def kernel_times(w, stream, n, us_direct):
+    """Per-kernel device time of n calls: CUDA events around each launch on
+    its stream (the library's timing hooks).  The calls are queued behind a
+    device-side delay longer than the host takes to issue them, so the GPU
+    runs them back to back and each event pair brackets its kernel, not the
+    host's time to issue the next call.  Returns {label_us,
+    label_launches_per_call} and the launches per call."""
+    import torch
+    import decode_attention_20_b300 as fd
+    delay_us = 2.0 * n * us_direct + 5000.0
+    fd.profile_enable(True)
+    sleep = getattr(torch.cuda, "_sleep", None)       # a device-side spin of N clock cycles
+    with torch.cuda.stream(stream):
+        if sleep is not None:
+            sleep(int(delay_us * SLEEP_CYCLES_PER_US))
+        for i in range(n):
+            w.call(i)
+    stream.synchronize()
+    kern = {}
+    launches = 0
+    for kind, label in KERNEL_LABELS:
+        cnt, ms = fd.profile_read(kind)
+        launches += cnt
+        if cnt:
+            kern[label + "_us"] = round(ms * 1e3 / cnt, 3)
+            kern[label + "_launches_per_call"] = cnt / n
+    fd.profile_enable(False)
+    return kern, launches / n
+
+
+def dominant_roofline(w, dom_us, peaks):
+    """(achieved, peak, per-launch units) of the workload's dominant kernel."""
+    if w.bound == "hbm":
+        return w.dominant_units / (dom_us * 1e-6) / 1e9, peaks["hbm_gbs"], int(w.dominant_units)
+    return w.dominant_units / (dom_us * 1e-6) / 1e12, peaks["bf16_tflops"], w.dominant_units
+
+
+def measure_config(short, dev, stream, L, peaks, window_s=0.15, ns=0):
+    """One BASELINE workload measured the way the headline is (graph steps
+    over rotating copies, direct calls, per-kernel events), as a compact
+    record for the line's `configs` object."""
+    import torch
+    import decode_attention_20_b300 as fd
+    w = make_workload(short, dev)
+    if isinstance(w, DecodeWorkload) and ns == 0:
+        ns = fd.choose_num_splits(w.B, w.Hkv, w.Lcap,
+                                  torch.cuda.get_device_properties(dev).multi_processor_count)
+    w.prepare(L, stream, ns)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            w.call(i)
+    stream.synchronize()
+    fd.check_device_error(stream)
+    t = time_steps(w, stream, 5, 2, window_s)
+    us_direct = time_direct(w, stream, max(32, min(500, w.nbuf * 2)))
+    kern, _ = kernel_times(w, stream, 64, us_direct)
+    dom_label = {FD_KERNEL_SPLIT: "split", FD_KERNEL_BIF_CTX: "bif_ctx"}[w.dominant]
+    dom_us = kern[dom_label + "_us"]
+    achieved, peak, _ = dominant_roofline(w, dom_us, peaks)
+    gbs = w.required / (t["us_per_call"] * 1e-6) / 1e9
+    rec = {"workload": w.name, "num_splits": ns, "us": round(t["us_per_call"], 3),
+           "direct_us": round(us_direct, 3), "required_bytes": int(w.required),
+           "achieved_gbs": round(gbs, 1), "frac_of_nominal_8tbs": round(gbs / 8000.0, 4),
+           "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+           "dominant_kernel_us": dom_us, "dominant_achieved": round(achieved, 1),
+           "dominant_unit": w.unit, "dominant_frac": round(achieved / peak, 4),
+           "rotating_copies": w.nbuf}
+    if isinstance(w, BifWorkload):
+        rep = DecodeWorkload("bif_replicated", lambda d: _replicated_case(w), dev)
+        rns = fd.choose_num_splits(rep.B, rep.Hkv, rep.Lcap,
+                                   torch.cuda.get_device_properties(dev).multi_processor_count)
+        rep.prepare(L, stream, rns)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                rep.call(i)
+        stream.synchronize()
+        rt = time_steps(rep, stream, 5, 2, window_s)
+        rec["replicated_context_us"] = round(rt["us_per_call"], 3)
+        rec["speedup_vs_replicated"] = round(rt["us_per_call"] / t["us_per_call"], 3)
+        kv_bif = w.case.k_ctx.numel() * 4 + sum(w.case.lens) * w.Hkv * w.D * 4
+        rec["kv_byte_ratio_replicated_over_bifurcated"] = round(rep.kv_req / kv_bif, 3)
+        rec["h_over_g"] = w.Hq // w.Hkv
+        del rep
+    fd.check_device_error(stream)
+    del w
+    torch.cuda.empty_cache()
+    return rec
+
+
+def _replicated_case(w):
+    from decode_attention_20_b300 import inputs
+    return inputs.replicate_context(w.case)
+
+
+SWEEP_LENGTHS = [512, 1024, 2048, 4096, 8192, 16384, 32768]
 
 
 def run_fd(args, rank, world):
@@ -789,134 +1045,81 @@ def run_fd(args, rank, world):
     warm = max(3, args.warmup)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        for i in range(warm):
+        for i in range(max(warm, w.nbuf)):
             w.call(i)
     stream.synchronize()
     fd.check_device_error(stream)
 
-    # CUDA graph of nbuf consecutive calls (one per rotating input copy)
-    # One graph holds at least 16 back-to-back calls (cycling the rotating
-    # input copies), so graph-launch boundaries, which break the
-    # programmatic overlap of consecutive calls, are rare.
-    glen = w.nbuf * max(1, math.ceil(16 / w.nbuf))
-    reps = max(1, math.ceil(args.steps / glen))
-    steps = reps * glen
-    graph = None
-    timing = f"CUDA graph of {glen} calls, replayed"
-    try:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(glen):
-                w.call(i)
-        for _ in range(2):
-            g.replay()
-        torch.cuda.synchronize()
-        graph = g
-    except Exception as ex:  # capture unsupported: time direct calls instead
-        timing = f"direct calls (graph capture failed: {type(ex).__name__})"
-        torch.cuda.synchronize()
-
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     gpu_id = vis.split(",")[dev.index] if vis else str(dev.index)
-    clocks = ClockSampler(gpu_id)
-    clocks.start()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        if graph is not None:
-            for _ in range(reps):
-                graph.replay()
-        else:
-            for i in range(steps):
-                w.call(i)
-        e1.record(stream)
-    stream.synchronize()
-    torch.cuda.synchronize()
-    barrier()
-    clk = clocks.stop()
-    us_per_call = e0.elapsed_time(e1) * 1e3 / steps
-    del graph
+    t = time_steps(w, stream, args.steps, warm, args.window_ms / 1e3, barrier=barrier,
+                   sampler=ClockSampler(gpu_id))
+    us_per_call, clk = t["us_per_call"], t["clocks"]
 
-    # Direct API calls (no graph), same rotation: launch overhead included.
-    dsteps = min(steps, 2000)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(dsteps):
-            w.call(i)
-        e1.record(stream)
-    stream.synchronize()
-    us_direct = e0.elapsed_time(e1) * 1e3 / dsteps
+    # Direct calls (no graph), same rotation: launch overhead included.
+    dsteps = max(w.nbuf, min(t["calls_per_step"] * args.steps, 2000))
+    us_direct = time_direct(w, stream, dsteps)
 
-    # Per-kernel durations (CUDA events around each launch on its stream).
-    # The calls are queued behind a device-side delay longer than the host
-    # takes to issue them, so the GPU runs them back to back and each event
-    # pair brackets its kernel, not the host's time to issue the next call
-    # (short calls are host-bound when issued one by one).
-    psteps = min(dsteps, 128)
-    delay_us = 2.0 * psteps * us_direct + 5000.0
-    fd.profile_enable(True)
-    sleep = getattr(torch.cuda, "_sleep", None)       # a device-side spin of N clock cycles
-    with torch.cuda.stream(stream):
-        if sleep is not None:
-            sleep(int(delay_us * SLEEP_CYCLES_PER_US))
-        for i in range(psteps):
-            w.call(i)
-    stream.synchronize()
-    kern = {}
-    launches = 0
-    for kind, label in [(FD_KERNEL_SPLIT, "split"), (FD_KERNEL_COMBINE, "combine"),
-                        (FD_KERNEL_BIF_CTX, "bif_ctx")]:
-        n, ms = fd.profile_read(kind)
-        launches += n
-        if n:
-            kern[label + "_us"] = round(ms * 1e3 / n, 3)
-            kern[label + "_launches_per_call"] = n / psteps
-    fd.profile_enable(False)
-    launches_per_call = launches / psteps
+    kern, launches_per_call = kernel_times(w, stream, min(dsteps, 128), us_direct)
     dom_label = {FD_KERNEL_SPLIT: "split", FD_KERNEL_BIF_CTX: "bif_ctx"}[w.dominant]
     dom_us = kern[dom_label + "_us"]
 
     extra = {}
     if isinstance(w, BifWorkload):
-        rep_us, rep_kv = w.replicated_us(stream, min(steps, 400), 0)
-        extra["replicated_context_us"] = round(rep_us, 3)
-        extra["speedup_vs_replicated"] = round(rep_us / us_per_call, 3)
+        rep = DecodeWorkload("bif_replicated", lambda d: _replicated_case(w), dev)
+        rns = fd.choose_num_splits(rep.B, rep.Hkv, rep.Lcap, props.multi_processor_count)
+        rep.prepare(L, stream, rns)
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                rep.call(i)
+        stream.synchronize()
+        rt = time_steps(rep, stream, 5, 2, 0.15)
+        extra["replicated_context_us"] = round(rt["us_per_call"], 3)
+        extra["speedup_vs_replicated"] = round(rt["us_per_call"] / us_per_call, 3)
         kv_bif = w.case.k_ctx.numel() * 4 + sum(w.case.lens) * w.Hkv * w.D * 4
-        extra["kv_byte_ratio_replicated_over_bifurcated"] = round(rep_kv / kv_bif, 3)
+        extra["kv_byte_ratio_replicated_over_bifurcated"] = round(rep.kv_req / kv_bif, 3)
         extra["h_over_g"] = w.Hq // w.Hkv
+        del rep
+        torch.cuda.empty_cache()
 
-    e2e_us, h2d, d2h = w.e2e(stream, max(1, min(steps, 1000)))
+    e2e_us, h2d, d2h = w.e2e(stream, max(1, min(t["calls_per_step"] * args.steps, 1000)))
     fd.check_device_error(stream)
 
     vals = torch.tensor([us_per_call, e2e_us, dom_us], dtype=torch.float64, device=dev)
     vals = max_over_ranks(vals, world)
     us_per_call, e2e_us, dom_us = [float(x) for x in vals.tolist()]
+
+    # The other BASELINE workloads and the batch-1 length sweep, measured the
+    # same way (rank 0 of a single-GPU run, default workload only).
+    configs = {}
+    if world == 1 and args.workload == "b1_64k" and not args.no_configs:
+        peaks = load_peaks()
+        configs["tiny_fp32_mha_L256"] = {}
+        for tns in (1, 4):
+            configs["tiny_fp32_mha_L256"][f"ns{tns}"] = measure_config(
+                "tiny_fp32", dev, stream, L, peaks, 0.05, ns=tns)
+        configs["flash_decoding_b1_sweep"] = {
+            str(n): measure_config(f"b1_L{n}", dev, stream, L, peaks, 0.1) for n in SWEEP_LENGTHS}
+        configs["ragged_b32"] = measure_config("ragged_b32", dev, stream, L, peaks, 0.3)
+        configs["bifurcated_mqa"] = measure_config("bif_mqa", dev, stream, L, peaks, 0.15)
+        configs["long_b4_peaked"] = measure_config("long_b4", dev, stream, L, peaks, 0.3)
     if rank != 0:
         return 0
 
     peaks = load_peaks()
     gbs = w.required / (us_per_call * 1e-6) / 1e9 * world
-    if w.bound == "hbm":
-        achieved = w.dominant_units / (dom_us * 1e-6) / 1e9
-        peak = peaks["hbm_gbs"]
-        per_launch = int(w.dominant_units)
-    else:
-        achieved = w.dominant_units / (dom_us * 1e-6) / 1e12
-        peak = peaks["bf16_tflops"]
-        per_launch = w.dominant_units
+    achieved, peak, per_launch = dominant_roofline(w, dom_us, peaks)
     line = {
         "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call",
-        "n_gpus": world, "steps": steps, "warmup": warm,
-        "ms_per_step": us_per_call / 1e3, "higher_is_better": False,
+        "n_gpus": world, "steps": args.steps, "warmup": warm,
+        "ms_per_step": t["ms_per_step"], "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": getattr(w, "dtype", "bf16"),
         "data": "synthetic",
-        "config": dict(w.config(ns), parallelism="replicas" if world > 1 else "single",
-                       l2=f"inputs larger than L2: {w.nbuf} rotating input copies",
-                       timing=timing),
+        "config": line_config(w, ns, world),
+        "timing": {"step": t["timing"], "calls_per_step": t["calls_per_step"],
+                   "calls_timed": t["calls_per_step"] * args.steps,
+                   "window_ms": round(t["ms_per_step"] * args.steps, 3),
+                   "value": "device microseconds per call, CUDA events around the steps"},
         "achieved_gbs": round(gbs, 1),
         "frac_of_nominal_8tbs": round(gbs / world / 8000.0, 4),
         "frac_of_measured_hbm": round(gbs / world / peaks["hbm_gbs"], 4),
@@ -932,14 +1135,13 @@ def run_fd(args, rank, world):
                    "reasons": clk["reasons"], "samples": clk["samples"]},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/call", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": int(round(launches_per_call * steps)),
+        "gpu_launches": int(round(launches_per_call * t["calls_per_step"] * args.steps)),
     }
     line.update(extra)
+    if configs:
+        line["configs"] = configs
     if world == 1 and not args.no_cpu_baseline:
-        import torch as _t
-        u, sample, dt = w.oracle_sample(args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(u, 1), "unit": "us/call", "cores": blas_threads(),
-                                "kind": "oracle", "sample": sample}
+        line["cpu_baseline"] = cpu_baseline(w, 3)
     print(json.dumps(line), flush=True)
     return 0
 
@@ -1056,14 +1258,17 @@ def run_bif_sweep(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--window-ms", type=float, default=400.0,
+                    help="device time the timed steps should span (sets the calls per step)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other BASELINE workloads and the length sweep in the line")
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="b1_64k",
                     choices=["b1_64k", "ragged_b32", "long_b4", "bif_mqa", "paged_b1_64k",
                              "int8_b1_64k", "e4m3_b1_64k", "verify4_b1_64k"])
     ap.add_argument("--num-splits", type=int, default=0)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep-splits", default="",
                     help="comma-separated split counts: print one timing line per count instead")
@@ -1079,7 +1284,7 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
-        return run_reference(args, rank)
+        return run_reference(args, rank, world)
     if world > 1:
         import torch
         import torch.distributed as dist

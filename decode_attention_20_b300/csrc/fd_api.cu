@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -342,6 +343,25 @@ int split_variant(int64_t chunk_tokens) {
   return 0;
 }
 
+// Test knobs of the bounded-wait error path, read on every call:
+// FD_TEST_WAIT_LIMIT_NS shortens the tensor-core split kernel's pipeline
+// waits (1 ns .. 1 s) and FD_TEST_PRODUCER_DELAY_NS makes its producer spin
+// that long (at most kMaxProducerDelayNs) before its first copies, so a test
+// can make a wait run out on a small, complete problem.  Unset: the 1 s limit
+// and no delay.
+void test_wait_knobs(unsigned long long* limit_ns, unsigned int* delay_ns) {
+  *limit_ns = kWaitLimitNs;
+  *delay_ns = 0u;
+  if (const char* e = getenv("FD_TEST_WAIT_LIMIT_NS")) {
+    const long long v = atoll(e);
+    if (v > 0) *limit_ns = (unsigned long long)std::min<long long>(v, (long long)kWaitLimitNs);
+  }
+  if (const char* e = getenv("FD_TEST_PRODUCER_DELAY_NS")) {
+    const long long v = atoll(e);
+    if (v > 0) *delay_ns = (unsigned int)std::min<long long>(v, (long long)kMaxProducerDelayNs);
+  }
+}
+
 bool mma_group_ok(int64_t G) { return G == 4 || G == 8 || G == 16 || G == 32 || G == 64; }
 
 // Split-count heuristic: the smallest ns with the lowest makespan
@@ -392,6 +412,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
                         int64_t l_st = 0, bool late_wait = false) {
   SplitParams p = {};
   p.late_wait = late_wait ? 1 : 0;
+  test_wait_knobs(&p.wait_limit_ns, &p.producer_delay_ns);
   if (pg) {
     p.block_table = pg->table;
     p.bt_stride = pg->stride;
@@ -943,7 +964,13 @@ fd_status fd_decode_attention_noalloc(const fd_tensor* q, const fd_tensor* k_cac
   if ((st = noalloc_setup(&dev))) return st;
   if (d.B == 0 || d.Hq == 0) return FD_OK;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const int ns = num_splits > 0 ? num_splits : choose_splits_host(d.B, d.Hkv, d.Lcap, dev->sms);
+  int ns = num_splits;
+  if (ns == 0) {
+    // The library's own choice never exceeds the scratch: the heuristic's
+    // count, lowered to the largest that fits (one split needs no scratch).
+    ns = choose_splits_host(d.B, d.Hkv, d.Lcap, dev->sms);
+    while (ns > 1 && workspace_bytes(d.B, d.Hq, d.D, ns) > (int64_t)FD_NOALLOC_SCRATCH_BYTES) --ns;
+  }
   const int32_t* sl = seqlens ? reinterpret_cast<const int32_t*>(seqlens->data) : nullptr;
   float* o = reinterpret_cast<float*>(out->data);
   float* l = lse ? reinterpret_cast<float*>(lse->data) : nullptr;

@@ -88,14 +88,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // As mbar_wait_bounded, but also gives up at once when another thread of the
 // CTA has set *abort_flag (after its own wait ran out), and sets it itself on
 // a timeout, so one stalled copy does not cost every later wait a full limit.
+// `limit_ns` is kWaitLimitNs except where a caller passes a shorter limit.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity,
-                                                   int* abort_flag) {
+                                                   int* abort_flag,
+                                                   uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*reinterpret_cast<volatile int*>(abort_flag)) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       raise_device_error(FD_DEVERR_TIMEOUT);
       *reinterpret_cast<volatile int*>(abort_flag) = 1;
       return false;

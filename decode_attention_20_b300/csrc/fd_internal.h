@@ -66,7 +66,17 @@ struct SplitParams {
   const int32_t* block_table;
   int64_t bt_stride;
   int page_size, num_pages, page_rows;
+  // Limit of the tensor-core split kernel's pipeline waits (its final drain
+  // of copies in flight always allows kWaitLimitNs), and a delay its
+  // producer thread spins before issuing its first copies: kWaitLimitNs and
+  // 0 except under the test knobs that make a wait run out on purpose
+  // (FD_TEST_WAIT_LIMIT_NS, FD_TEST_PRODUCER_DELAY_NS).
+  unsigned long long wait_limit_ns;
+  unsigned int producer_delay_ns;
 };
+
+// Longest producer delay the test knob may ask for (10 ms).
+constexpr unsigned int kMaxProducerDelayNs = 10000000u;
 
 // Arguments of the log-sum-exp combine kernel.
 struct CombineParams {

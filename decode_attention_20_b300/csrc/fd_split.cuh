@@ -47,9 +47,12 @@ constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Device copy of the split partition; must equal fd_split_bounds().
+// Computed in 64 bits: len may come within a few tokens of INT32_MAX (a
+// paged cache's capacity needs no memory behind it), where len + ns - 1
+// would overflow an int.
 __device__ __forceinline__ void split_range(int len, int ns, int i, int& begin, int& end) {
-  const int per = (len + ns - 1) / ns;
-  const long long chunk = (long long)((per + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
+  const long long per = ((long long)len + ns - 1) / ns;
+  const long long chunk = ((per + kSplitAlign - 1) / kSplitAlign) * kSplitAlign;
   const long long b0 = (long long)i * chunk;
   begin = (int)(b0 < len ? b0 : len);
   end = (int)(b0 + chunk < len ? b0 + chunk : len);

@@ -307,7 +307,9 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
       }
     }
   };
-  if (threadIdx.x == 0) {
+  // Thread 0 fills the ring.  (A test delay moves the fill after the query
+  // staging and spins first, so that the other warps' first waits run out.)
+  auto fill_ring = [&]() {
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     policy = l2_policy_evict_first();
@@ -315,7 +317,8 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
       issue(t);
       ++issued;
     }
-  }
+  };
+  if (threadIdx.x == 0 && p.producer_delay_ns == 0) fill_ring();
 
   // ---- raw query values (fp32 bit patterns), turned into MMA fragments below.
   uint32_t qraw[NPW][8][4];
@@ -473,9 +476,19 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     limB[j] = len - TQ + min(rA + 1, R - 1) / G + 1;
   }
 
+  if (threadIdx.x == 0 && p.producer_delay_ns != 0) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < p.producer_delay_ns) {
+    }
+    fill_ring();
+  }
+
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % C::NSTAGE;
-    if (!mbar_wait_or_abort(&full_bar[s], (t / C::NSTAGE) & 1, abort_s)) break;
+    // Warp-uniform: a lane must not run on into the warp-wide MMAs and
+    // shuffles of a tile that another lane of its warp has given up on.
+    const bool got = mbar_wait_or_abort(&full_bar[s], (t / C::NSTAGE) & 1, abort_s, p.wait_limit_ns);
+    if (!__all_sync(0xffffffffu, got)) break;
     const uint32_t kbase = smem_u32(smem + s * C::STAGE_BYTES);
     const uint32_t vbase = kbase + (C::Q8 ? 1 : 2) * C::HALF_BYTES;   // V box(es) after K
     const int nvalid = min(C::T, end - (begin + t * C::T));
@@ -681,7 +694,8 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     if (lane == 0) mbar_arrive(&empty_bar[s]);
     if (threadIdx.x == 0 && t >= 1 && issued < ntiles) {
       const int tp = t - 1;
-      if (mbar_wait_or_abort(&empty_bar[tp % C::NSTAGE], (tp / C::NSTAGE) & 1, abort_s)) {
+      if (mbar_wait_or_abort(&empty_bar[tp % C::NSTAGE], (tp / C::NSTAGE) & 1, abort_s,
+                             p.wait_limit_ns)) {
         issue(issued);
         ++issued;
       }

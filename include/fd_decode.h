@@ -215,10 +215,13 @@ FD_API fd_status fd_decode_attention_paged(const fd_tensor* q, const fd_tensor* 
  * array of FD_NOALLOC_SCRATCH_BYTES bytes instead of stream-ordered
  * workspace.  That array exists on every GPU that loads the library, for the
  * life of the process.
- *   - Calls whose partial results would not fit (fd_workspace_bytes(B, Hq,
- *     D, ns) > FD_NOALLOC_SCRATCH_BYTES, ns being num_splits or the
- *     heuristic's choice) return FD_ERR_UNSUPPORTED and enqueue nothing; pass
- *     a smaller num_splits or use fd_decode_attention.
+ *   - num_splits = 0: the heuristic's split count, lowered where needed to
+ *     the largest count whose partial results fit the array, so the
+ *     library's own choice is never refused.
+ *   - An explicit num_splits whose partial results would not fit
+ *     (fd_workspace_bytes(B, Hq, D, num_splits) > FD_NOALLOC_SCRATCH_BYTES)
+ *     returns FD_ERR_UNSUPPORTED and enqueues nothing; pass a smaller
+ *     num_splits or use fd_decode_attention.
  *   - All calls on a device share the one array: two calls whose work
  *     overlaps on the GPU (different streams, no ordering between them) race
  *     and may return wrong results.  Order them on one stream or with events.

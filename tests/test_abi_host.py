@@ -68,6 +68,24 @@ def test_split_bounds_bit_exact_vs_oracle(L):
                 assert (b, e) == oracle.split_bounds_ref(length, ns, i), (length, ns, i)
 
 
+def test_split_bounds_at_the_largest_accepted_length(L):
+    """The largest cache length the entry points accept (INT32_MAX - 128),
+    where len + ns - 1 no longer fits a 32-bit int: the host partition (and
+    the device copy, computed in 64 bits the same way) still covers [0, len)
+    exactly, in order, with the oracle's bounds."""
+    top = (1 << 31) - 1 - 128
+    for length in [top, top - 1, top - 63, (1 << 31) - 1 - 255]:
+        for ns in [2, 3, 37, 255, 256]:
+            prev = 0
+            for i in range(ns):
+                st, b, e = _bounds(L, length, ns, i)
+                assert st == 0
+                assert (b, e) == oracle.split_bounds_ref(length, ns, i)
+                assert b == prev and b <= e <= length
+                prev = e
+            assert prev == length
+
+
 def test_split_bounds_errors(L):
     for args in [(10, 0, 0), (10, 2, 2), (10, 2, -1), (-1, 2, 0)]:
         st, b, e = _bounds(L, *args)

@@ -159,6 +159,35 @@ def test_strided_q_and_out(cuda_device):
     assert torch.all(lse_big[:, :4] == 7.0) and torch.all(lse_big[:, 20:] == 7.0)
 
 
+def test_bounded_wait_running_out_is_reported_and_the_context_survives(cuda_device, monkeypatch):
+    """The bounded-wait error path of the tensor-core split kernel.  Under
+    the test knobs its producer thread spins 200 us before issuing its first
+    copies while every other thread may wait only 1 us for them, so those
+    waits run out: the kernel sets the device error word, drains the copies
+    it issued (those waits keep the full limit), writes empty partials and
+    returns.  Nothing faults and nothing is left waiting; the host reads
+    FD_ERR_DEVICE_TIMEOUT, and the next call without the knobs matches the
+    oracle."""
+    case = inputs.decode_case(1, 8, 1, 128, 4096, seed=19)
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    monkeypatch.delenv("FD_SPLIT_VARIANT", raising=False)
+    fd.check_device_error()                              # start clean
+    monkeypatch.setenv("FD_TEST_WAIT_LIMIT_NS", "1000")
+    monkeypatch.setenv("FD_TEST_PRODUCER_DELAY_NS", "200000")
+    fd.decode_attention(q, k, v, None, 4, case.scale)
+    with pytest.raises(FdError) as ei:
+        fd.check_device_error()
+    assert ei.value.status_name == "FD_ERR_DEVICE_TIMEOUT"
+    monkeypatch.delenv("FD_TEST_WAIT_LIMIT_NS")
+    monkeypatch.delenv("FD_TEST_PRODUCER_DELAY_NS")
+    fd.check_device_error()                              # the word was cleared
+    O, L = fd.decode_attention(q, k, v, None, 4, case.scale)
+    fd.check_device_error()
+    O_ref, L_ref = oracle.decode_attention_ref(to_f64(case.q), to_f64(case.k), to_f64(case.v),
+                                               None, case.scale)
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16, "after the timeout")
+
+
 def test_out_of_range_seqlens_are_clamped_and_flagged(cuda_device):
     case = inputs.decode_case(3, 8, 1, 128, 150, seed=18)
     sl = torch.tensor([-5, 10 ** 6, 40], dtype=torch.int32)

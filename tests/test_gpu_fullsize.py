@@ -35,6 +35,8 @@ def test_flash_decoding_b1_64k_full(cuda_device):
 
 
 def test_ragged_batch_full_size_sampled(cuda_device):
+    """Every kv head of the shortest, median and longest sequences, and of
+    two fixed ones, in the benchmark's launch configuration."""
     case = inputs.ragged_batch(device="cuda")
     lens = case.lens
     O, L = fd.decode_attention(case.q, case.k, case.v, case.seqlens.cuda(), 0, case.scale)
@@ -43,20 +45,34 @@ def test_ragged_batch_full_size_sampled(cuda_device):
     order = np.argsort(lens)
     picks = sorted({int(order[0]), int(order[-1]), int(order[len(order) // 2]), 5, 17})
     for b in picks:
-        for g in [0, 3, 7]:
+        for g in range(case.k.shape[2]):
             O_ref, L_ref = _slice_ref(case, b, g, lens)
             assert_parity(to_f64(O[b:b + 1, g * G:(g + 1) * G]), to_f64(L[b:b + 1, g * G:(g + 1) * G]),
                           O_ref, L_ref, torch.bfloat16, f"ragged b={b} g={g} len={lens[b]}")
 
 
+_LONG = {}
+
+
+def _long_case_and_refs():
+    """The long peaked workload and the oracle of all its 4 x 8 (sequence,
+    kv head) slices, computed once for the parametrised tests below."""
+    if "case" not in _LONG:
+        case = inputs.long_context_peaked(device="cuda")
+        lens = case.lens
+        refs = {(b, g): _slice_ref(case, b, g, lens)
+                for b in range(case.k.shape[0]) for g in range(case.k.shape[2])}
+        _LONG["case"], _LONG["refs"] = case, refs
+    return _LONG["case"], _LONG["refs"]
+
+
 @pytest.mark.parametrize("ns", [0, 1, 64, 256])
-def test_long_context_peaked_sampled(cuda_device, ns):
-    case = inputs.long_context_peaked(device="cuda")
-    lens = case.lens
+def test_long_context_peaked_every_slice(cuda_device, ns):
+    """All 32 (sequence, kv head) slices of the 4 x 131072 peaked workload."""
+    case, refs = _long_case_and_refs()
     O, L = fd.decode_attention(case.q, case.k, case.v, None, ns, case.scale)
     fd.check_device_error()
     G = case.q.shape[1] // case.k.shape[2]
-    for b, g in [(0, 0), (1, 5), (2, 2), (3, 7)]:
-        O_ref, L_ref = _slice_ref(case, b, g, lens)
+    for (b, g), (O_ref, L_ref) in refs.items():
         assert_parity(to_f64(O[b:b + 1, g * G:(g + 1) * G]), to_f64(L[b:b + 1, g * G:(g + 1) * G]),
                       O_ref, L_ref, torch.bfloat16, f"long b={b} g={g} ns={ns}")

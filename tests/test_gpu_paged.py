@@ -73,11 +73,18 @@ def test_paged_shared_prefix_and_empty(cuda_device):
         _check(case, ns, f"shared prefix ns={ns}")
 
 
-def test_paged_batch1_64k_matches_contiguous(cuda_device):
-    """The benchmark's paged layer: scattered 64-token pages give the same
-    result as the contiguous cache holding the same tokens."""
+def test_paged_batch1_64k_matches_oracle_and_contiguous(cuda_device):
+    """The benchmark's paged layer, in the benchmark's launch configuration
+    (heuristic split count): every output against the fp64 paged oracle;
+    and, as a second property, scattered 64-token pages give the same result
+    as the contiguous cache holding the same tokens."""
     case = inputs.paged_flash_decoding_b1(65536, 64, device="cuda")
     O, L = _run(case)
+    O_ref, L_ref = oracle.paged_decode_attention_ref(to_f64(case.q), to_f64(case.k_pages),
+                                                     to_f64(case.v_pages),
+                                                     case.block_table.cpu().numpy(), None,
+                                                     case.page_size, case.scale)
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16, "paged b1 64K vs oracle")
     kc = case.k_pages[case.block_table.cuda().long()].reshape(1, 65536, 8, 128)
     vc = case.v_pages[case.block_table.cuda().long()].reshape(1, 65536, 8, 128)
     O2, L2 = fd.decode_attention(case.q, kc, vc, None, 0, case.scale)

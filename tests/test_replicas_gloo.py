@@ -65,8 +65,40 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     sys.path.insert(0, ROOT)
     import bench
     args = bench.argparse.Namespace(workload="b1_64k", steps=1, warmup=0, gpus=2, num_splits=0)
-    assert bench.run_reference(args, rank=1) == 0
+    assert bench.run_reference(args, rank=1, world=2) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_gpu_arm_config(capsys):
+    """The oracle arm's `config` is the object the GPU arm prints for the same
+    workload: the library heuristic's split count (its oracle mirror), the
+    same rotating-copy count, parallelism and L2 note; its cpu_baseline is the
+    best step over the same fixed sample."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    from decode_attention_20_b300 import _lib
+    args = bench.argparse.Namespace(workload="tiny_fp32", steps=2, warmup=1, gpus=1, num_splits=0)
+    assert bench.run_reference(args, rank=0, world=1) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = bench.make_workload("tiny_fp32", "cpu")          # as the GPU arm builds it (with copies)
+    ns = _lib.lib().fd_choose_num_splits(w.B, w.Hkv, w.Lcap, bench.num_sms_for_config())
+    assert line["config"] == bench.line_config(w, ns, 1)
+    assert line["steps"] == 2 and line["impl"] == "reference"
+    assert line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "us/call", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_rotation_copies_exceed_l2():
+    """Rotating input copies always span more than twice L2 (up to the cap),
+    so a timed call never finds its K/V resident."""
+    sys.path.insert(0, ROOT)
+    import bench
+    for per_copy in [1 << 20, 2 << 20, 50 << 20, 126 << 20, 268 << 20, 2 << 30]:
+        n = bench.rotation_copies(per_copy)
+        assert n * per_copy > 2 * bench.L2_BYTES or n == 512
+        assert n >= 1
 
 
 def test_traffic_hash_ignores_comments_not_code():

@@ -1,9 +1,9 @@
 """GPU test of fd_decode_attention_noalloc, the entry point for callers that
 cannot allocate device memory while they run (a runtime that owns all device
 memory, a region where no pool may grow, a loop that cannot risk an
-allocation stall).  It must give the same result as fd_decode_attention,
-call after call, while keeping its partial results in the library's fixed
-scratch array.
+allocation stall).  Call after call, it must match the fp64 oracle and give
+the same result as fd_decode_attention, while keeping its partial results
+in the library's fixed scratch array.
 
 The file is named so that pytest collects it last: a run that stops at the
 first failure has then already run every other test.  It also passes on its
@@ -16,6 +16,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from decode_attention_20_b300 import _lib, inputs
 from decode_attention_20_b300.api import _desc
 
@@ -39,7 +40,15 @@ def _call(fn, case, q, k, v, sl, ns):
     return out, lse
 
 
+def _oracle(case):
+    lens = case.seqlens.numpy() if case.seqlens is not None else None
+    return oracle.decode_attention_ref(to_f64(case.q), to_f64(case.k), to_f64(case.v), lens,
+                                       case.scale)
+
+
 def test_noalloc_matches_allocating_entry_two_calls_in_a_row(cuda_device):
+    """Both calls in a row match the fp64 oracle and the allocating entry
+    point, within the bf16 tolerances."""
     L = _lib.lib()
     cases = [
         (inputs.flash_decoding_b1(4096, seed=5), 0),                                 # heuristic splits
@@ -48,11 +57,32 @@ def test_noalloc_matches_allocating_entry_two_calls_in_a_row(cuda_device):
     for case, ns in cases:
         q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
         sl = case.seqlens.cuda() if case.seqlens is not None else None
+        O_ref, L_ref = _oracle(case)
         ref_o, ref_l = _call(L.fd_decode_attention, case, q, k, v, sl, ns)
+        assert_parity(to_f64(ref_o), to_f64(ref_l), O_ref, L_ref, torch.bfloat16,
+                      f"allocating entry {case.name}")
         for call in range(2):                       # the scratch keeps the last call's contents
             o, l = _call(L.fd_decode_attention_noalloc, case, q, k, v, sl, ns)
+            assert_parity(to_f64(o), to_f64(l), O_ref, L_ref, torch.bfloat16,
+                          f"noalloc vs oracle {case.name} call {call}")
             assert_parity(to_f64(o), to_f64(l), to_f64(ref_o), to_f64(ref_l), torch.bfloat16,
-                          f"noalloc {case.name} call {call}")
+                          f"noalloc vs allocating entry {case.name} call {call}")
+
+
+def test_noalloc_lowers_the_heuristic_split_count_to_the_scratch(cuda_device):
+    """With num_splits = 0 the library's own choice is never refused: one kv
+    head with 64 query heads over 65536 tokens makes the heuristic pick 256
+    splits, whose partials (8.45 MB) exceed the 8 MiB scratch; the call runs
+    with fewer splits and still matches the oracle."""
+    L = _lib.lib()
+    case = inputs.decode_case(1, 64, 1, 128, 65536, seed=8)
+    assert L.fd_choose_num_splits(1, 1, 65536, 148) == 256
+    assert L.fd_workspace_bytes(1, 64, 128, 256) > SCRATCH_BYTES
+    q, k, v = case.q.cuda(), case.k.cuda(), case.v.cuda()
+    O_ref, L_ref = _oracle(case)
+    for call in range(2):
+        o, l = _call(L.fd_decode_attention_noalloc, case, q, k, v, None, 0)
+        assert_parity(to_f64(o), to_f64(l), O_ref, L_ref, torch.bfloat16, f"capped call {call}")
 
 
 def test_noalloc_rejects_work_beyond_the_scratch(cuda_device):
