@@ -202,6 +202,31 @@ bool make_3d_map(CUtensorMap* map, const void* base, int64_t D, int64_t n1, int6
   return r == CUDA_SUCCESS;
 }
 
+// 4-D bf16 map over the queries of a bifurcated call, q [n, Hq, D] seen as
+// [n][Hkv][G][D] (element strides q_sb, q_sh), with a box of 64 head dims x
+// rb heads x 1 kv head x sb samples (rb = min(G, 128), sb = 128 / rb) and
+// the 128-byte swizzle: one box is half a 128-row query tile of kv head g in
+// row order (sample, head).  Needs G to divide 128 or 128 to divide G.
+bool make_q_map(CUtensorMap* map, const void* base, int64_t n, int64_t Hkv, int64_t G,
+                int64_t D, int64_t q_sb, int64_t q_sh) {
+  if (!(128 % G == 0 || G % 128 == 0)) return false;
+  const int64_t rb = G < 128 ? G : 128, sb = 128 / rb;
+  const int64_t esz = 2;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)Hkv, (cuuint64_t)n};
+  // Unit extents never step along their strides; give them legal ones.
+  const int64_t sg = G * q_sh;
+  const int64_t ss = (n == 1) ? sg * Hkv : q_sb;
+  cuuint64_t strides[3] = {(cuuint64_t)(q_sh * esz), (cuuint64_t)(sg * esz),
+                           (cuuint64_t)(ss * esz)};
+  cuuint32_t box[4] = {64u, (cuuint32_t)rb, 1u, (cuuint32_t)sb};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = g_encode()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ validation
 
 int64_t esize(int32_t dt) {
@@ -1270,8 +1295,16 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         bp.fold = fold ? 1 : 0;
         bp.dec_lens = dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr;
         bp.Ld = (int)Ld;
-        e = launch_bif_ctx(bp, tmK, tmV, fold ? tmKd : tmK, fold ? tmVd : tmV, (int)mtiles, cs,
-                           !prof);
+        // The query tile by one TMA load where the map can describe it
+        // (tuning and test knob, read on every call: FD_BIF_Q_TMA = 0 keeps
+        // the per-thread query loads).
+        CUtensorMap tmQ = tmK;
+        const char* qe = getenv("FD_BIF_Q_TMA");
+        bp.q_tma = (!(qe && qe[0] == '0') &&
+                    make_q_map(&tmQ, q->data, n, Hkv, G, D, q->stride[0], q->stride[1]))
+                       ? 1 : 0;
+        e = launch_bif_ctx(bp, tmK, tmV, fold ? tmKd : tmK, fold ? tmVd : tmV, tmQ, (int)mtiles,
+                           cs, !prof);
         prof_end(FD_KERNEL_BIF_CTX, cs, prof, rec);
         if (e != cudaSuccess) st = cuda_fail(e, "bifurcated context kernel launch");
         ctx_done = true;

@@ -88,10 +88,12 @@ struct BifCfg {
   static constexpr int KV_BYTES = 2 * KV_CHUNK; // one K or V tile (two boxes)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + NK * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + NV * KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + NV * KV_BYTES;  // query tile (two swizzled boxes)
+  static constexpr int Q_BYTES = MT * D * 2;
+  static constexpr int OFF_BAR = OFF_Q + Q_BYTES;
   // barriers: k_full[NK], k_empty[NK], v_full[NV], v_empty[NV], q_ready,
-  // s_full[2], p_full[2], o_done, o_final, drain
-  static constexpr int NBAR = 2 * NK + 2 * NV + 1 + 2 + 2 + 3;
+  // s_full[2], p_full[2], o_done, o_final, drain, q_full
+  static constexpr int NBAR = 2 * NK + 2 * NV + 1 + 2 + 2 + 3 + 1;
   static constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBAR * 8 + 16;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_Q = 0;          // 64 columns
@@ -116,12 +118,9 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     bif_ctx_kernel(const __grid_constant__ BifCtxParams p, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmKd,
-                   const __grid_constant__ CUtensorMap tmVd) {
+                   const __grid_constant__ CUtensorMap tmVd,
+                   const __grid_constant__ CUtensorMap tmQ) {
   using C = BifCfg;
-  pdl_wait_prerequisites();   // launched with PDL: no memory access before this
-  // Every earlier grid has now finished: the decode part (which reads none of
-  // this kernel's output) may start on the SMs this grid leaves free.
-  pdl_launch_dependents();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,7 +135,8 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   uint64_t* o_done = p_full + 2;
   uint64_t* o_final = o_done + 1;
   uint64_t* drain = o_final + 1;
-  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* q_full = drain + 1;                 // the query tile's TMA load
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(q_full + 1);
   int* abort_s = reinterpret_cast<int*>(taddr_s + 1);
 
   const int mtile = blockIdx.x;                 // 128-row query tile
@@ -144,6 +144,37 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
   const int g = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+
+  // Set-up that reads no global memory (barriers, tensor memory, the
+  // tensor maps in parameter space) runs before the launch wait, so it
+  // overlaps the tail of the previous kernel on the stream.
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NBAR; ++i) {
+      const bool is_q = &bars[i] == q_ready;
+      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + 2);
+      mbar_init(&bars[i], (is_q || is_p) ? C::NSW * 32 : 1);
+    }
+    *abort_s = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(taddr_s, C::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    if (p.fold) {
+      prefetch_tensormap(&tmKd);
+      prefetch_tensormap(&tmVd);
+    }
+    if (p.q_tma) prefetch_tensormap(&tmQ);
+  }
+  pdl_wait_prerequisites();   // launched with PDL: no global memory access before this
+  // Every earlier grid has now finished: the decode part (which reads none of
+  // this kernel's output) may start on the SMs this grid leaves free.
+  pdl_launch_dependents();
+
   // Without the fold: context tiles [begin, end) of this split.  With it:
   // the query tile's work is the list of the nct context tiles followed by
   // the decode tiles of its samples s_first .. s_first + nsamp - 1 (sample
@@ -215,6 +246,38 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     nv = min(C::TN, len - tok);
   };
 
+  // Without the query TMA, the softmax warps issue their query-row loads now (one row per thread,
+  // bf16 pairs, dim 2c in the low half of word c), so they are in flight
+  // while the CTA finishes its set-up.  Rows past n * G load zeros.  A
+  // negative scale is folded in here (the sign bits flip), so the softmax
+  // always scales by |scale|.
+  uint32_t qv[2][32];
+  if (warp >= 2 && !p.q_tma && !(ntiles == 0 && p.cs == 1)) {
+    const int m = mtile * C::MT + (warp & 3) * 32 + lane;
+    if (m < p.rows) {
+      const int s = m / p.G;
+      const int h = g * p.G + (m - s * p.G);
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + s * p.q_sb + h * p.q_sh);
+      const uint32_t flip = p.negate_q ? 0x80008000u : 0u;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint4 w = src[i];
+        qv[i >> 3][(i & 7) * 4 + 0] = w.x ^ flip;
+        qv[i >> 3][(i & 7) * 4 + 1] = w.y ^ flip;
+        qv[i >> 3][(i & 7) * 4 + 2] = w.z ^ flip;
+        qv[i >> 3][(i & 7) * 4 + 3] = w.w ^ flip;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) qv[0][i] = qv[1][i] = 0u;
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *taddr_s;
+
   if (ntiles == 0 && p.cs == 1) {
     // Empty split: O = 0, lse = -inf for every valid row.  (In a cluster an
     // empty split still runs through, stages (m, l) = (-inf, 0) and joins the
@@ -228,139 +291,167 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
         if (p.lse) p.lse[s * p.l_sb + h * p.l_sh + split * p.l_ss] = kNegInf;
       }
     }
+    if (warp == 1) tc::tmem_dealloc(tmem, C::TMEM_COLS);
     return;
   }
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NBAR; ++i) {
-      const bool is_q = &bars[i] == q_ready;
-      const bool is_p = (&bars[i] >= p_full) && (&bars[i] < p_full + 2);
-      mbar_init(&bars[i], (is_q || is_p) ? C::NSW * 32 : 1);
-    }
-    *abort_s = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tc::tmem_alloc(taddr_s, C::TMEM_COLS);
-    tc::tmem_relinquish();
-  }
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *taddr_s;
 
   const uint32_t sbase = smem_u32(smem);
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-      if (fold) {
-        prefetch_tensormap(&tmKd);
-        prefetch_tensormap(&tmVd);
-      }
-      const uint64_t policy = l2_policy_evict_first();
-      int kt = 0, vt = 0;                           // next K / V tile to issue
-      bool ok = true;
-      while (ok && (kt < ntiles || vt < ntiles)) {
-        // K runs up to NK tiles ahead of V; V follows.
-        if (kt < ntiles && kt < vt + C::NK) {
-          const int st = kt % C::NK;
-          if (kt >= C::NK) ok = mbar_wait_or_abort(&k_empty[st], ((kt / C::NK) - 1) & 1, abort_s);
-          if (!ok) break;
-          unsigned char* dst = smem + C::OFF_K + st * C::KV_BYTES;
-          mbar_arrive_expect_tx(&k_full[st], C::KV_BYTES);
-          bool is_dec;
-          int k, tok, nv;
-          tile_of(kt, is_dec, k, tok, nv);
-          if (is_dec) {
-            tma_load_4d(dst, &tmKd, &k_full[st], 0, g, tok, s_first + k, policy);
-            tma_load_4d(dst + C::KV_CHUNK, &tmKd, &k_full[st], 64, g, tok, s_first + k, policy);
-          } else {
-            tma_load_3d(dst, &tmK, &k_full[st], 0, g, tok);
-            tma_load_3d(dst + C::KV_CHUNK, &tmK, &k_full[st], 64, g, tok);
-          }
-          ++kt;
-        }
-        if (vt < ntiles && vt < kt) {
-          const int st = vt % C::NV;
-          if (vt >= C::NV) ok = mbar_wait_or_abort(&v_empty[st], ((vt / C::NV) - 1) & 1, abort_s);
-          if (!ok) break;
-          unsigned char* dst = smem + C::OFF_V + st * C::KV_BYTES;
-          mbar_arrive_expect_tx(&v_full[st], C::KV_BYTES);
-          bool is_dec;
-          int k, tok, nv;
-          tile_of(vt, is_dec, k, tok, nv);
-          if (is_dec) {
-            tma_load_4d(dst, &tmVd, &v_full[st], 0, g, tok, s_first + k, policy);
-            tma_load_4d(dst + C::KV_CHUNK, &tmVd, &v_full[st], 64, g, tok, s_first + k, policy);
-          } else {
-            tma_load_3d(dst, &tmV, &v_full[st], 0, g, tok);
-            tma_load_3d(dst + C::KV_CHUNK, &tmV, &v_full[st], 64, g, tok);
-          }
-          ++vt;
-        }
-      }
-      // Never leave with copies in flight: wait for the last load of every
-      // stage (earlier loads of a stage completed before it was refilled).
-      for (int t = (kt > C::NK ? kt - C::NK : 0); t < kt; ++t)
-        mbar_wait_bounded(&k_full[t % C::NK], (t / C::NK) & 1);
-      for (int t = (vt > C::NV ? vt - C::NV : 0); t < vt; ++t)
-        mbar_wait_bounded(&v_full[t % C::NV], (t / C::NV) & 1);
+    // The whole warp runs the loop (warp-uniform waits and operands); one
+    // elected lane issues each copy.
+    const uint64_t policy = l2_policy_evict_first();
+    if (p.q_tma) {
+      // The query tile first: rows m0 .. m0 + 127 of kv head g are heads
+      // r0 .. of samples s0 .. (rows past n * G fill with zeros); the
+      // query rows of a tile are reused by every split, so they are kept in
+      // L2 with priority.
+      const int m0 = mtile * C::MT;
+      const int s0 = m0 / p.G, r0 = m0 - s0 * p.G;
+      const uint64_t qpol = l2_policy_evict_last();
+      mbar_arrive_expect_tx_w(q_full, C::Q_BYTES);
+      tma_load_4d_w(smem + C::OFF_Q, &tmQ, q_full, 0, r0, g, s0, qpol);
+      tma_load_4d_w(smem + C::OFF_Q + C::Q_BYTES / 2, &tmQ, q_full, 64, r0, g, s0, qpol);
     }
+    int kt = 0, vt = 0;                             // next K / V tile to issue
+    bool ok = true;
+    while (ok && (kt < ntiles || vt < ntiles)) {
+      // K runs up to NK tiles ahead of V; V follows.
+      if (kt < ntiles && kt < vt + C::NK) {
+        const int st = kt % C::NK;
+        if (kt >= C::NK)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_or_abort(&k_empty[st], ((kt / C::NK) - 1) & 1, abort_s));
+        if (!ok) break;
+        unsigned char* dst = smem + C::OFF_K + st * C::KV_BYTES;
+        mbar_arrive_expect_tx_w(&k_full[st], C::KV_BYTES);
+        bool is_dec;
+        int k, tok, nv;
+        tile_of(kt, is_dec, k, tok, nv);
+        if (is_dec) {
+          tma_load_4d_w(dst, &tmKd, &k_full[st], 0, g, tok, s_first + k, policy);
+          tma_load_4d_w(dst + C::KV_CHUNK, &tmKd, &k_full[st], 64, g, tok, s_first + k, policy);
+        } else {
+          tma_load_3d_w(dst, &tmK, &k_full[st], 0, g, tok);
+          tma_load_3d_w(dst + C::KV_CHUNK, &tmK, &k_full[st], 64, g, tok);
+        }
+        ++kt;
+      }
+      if (vt < ntiles && vt < kt) {
+        const int st = vt % C::NV;
+        if (vt >= C::NV)
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait_or_abort(&v_empty[st], ((vt / C::NV) - 1) & 1, abort_s));
+        if (!ok) break;
+        unsigned char* dst = smem + C::OFF_V + st * C::KV_BYTES;
+        mbar_arrive_expect_tx_w(&v_full[st], C::KV_BYTES);
+        bool is_dec;
+        int k, tok, nv;
+        tile_of(vt, is_dec, k, tok, nv);
+        if (is_dec) {
+          tma_load_4d_w(dst, &tmVd, &v_full[st], 0, g, tok, s_first + k, policy);
+          tma_load_4d_w(dst + C::KV_CHUNK, &tmVd, &v_full[st], 64, g, tok, s_first + k, policy);
+        } else {
+          tma_load_3d_w(dst, &tmV, &v_full[st], 0, g, tok);
+          tma_load_3d_w(dst + C::KV_CHUNK, &tmV, &v_full[st], 64, g, tok);
+        }
+        ++vt;
+      }
+    }
+    // Never leave with copies in flight: wait for the last load of every
+    // stage (earlier loads of a stage completed before it was refilled).
+    for (int t = (kt > C::NK ? kt - C::NK : 0); t < kt; ++t)
+      mbar_wait_bounded(&k_full[t % C::NK], (t / C::NK) & 1);
+    for (int t = (vt > C::NV ? vt - C::NV : 0); t < vt; ++t)
+      mbar_wait_bounded(&v_full[t % C::NV], (t / C::NV) & 1);
+    if (p.q_tma) mbar_wait_bounded(q_full, 0);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop; one elected lane issues each MMA and
+    // commit (warp-uniform descriptors stay in uniform registers, so the
+    // issue keeps ahead of the tensor core).
+    {
       constexpr uint32_t IDESC_S = tc::idesc_bf16_f32(C::MT, C::TN, false, false);
       constexpr uint32_t IDESC_O = tc::idesc_bf16_f32(C::MT, C::D, false, true);
-      // S[j % 2] = Q K_j^T (8 MMAs of K = 16 head dims; Q columns 8 kk).
-      auto issue_s = [&](int j) {
-        const uint32_t k_addr = sbase + C::OFF_K + (j % C::NK) * C::KV_BYTES;
-        const uint32_t d_tmem = tmem + C::COL_S + (j & 1) * 128;
+      // Descriptors of stage 0's K and V boxes.  A stage, a 16-column step
+      // of K or a 16-token step of V adds a constant to the start-address
+      // field (16-byte units, low bits; shared addresses stay below 2^18, so
+      // the field never carries).
+      const uint64_t kd0 = tc::smem_desc_sw128(sbase + C::OFF_K, 16, 1024);
+      const uint64_t vd0 = tc::smem_desc_sw128(sbase + C::OFF_V, C::KV_CHUNK, 1024);
+      const uint32_t q_t = tmem + C::COL_Q;
+      // S[j % 2] = Q K_j^T from K stage kst (8 MMAs of K = 16 head dims; Q
+      // columns 8 kk; K box kk / 4, 32 bytes per 16 dims within it).
+      auto issue_s = [&](int j, int kst) {
+        const uint64_t kd = kd0 + (uint64_t)(kst * (C::KV_BYTES >> 4));
+        const uint32_t d_tmem = tmem + C::COL_S + (uint32_t)(j & 1) * 128u;
+        tc::mma_bf16_ts_w<false>(d_tmem, q_t, kd, IDESC_S);
 #pragma unroll
-        for (int kk = 0; kk < C::D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * C::KV_CHUNK + (kk & 3) * 32;
-          tc::mma_bf16_ts(d_tmem, tmem + C::COL_Q + kk * 8,
-                          tc::smem_desc_sw128(k_addr + koff, 16, 1024), IDESC_S, kk > 0);
+        for (int kk = 1; kk < C::D / 16; ++kk)
+          tc::mma_bf16_ts_w<true>(d_tmem, q_t + kk * 8,
+                                  kd + (uint64_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4),
+                                  IDESC_S);
+        tc::commit_w(&s_full[j & 1]);
+      };
+      // O += P_j V_j from V stage vst (8 MMAs of K = 16 tokens; P_j from the
+      // first 64 columns of S[j % 2], 8 per MMA; V MN-major: 16 token rows
+      // of 128 bytes per step, two 64-wide head-dim blocks KV_CHUNK apart).
+      auto issue_pv = [&](int j, int vst) {
+        const uint64_t vd = vd0 + (uint64_t)(vst * (C::KV_BYTES >> 4));
+        const uint32_t a_tmem = tmem + C::COL_S + (uint32_t)(j & 1) * 128u;
+        if (j == 0)
+          tc::mma_bf16_ts_w<false>(tmem + C::COL_O, a_tmem, vd, IDESC_O);
+        else
+          tc::mma_bf16_ts_w<true>(tmem + C::COL_O, a_tmem, vd, IDESC_O);
+#pragma unroll
+        for (int kk = 1; kk < C::TN / 16; ++kk)
+          tc::mma_bf16_ts_w<true>(tmem + C::COL_O, a_tmem + kk * 8,
+                                  vd + (uint64_t)((kk * 16 * 128) >> 4), IDESC_O);
+        tc::commit_w(o_done);
+      };
+      auto wait = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait_or_abort(bar, parity, abort_s));
+      };
+      bool ok = wait(q_ready, 0);
+      if (ok && p.q_tma) {
+        // Query tile (shared memory, K-major, 128-byte swizzle) -> Q in
+        // tensor memory: 8 copies of 16 head dims, ordered before the MMAs.
+        ok = wait(q_full, 0);
+        if (ok) {
+          tc::fence_after_sync();
+          const uint64_t qd0 = tc::smem_desc_sw128(sbase + C::OFF_Q, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < C::D / 16; ++kk)
+            tc::cp_128x256b_w(q_t + kk * 8,
+                              qd0 + (uint64_t)(((kk >> 2) * (C::Q_BYTES / 2) + (kk & 3) * 32) >> 4));
         }
-        tc::commit(&s_full[j & 1]);
-      };
-      // O += P_j V_j (8 MMAs of K = 16 tokens; P_j from the first 64 columns
-      // of S[j % 2], 8 per MMA; V MN-major: 16 token rows at 16 kk, two
-      // 64-wide head-dim blocks KV_CHUNK apart).
-      auto issue_pv = [&](int j) {
-        const uint32_t v_addr = sbase + C::OFF_V + (j % C::NV) * C::KV_BYTES;
-        const uint32_t a_tmem = tmem + C::COL_S + (j & 1) * 128;
-#pragma unroll
-        for (int kk = 0; kk < C::TN / 16; ++kk)
-          tc::mma_bf16_ts(tmem + C::COL_O, a_tmem + kk * 8,
-                          tc::smem_desc_sw128(v_addr + kk * 16 * 128, C::KV_CHUNK, 1024),
-                          IDESC_O, (j > 0) || (kk > 0));
-        tc::commit(o_done);
-      };
-      bool ok = mbar_wait_or_abort(q_ready, 0, abort_s);
+      }
       // Prologue: scores of tiles 0 and 1.
       for (int j = 0; ok && j < 2 && j < ntiles; ++j) {
-        if (!mbar_wait_or_abort(&k_full[j % C::NK], (j / C::NK) & 1, abort_s)) { ok = false; break; }
+        if (!wait(&k_full[j % C::NK], (j / C::NK) & 1)) { ok = false; break; }
         tc::fence_after_sync();
-        issue_s(j);
-        tc::commit(&k_empty[j % C::NK]);
+        issue_s(j, j % C::NK);
+        tc::commit_w(&k_empty[j % C::NK]);
       }
+      int vst = 0, vph = 0;                          // V stage and phase of tile j
+      int kst = 2 % C::NK, kph = (2 / C::NK) & 1;    // K stage and phase of tile j + 2
       for (int j = 0; ok && j < ntiles; ++j) {
-        if (!mbar_wait_or_abort(&v_full[j % C::NV], (j / C::NV) & 1, abort_s)) break;
-        if (!mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1, abort_s)) break;
+        if (!wait(&v_full[vst], (uint32_t)vph)) break;
+        if (!wait(&p_full[j & 1], (j >> 1) & 1)) break;
         tc::fence_after_sync();
-        issue_pv(j);
-        tc::commit(&v_empty[j % C::NV]);
+        issue_pv(j, vst);
+        tc::commit_w(&v_empty[vst]);
         if (j + 2 < ntiles) {
-          if (!mbar_wait_or_abort(&k_full[(j + 2) % C::NK], ((j + 2) / C::NK) & 1, abort_s)) break;
-          issue_s(j + 2);
-          tc::commit(&k_empty[(j + 2) % C::NK]);
+          if (!wait(&k_full[kst], (uint32_t)kph)) break;
+          issue_s(j + 2, kst);
+          tc::commit_w(&k_empty[kst]);
         }
+        if (++vst == C::NV) { vst = 0; vph ^= 1; }
+        if (++kst == C::NK) { kst = 0; kph ^= 1; }
       }
-      tc::commit(o_final);
+      tc::commit_w(o_final);
       // Drain: every MMA issued above completes before the TMEM is freed.
-      tc::commit(drain);
+      tc::commit_w(drain);
       mbar_wait_bounded(drain, 0);
     }
   } else {
@@ -372,90 +463,107 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
     const uint32_t o_tmem = tmem + lane_base + C::COL_O;
     const int m0 = mtile * C::MT;                 // first row of this tile
     const int row_s = (m0 + r) / p.G;             // sample of this row
-    {
-      // Query row -> Q (bf16 pairs, dim 2c in the low half of column c).
-      // Rows past n * G load zeros.  A negative scale is folded in here (the
-      // sign bits flip), so the softmax below always scales by |scale|.
-      uint32_t qv[2][32];
-      const int m = m0 + r;
-      if (m < p.rows) {
-        const int s = m / p.G;
-        const int h = g * p.G + (m - s * p.G);
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + s * p.q_sb + h * p.q_sh);
-        const uint32_t flip = p.negate_q ? 0x80008000u : 0u;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint4 w = src[i];
-          qv[i >> 3][(i & 7) * 4 + 0] = w.x ^ flip;
-          qv[i >> 3][(i & 7) * 4 + 1] = w.y ^ flip;
-          qv[i >> 3][(i & 7) * 4 + 2] = w.z ^ flip;
-          qv[i >> 3][(i & 7) * 4 + 3] = w.w ^ flip;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) qv[0][i] = qv[1][i] = 0u;
-      }
+    bool q_ok = true;
+    if (!p.q_tma) {
+      // Query row (loaded above) -> Q in tensor memory.
       tc::tmem_st32(q_tmem, qv[0]);
       tc::tmem_st32(q_tmem + 32, qv[1]);
       tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(q_ready);
+    } else if (p.negate_q) {
+      // A negative scale: flip the sign bits of the staged query tile before
+      // the MMA warp copies it (consecutive threads on consecutive 16 bytes).
+      q_ok = __all_sync(0xffffffffu, mbar_wait_or_abort(q_full, 0, abort_s));
+      if (q_ok) {
+        uint4* qs = reinterpret_cast<uint4*>(smem + C::OFF_Q);
+        const int t = threadIdx.x - 64;
+        for (int i = t; i < C::Q_BYTES / 16; i += C::NSW * 32) {
+          uint4 w = qs[i];
+          w.x ^= 0x80008000u;
+          w.y ^= 0x80008000u;
+          w.z ^= 0x80008000u;
+          w.w ^= 0x80008000u;
+          qs[i] = w;
+        }
+        tc::fence_proxy_async_smem();
+      }
     }
+    mbar_arrive(q_ready);
     float m_run = kNegInf, l_run = 0.f;
-    bool ok = true;
+    bool ok = q_ok;
     const float c2 = p.scale_log2;                 // |scale| * log2(e) >= 0
-    for (int j = 0; j < ntiles; ++j) {
+    const uint64_t c2x2 = f2_pack(c2, c2);
+    for (int j = 0; ok && j < ntiles; ++j) {
       const uint32_t s_tmem = tmem + lane_base + C::COL_S + (j & 1) * 128;
       // Waits are made warp-uniform before any .sync.aligned tcgen05 access.
       const bool got = mbar_wait_or_abort(&s_full[j & 1], (j >> 1) & 1, abort_s);
       if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
       tc::fence_after_sync();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, sr[c]);
-      tc::tmem_wait_ld();
       // Context tile: the context's tail; decode tile: its sample's tail,
       // and nothing at all for rows of the tile's other samples.
       bool is_dec;
       int ks, tok, tile_valid;
       tile_of(j, is_dec, ks, tok, tile_valid);
       const int nvalid = (!is_dec || row_s == s_first + ks) ? tile_valid : 0;
-      if (nvalid < C::TN) {                        // tail tiles (and other samples' decode tiles)
+      float m_new = m_run, alpha = 1.f, tile_sum = 0.f;
+      if (__all_sync(0xffffffffu, nvalid == 0)) {
+        // A decode tile of a sample none of this warp's rows belongs to:
+        // P = 0 on every row, nothing to exponentiate.
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0u;
+        tc::tmem_st32(s_tmem, z);
+        tc::tmem_st32(s_tmem + 32, z);
+      } else {
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, sr[c]);
+        tc::tmem_wait_ld();
+        if (nvalid < C::TN) {                      // tail tiles (and other samples' decode tiles)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= nvalid) sr[c][i] = __float_as_uint(kNegInf);
+        }
+        // Row maximum: three-input maxima in 4 independent chains.
+        float mx4[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= nvalid) sr[c][i] = __float_as_uint(kNegInf);
-      }
-      // Row maximum with 8 independent chains.
-      float mx8[8];
+          for (int i = 0; i < 16; ++i)
+            mx4[i & 3] = fmax3(mx4[i & 3], __uint_as_float(sr[c][2 * i]),
+                               __uint_as_float(sr[c][2 * i + 1]));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c2;  // -inf stays -inf (c2 > 0)
+        m_new = (mx > m_run + 8.f) ? mx : m_run;
+        alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
+        const float m_use = (m_new == kNegInf) ? 0.f : m_new;   // all -inf: p = 0, not NaN
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        // p = 2^(s * c2 - m): one packed FMA per pair of columns, one ex2 per
+        // column, the pair packed as bf16 (even token in the low half) and
+        // summed with one packed add; P_j is stored into the first 64
+        // columns of the score buffer.
+        uint64_t sum2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = kNegInf;
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sr[c][i]));
-#pragma unroll
-      for (int k = 1; k < 8; ++k) mx8[0] = fmaxf(mx8[0], mx8[k]);
-      const float mx = mx8[0] * c2;                 // -inf stays -inf (c2 > 0)
-      const float m_new = (mx > m_run + 8.f) ? mx : m_run;
-      const float alpha = (m_new == m_run) ? 1.f : fast_exp2(m_run - m_new);
-      const float m_use = (m_new == kNegInf) ? 0.f : m_new;   // all -inf: p = 0, not NaN
-      // p = 2^(s * c2 - m); P_j as bf16 pairs (even token in the low half)
-      // packed in place and stored into the first 64 columns of the buffer.
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i]), c2, -m_use));
-          const float p1 = fast_exp2(fmaf(__uint_as_float(sr[c][2 * i + 1]), c2, -m_use));
-          sum4[i & 3] += p0 + p1;
-          uint32_t w;
-          asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(p1), "f"(p0));
-          sr[c][i] = w;
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])),
+                             c2x2, negm2), x0, x1);
+            const float p0 = fast_exp2(x0);
+            const float p1 = fast_exp2(x1);
+            sum2[i & 3] = f2_add(sum2[i & 3], f2_pack(p0, p1));
+            uint32_t w;
+            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(p1), "f"(p0));
+            sr[c][i] = w;
+          }
+          tc::tmem_st16(s_tmem + c * 16, sr[c]);
         }
-        tc::tmem_st16(s_tmem + c * 16, sr[c]);
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(sum2[0], sum2[1]), a0, a1);
+        f2_unpack(f2_add(sum2[2], sum2[3]), b0, b1);
+        tile_sum = (a0 + a1) + (b0 + b1);
       }
       // Rescale O where its max moved (rare), once O += P_{j-1} V_{j-1} is
       // done: o_done has then completed phases 0..j-1 (phase j needs P_j).
@@ -493,7 +601,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
       tc::tmem_wait_st();
       tc::fence_before_sync();
       mbar_arrive(&p_full[j & 1]);
-      l_run = l_run * alpha + ((sum4[0] + sum4[1]) + (sum4[2] + sum4[3]));
+      l_run = l_run * alpha + tile_sum;
       m_run = m_new;
     }
     // ------------------------------------------------------------ epilogue
@@ -542,7 +650,7 @@ __global__ void __launch_bounds__(BifCfg::THREADS, 1)
         const int s = m / p.G;
         const int h = g * p.G + (m - s * p.G);
         bulk_store(p.o + s * p.o_sb + h * p.o_sh + split * p.o_ss, stage + r * SROW, C::D * 4);
-        bulk_store_commit_and_wait();
+        bulk_store_commit_and_wait_read();
       }
     }
   }

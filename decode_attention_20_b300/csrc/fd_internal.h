@@ -118,6 +118,12 @@ struct BifCtxParams {
   int fold;
   const int32_t* dec_lens;
   int Ld;
+  // 1: the query tile arrives by one TMA load (tensor map over q as
+  // [n][Hkv][G][D], a box of min(G, 128) heads x max(1, 128 / G) samples;
+  // G divides 128 or 128 divides G) into shared memory and is copied into
+  // tensor memory by the MMA warp (tcgen05.cp); 0: each softmax thread
+  // loads its query row from global memory into tensor memory.
+  int q_tma;
 };
 
 // Most samples a 128-row query tile can span when the decode part is folded.
@@ -141,7 +147,7 @@ cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, b
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmKd, const CUtensorMap& tmVd,
-                           int mtiles, cudaStream_t st, bool pdl);
+                           const CUtensorMap& tmQ, int mtiles, cudaStream_t st, bool pdl);
 
 // Tile height (tokens) of the TMA split kernel; the tensor-map box uses it.
 constexpr int kSplitTileTokens = 64;

@@ -209,13 +209,13 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
 
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmKd, const CUtensorMap& tmVd,
-                           int mtiles, cudaStream_t st, bool pdl) {
+                           const CUtensorMap& tmQ, int mtiles, cudaStream_t st, bool pdl) {
   static std::atomic<unsigned long long> optin{0ull};
   const cudaError_t e = smem_optin(bif_ctx_kernel, BifCfg::SMEM_BYTES, optin);
   if (e != cudaSuccess) return e;
   if (p.cs <= 1)
     return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
-                     BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV, tmKd, tmVd);
+                     BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV, tmKd, tmVd, tmQ);
   // Clusters of cs CTAs along the splits (grid.y is a multiple of cs).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(mtiles, p.ns, p.Hkv);
@@ -229,7 +229,7 @@ cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bif_ctx_kernel, p, tmK, tmV, tmKd, tmVd);
+  return cudaLaunchKernelEx(&cfg, bif_ctx_kernel, p, tmK, tmV, tmKd, tmVd, tmQ);
 }
 
 }  // namespace fd
