@@ -227,6 +227,29 @@ bool make_q_map(CUtensorMap* map, const void* base, int64_t n, int64_t Hkv, int6
   return r == CUDA_SUCCESS;
 }
 
+// 5-D fp32 map over the bifurcated partial outputs [S][n][Hq][D] (element
+// strides o_ss, o_sb, o_sh) seen as [S][n][Hkv][G][D], with a box of 32
+// head dims x rb heads x 1 kv head x sb samples x 1 slot (rb = min(G, 128),
+// sb = 128 / rb) and the 128-byte swizzle: four boxes are the 128 partial
+// rows of one context CTA.  Needs G to divide 128 or 128 to divide G.
+bool make_o_map(CUtensorMap* map, void* base, int64_t S, int64_t n, int64_t Hkv, int64_t G,
+                int64_t D, int64_t o_ss, int64_t o_sb, int64_t o_sh) {
+  if (!(128 % G == 0 || G % 128 == 0)) return false;
+  const int64_t rb = G < 128 ? G : 128, sb = 128 / rb;
+  const int64_t esz = 4;
+  cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)G, (cuuint64_t)Hkv, (cuuint64_t)n,
+                        (cuuint64_t)S};
+  const int64_t sg = G * o_sh;
+  cuuint64_t strides[4] = {(cuuint64_t)(o_sh * esz), (cuuint64_t)(sg * esz),
+                           (cuuint64_t)(o_sb * esz), (cuuint64_t)(o_ss * esz)};
+  cuuint32_t box[5] = {32u, (cuuint32_t)rb, 1u, (cuuint32_t)sb, 1u};
+  cuuint32_t estr[5] = {1u, 1u, 1u, 1u, 1u};
+  CUresult r = g_encode()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ validation
 
 int64_t esize(int32_t dt) {
@@ -1180,19 +1203,15 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
                         kBifTileTokens);
   }
   const int64_t mtiles = (n * G + 128 * kBifQueryTiles - 1) / (128 * kBifQueryTiles);
-  // Optional thread-block clusters (see below).  Tuning knob, read on every
-  // call.
-  const char* ce = getenv("FD_BIF_CLUSTER");
-  const int cmax = ce ? atoi(ce) : 1;
   // Decode part folded into the context kernel: each query tile's decode
   // tiles join its list of context tiles, masked per sample, and the list is
   // shared out evenly over the splits.  Used when a 128-row tile spans few
-  // samples (G >= 16), no clusters are asked for and the decode caches can
+  // samples (G >= 16) and the decode caches can
   // be streamed by TMA; FD_BIF_FOLD = 0 turns it off (tuning and test knob,
   // read on every call).
   CUtensorMap tmKd, tmVd;
   bool fold = false;
-  if (tc_ok && cmax < 2 && G >= 16 && Ld > 0) {
+  if (tc_ok && G >= 16 && Ld > 0) {
     const char* fe = getenv("FD_BIF_FOLD");
     fold = !(fe && fe[0] == '0') && aligned16(k_dec->data) && aligned16(v_dec->data);
     for (int i = 0; fold && i < 3; ++i)
@@ -1232,24 +1251,7 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
     if (want > kMaxSplits) want = kMaxSplits;
     ns_dec = want < 1 ? 1 : (int)want;
   }
-  // Optional thread-block clusters along the context splits merge them on
-  // chip (distributed shared memory) instead of writing one partial per
-  // split.  Off by default: on B300 the clustered launch measured slower
-  // (clusters of 8 CTAs of ~190 KB shared memory each are hard to co-place
-  // in one GPC).  FD_BIF_CLUSTER = 2, 4 or 8 enables clusters of at most
-  // that many CTAs: the cluster size is then the largest power of two up to
-  // it dividing ns_ctx (it must divide the 128 rows of a tile), used only
-  // when every split holds tokens.
-  int csize = 1;
-  if (tc_ok) {
-    const int64_t per = (Lc + ns_ctx - 1) / ns_ctx;
-    const int64_t chunk = ((per + kBifTileTokens - 1) / kBifTileTokens) * kBifTileTokens;
-    const bool all_full = (int64_t)(ns_ctx - 1) * chunk < Lc;
-    if (cmax >= 2 && all_full)
-      for (int d = 8; d >= 2; d /= 2)
-        if (d <= cmax && ns_ctx % d == 0) { csize = d; break; }
-  }
-  const int S = ns_ctx / csize + ns_dec;
+  const int S = ns_ctx + ns_dec;
   const int64_t bytes = workspace_bytes(n, Hq, D, S);
   void* ws = nullptr;
   cudaError_t e = cudaMallocFromPoolAsync(&ws, (size_t)bytes, info->pool, cs);
@@ -1281,7 +1283,6 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         // masked tail scores stay at -inf instead of 0 * inf = NaN.
         bp.scale_log2 = scale == 0.f ? 1e-30f : std::fabs(scale) * 1.4426950408889634f;
         bp.negate_q = scale < 0.f ? 1 : 0;
-        bp.cs = csize;
         bp.o = po;
         bp.o_sb = Hq * D;
         bp.o_sh = D;
@@ -1303,8 +1304,15 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
         bp.q_tma = (!(qe && qe[0] == '0') &&
                     make_q_map(&tmQ, q->data, n, Hkv, G, D, q->stride[0], q->stride[1]))
                        ? 1 : 0;
-        e = launch_bif_ctx(bp, tmK, tmV, fold ? tmKd : tmK, fold ? tmVd : tmV, tmQ, (int)mtiles,
-                           cs, !prof);
+        // The partial rows leave by TMA tensor stores where the same box
+        // rule describes them (FD_BIF_O_TMA = 0: per-thread stores).
+        CUtensorMap tmO = tmK;
+        const char* oe = getenv("FD_BIF_O_TMA");
+        bp.o_tma = (!(oe && oe[0] == '0') &&
+                    make_o_map(&tmO, po, S, n, Hkv, G, D, bp.o_ss, bp.o_sb, bp.o_sh))
+                       ? 1 : 0;
+        e = launch_bif_ctx(bp, tmK, tmV, fold ? tmKd : tmK, fold ? tmVd : tmV, tmQ, tmO,
+                           (int)mtiles, cs, !prof);
         prof_end(FD_KERNEL_BIF_CTX, cs, prof, rec);
         if (e != cudaSuccess) st = cuda_fail(e, "bifurcated context kernel launch");
         ctx_done = true;
@@ -1324,9 +1332,9 @@ fd_status fd_bifurcated_attention_lse(const fd_tensor* q, const fd_tensor* k_ctx
     DecodeDesc dd = {n, Hq, Hkv, D, Ld, Hq / Hkv, FD_BF16, FD_BF16};
     st = enqueue_split(dd, q, k_dec, v_dec,
                        dec_lens ? reinterpret_cast<const int32_t*>(dec_lens->data) : nullptr,
-                       ns_dec, scale, po + (int64_t)(ns_ctx / csize) * n * Hq * D, Hq * D, D,
-                       n * Hq * D, pl + (int64_t)(ns_ctx / csize) * n * Hq, Hq, 1, n * Hq, false,
-                       cs, nullptr, 0, 0, /*late_wait=*/ctx_done && csize == 1);
+                       ns_dec, scale, po + (int64_t)ns_ctx * n * Hq * D, Hq * D, D,
+                       n * Hq * D, pl + (int64_t)ns_ctx * n * Hq, Hq, 1, n * Hq, false,
+                       cs, nullptr, 0, 0, /*late_wait=*/ctx_done);
   }
   if (st == FD_OK) {
     CombineParams cp = {};

@@ -270,4 +270,85 @@ __global__ void __launch_bounds__(kCombineManyThreads)
     p.lse[r1 * p.lse_r1 + r2 * p.lse_r2 + (MULTI ? rm * p.lse_rm : 0)] = empty ? M : M + __logf(tot);
 }
 
+// Warp-per-row layout for grids of many rows with at most 32 splits and a
+// head dim of at most 128 (D / 4 lanes own 4 consecutive elements each):
+// lane s loads lse_s, the warp's shuffle reductions give M and
+// sum_i e^(lse_i - M) with no block barrier, and the partial-row loads
+// (up to kCombineRowBatch splits at a time, issued before the weights are
+// known) go out with the lse loads, so a row costs about one round of
+// memory latency.  kCombineRowWarps rows per CTA.
+constexpr int kCombineRowWarps = 4;
+constexpr int kCombineRowBatch = 16;
+
+template <bool MULTI>
+__global__ void __launch_bounds__(kCombineRowWarps * 32)
+    lse_combine_rows_kernel(const __grid_constant__ CombineParams p) {
+  constexpr float kNegInfC = -__builtin_huge_valf();
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kCombineRowWarps + (threadIdx.x >> 5);
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
+  int r1, rm = 0, r2;
+  if constexpr (MULTI) {                 // (sequence, query token, head) rows
+    if (row >= p.R1 * p.Rm * p.R2) return;
+    r1 = row / (p.Rm * p.R2);
+    const int rr = row - r1 * (p.Rm * p.R2);
+    rm = rr / p.R2;
+    r2 = rr - rm * p.R2;
+  } else {
+    if (row >= p.R1 * p.R2) return;
+    r1 = row / p.R2;
+    r2 = row - r1 * p.R2;
+  }
+  const float* pl = p.part_lse + r1 * p.pl_r1 + r2 * p.pl_r2 + (MULTI ? rm * p.pl_rm : 0);
+  const float* po = p.part_o + r1 * p.po_r1 + r2 * p.po_r2 + (MULTI ? rm * p.po_rm : 0);
+  const int CD = p.D >> 2;
+  const bool owner = lane < CD;
+  const float* pc = po + lane * 4;
+  // First batch of partial rows and every lse, all in flight at once.
+  float4 v[kCombineRowBatch];
+#pragma unroll
+  for (int k = 0; k < kCombineRowBatch; ++k)
+    v[k] = (owner && k < p.S) ? *reinterpret_cast<const float4*>(pc + k * p.po_s)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float ls = lane < p.S ? pl[lane * p.pl_s] : kNegInfC;
+  float M = ls;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const bool empty = (M == kNegInfC);
+  const float e = empty ? 0.f : fast_exp2((ls - M) * kLog2e);   // -inf -> 0
+  float tot = e;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const float w_mine = empty ? 0.f : e / tot;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [&](const float4& x, float w) {
+    if (w != 0.f) {              // an empty split's row is never used (it may hold anything)
+      acc.x = fmaf(w, x.x, acc.x);
+      acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z);
+      acc.w = fmaf(w, x.w, acc.w);
+    }
+  };
+#pragma unroll
+  for (int k = 0; k < kCombineRowBatch; ++k) add(v[k], __shfl_sync(0xffffffffu, w_mine, k));
+  for (int s0 = kCombineRowBatch; s0 < p.S; s0 += kCombineRowBatch) {
+#pragma unroll
+    for (int k = 0; k < kCombineRowBatch; ++k)
+      v[k] = (owner && s0 + k < p.S) ? *reinterpret_cast<const float4*>(pc + (s0 + k) * p.po_s)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kCombineRowBatch; ++k) add(v[k], __shfl_sync(0xffffffffu, w_mine, (s0 + k) & 31));
+  }
+  if (owner) {
+    float* out = p.out + r1 * p.out_r1 + r2 * p.out_r2 + (MULTI ? rm * p.out_rm : 0) + lane * 4;
+    out[0] = acc.x;
+    out[1] = acc.y;
+    out[2] = acc.z;
+    out[3] = acc.w;
+  }
+  if (lane == 0 && p.lse != nullptr)
+    p.lse[r1 * p.lse_r1 + r2 * p.lse_r2 + (MULTI ? rm * p.lse_rm : 0)] = empty ? M : M + __logf(tot);
+}
+
 }  // namespace fd

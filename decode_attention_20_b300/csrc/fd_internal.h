@@ -103,8 +103,6 @@ struct BifCtxParams {
   int rows;                   // n * G
   float scale_log2;           // |scale| * log2(e)
   int negate_q;               // 1: scale < 0, the kernel negates Q as it loads it
-  int cs;                     // CTAs per cluster along the splits (1, 2, 4 or 8); a
-                              // cluster merges its splits into partial slot split / cs
   float* o;                   // partial outputs, fp32
   int64_t o_sb, o_sh, o_ss;   // strides over (sample, q head, split)
   float* lse;                 // natural-log partial lse
@@ -124,6 +122,10 @@ struct BifCtxParams {
   // tensor memory by the MMA warp (tcgen05.cp); 0: each softmax thread
   // loads its query row from global memory into tensor memory.
   int q_tma;
+  // 1: the 128 partial rows of a CTA leave by TMA tensor stores (tensor map
+  // over the partial outputs as [S][n][Hkv][G][D], same box rule as the
+  // query map); 0: each softmax thread writes its half row.
+  int o_tma;
 };
 
 // Most samples a 128-row query tile can span when the decode part is folded.
@@ -147,7 +149,8 @@ cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, b
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmKd, const CUtensorMap& tmVd,
-                           const CUtensorMap& tmQ, int mtiles, cudaStream_t st, bool pdl);
+                           const CUtensorMap& tmQ, const CUtensorMap& tmO, int mtiles,
+                           cudaStream_t st, bool pdl);
 
 // Tile height (tokens) of the TMA split kernel; the tensor-map box uses it.
 constexpr int kSplitTileTokens = 64;

@@ -197,6 +197,13 @@ cudaError_t launch_split_generic(const SplitParams& p, int D, cudaStream_t st, b
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
   const int rows = p.R1 * (p.Rm > 1 ? p.Rm : 1) * p.R2;   // Rm is 0 or 1 without query tokens
+  if (rows > kCombineFewRows && p.S <= 32 && p.D <= 128) {
+    const dim3 grid((rows + kCombineRowWarps - 1) / kCombineRowWarps);
+    return p.Rm > 1 ? launch_ex(lse_combine_rows_kernel<true>, grid, dim3(kCombineRowWarps * 32),
+                                0, st, pdl, p)
+                    : launch_ex(lse_combine_rows_kernel<false>, grid, dim3(kCombineRowWarps * 32),
+                                0, st, pdl, p);
+  }
   if (rows > kCombineFewRows)
     return p.Rm > 1 ? launch_ex(lse_combine_many_kernel<true>, dim3(rows),
                                 dim3(kCombineManyThreads), 0, st, pdl, p)
@@ -209,27 +216,13 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t st, bool pdl) {
 
 cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const CUtensorMap& tmV,
                            const CUtensorMap& tmKd, const CUtensorMap& tmVd,
-                           const CUtensorMap& tmQ, int mtiles, cudaStream_t st, bool pdl) {
+                           const CUtensorMap& tmQ, const CUtensorMap& tmO, int mtiles,
+                           cudaStream_t st, bool pdl) {
   static std::atomic<unsigned long long> optin{0ull};
   const cudaError_t e = smem_optin(bif_ctx_kernel, BifCfg::SMEM_BYTES, optin);
   if (e != cudaSuccess) return e;
-  if (p.cs <= 1)
-    return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
-                     BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV, tmKd, tmVd, tmQ);
-  // Clusters of cs CTAs along the splits (grid.y is a multiple of cs).
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(mtiles, p.ns, p.Hkv);
-  cfg.blockDim = dim3(BifCfg::THREADS);
-  cfg.dynamicSmemBytes = BifCfg::SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = p.cs;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bif_ctx_kernel, p, tmK, tmV, tmKd, tmVd, tmQ);
+  return launch_ex(bif_ctx_kernel, dim3(mtiles, p.ns, p.Hkv), dim3(BifCfg::THREADS),
+                   BifCfg::SMEM_BYTES, st, pdl, p, tmK, tmV, tmKd, tmVd, tmQ, tmO);
 }
 
 }  // namespace fd

@@ -76,16 +76,19 @@ def test_bifurcated_mqa_sampling_workload(cuda_device):
 # oracle, across M-tile tails, context tails, split counts and a peaked
 # softmax that makes the running max jump (accumulator rescaling).
 
-@pytest.fixture(params=["tc", "tc_nofold", "tc_cluster", "split"])
+@pytest.fixture(params=["tc", "tc_nofold", "tc_rowio", "split"])
 def ctx_path(request, monkeypatch):
     """tc: tensor-core context kernel, one partial per split, with the decode
-    part folded into it where G >= 16 (default); tc_nofold: the same with the
-    decode part on the split kernel; tc_cluster: splits merged in
-    thread-block clusters of up to 8 CTAs where they divide evenly; split:
-    the split kernel over a broadcast view of the context."""
+    part folded into it where G >= 16, the query tile loaded and the partial
+    rows stored by TMA where the maps apply (default); tc_nofold: the same
+    with the decode part on the split kernel; tc_rowio: query rows loaded
+    and partial rows stored by each thread; split: the split kernel over a
+    broadcast view of the context."""
     monkeypatch.setenv("FD_BIF_CTX", "split" if request.param == "split" else "tc")
-    monkeypatch.setenv("FD_BIF_CLUSTER", "8" if request.param == "tc_cluster" else "1")
     monkeypatch.setenv("FD_BIF_FOLD", "0" if request.param == "tc_nofold" else "1")
+    rowio = "0" if request.param == "tc_rowio" else "1"
+    monkeypatch.setenv("FD_BIF_Q_TMA", rowio)
+    monkeypatch.setenv("FD_BIF_O_TMA", rowio)
     return request.param
 
 
@@ -96,9 +99,11 @@ def ctx_path(request, monkeypatch):
     (3, 2, 64, 129, 5, 2),         # G = 64, second split holds one token
     (16, 1, 8, 4173, 20, 1),       # one split streams 33 tiles (rings wrap many times)
     (2, 1, 1, 700, 9, 0),          # G = 1
-    (12, 1, 32, 2000, 17, 4),      # 4 splits of 512 tokens: one cluster of 4
-    (12, 1, 32, 2000, 17, 8),      # 8 splits, the last holds 208 tokens: cluster of 8
-    (9, 2, 16, 1500, 3, 2),        # cluster of 2, GQA, M-tile tail
+    (12, 1, 32, 2000, 17, 4),      # 4 splits of 512 tokens
+    (12, 1, 32, 2000, 17, 8),      # 8 splits, the last holds 208 tokens
+    (9, 2, 16, 1500, 3, 2),        # GQA, M-tile tail
+    (10, 2, 12, 900, 40, 3),       # G = 12: no query / output tensor map applies
+    (3, 1, 256, 500, 9, 0),        # G = 256: a query tile is half a sample's heads
 ])
 def test_bifurcated_ctx_paths(cuda_device, ctx_path, n, hkv, G, lc, ld, ctx_splits):
     case = inputs.bifurcated_case(n, hkv * G, hkv, 128, lc, ld, seed=n * 7 + G,
@@ -150,7 +155,6 @@ def test_decode_folded_into_context_kernel(cuda_device, monkeypatch, n, G, ld, d
     tile list of a query tile cut into 1, 4 or 40 runs (40: some splits get
     nothing) or the library's count."""
     monkeypatch.setenv("FD_BIF_CTX", "tc")
-    monkeypatch.setenv("FD_BIF_CLUSTER", "1")
     monkeypatch.setenv("FD_BIF_FOLD", "1")
     case = inputs.bifurcated_case(n, G, 1, 128, 700, ld, seed=n * 13 + G, dec_lens=dec_lens)
     lens = [ld] * n if dec_lens is None else dec_lens

@@ -230,13 +230,16 @@ def test_lse_combine_standalone(cuda_device):
     (1, 1, 128), (64, 37, 128), (5, 100, 128), (3, 300, 64),      # one and several load batches
     (2, 4096, 512), (4, 33, 4), (7, 20, 12), (3, 17, 512),         # widest rows, 1 and 3 chunks per row
     (1500, 9, 128), (1100, 70, 64),                                # grids of many rows
+    (2048, 9, 128), (600, 1, 128), (777, 16, 128), (513, 17, 64),  # warp-per-row layout: one
+    (1000, 32, 128), (900, 31, 4), (530, 20, 100),                 # and two batches, D < 128
 ])
 def test_lse_combine_shapes(cuda_device, R, S, D):
     """Split counts and head dims across the combine's thread layouts: one
     or several batches of partial rows per thread, rows of 1 to 128 float4
     chunks (threads left over when the chunks do not divide the block),
-    grids of few and many rows; empty splits hold NaN, which must not reach
-    the result."""
+    grids of few and many rows (a warp per row for up to 32 splits and head
+    dims up to 128); empty splits hold NaN, which must not reach the
+    result."""
     g = torch.Generator().manual_seed(R * 7 + S * 3 + D)
     po = torch.randn((R, S, D), generator=g)
     pl = torch.randn((R, S), generator=g) * 8
