@@ -192,7 +192,11 @@ struct MmaCfg {
   static constexpr int SMEM_BYTES = 1024 + OFF_Q + Q_BYTES;
   static_assert(NT % WN == 0, "n-tiles split evenly over warps");
   static_assert(W % WN == 0 && BLK % WT == 0 && BPW >= 1, "blocks split evenly over warps");
-  static_assert(WT * GP * (D + 3) * 4 + GP * 4 <= RING_BYTES, "epilogue fits the ring");
+  // Epilogue accumulator rows: D + 4 floats apart (bank-conflict free
+  // stores for the bf16 fragment layout, 2-way with the 8-bit one's swizzle).
+  static constexpr int AS = D + 4;
+  static_assert(WT * GP * 2 * 4 + WT * GP * AS * 4 + (WT + 1) * GP * 4 <= RING_BYTES,
+                "epilogue fits the ring");
   static_assert(Q_BYTES == 0 || OFF_Q % 16 == 0, "staged query rows are 16-byte aligned");
   static_assert(HALF_BYTES % 1024 == 0, "swizzled boxes need 1024-byte alignment");
 };
@@ -225,6 +229,13 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   split_range(len, p.ns, split, begin, end);
   const int ntiles = (end - begin + C::T - 1) / C::T;
   const int kvb = p.kv_batch_broadcast ? 0 : b;
+  // 8-bit caches: the kv head's scales, loaded now so that their latency
+  // hides behind the ring fill (the query set-up and the epilogue use them).
+  float ks_g = 1.f, vs_g = 1.f;
+  if constexpr (C::Q8) {
+    ks_g = p.k_scale[g];
+    vs_g = p.v_scale[g];
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NSTAGE; ++s) {
@@ -269,20 +280,23 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
 
   uint64_t policy = 0;
   int issued = 0;
+  // Warp 0 as a whole issues the copies (warp-uniform operands; one elected
+  // lane issues each instruction): measured on B300, a copy issued by one
+  // lane of a divergent branch costs its warp far more issue time.
   auto issue = [&](int t) {
     const int s = t % C::NSTAGE;
     unsigned char* stage = smem + s * C::STAGE_BYTES;
-    mbar_arrive_expect_tx(&full_bar[s], C::STAGE_BYTES);
+    mbar_arrive_expect_tx_w(&full_bar[s], C::STAGE_BYTES);
     const int tok = begin + t * C::T;
     if (p.block_table == nullptr) {
       if constexpr (C::Q8) {
-        tma_load_4d(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
-        tma_load_4d(stage + C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
+        tma_load_4d_w(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
+        tma_load_4d_w(stage + C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
       } else {
-        tma_load_4d(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
-        tma_load_4d(stage + C::HALF_BYTES, &tmK, &full_bar[s], 64, g, tok, kvb, policy);
-        tma_load_4d(stage + 2 * C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
-        tma_load_4d(stage + 3 * C::HALF_BYTES, &tmV, &full_bar[s], 64, g, tok, kvb, policy);
+        tma_load_4d_w(stage, &tmK, &full_bar[s], 0, g, tok, kvb, policy);
+        tma_load_4d_w(stage + C::HALF_BYTES, &tmK, &full_bar[s], 64, g, tok, kvb, policy);
+        tma_load_4d_w(stage + 2 * C::HALF_BYTES, &tmV, &full_bar[s], 0, g, tok, kvb, policy);
+        tma_load_4d_w(stage + 3 * C::HALF_BYTES, &tmV, &full_bar[s], 64, g, tok, kvb, policy);
       }
     } else {
       // Paged cache: the tile is page_rows-row segments, each inside one page
@@ -296,29 +310,31 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
         const int off = tk % p.page_size;
         const int so = sg * p.page_rows * 128;
         if constexpr (C::Q8) {
-          tma_load_4d(stage + so, &tmK, &full_bar[s], 0, g, off, pid, policy);
-          tma_load_4d(stage + C::HALF_BYTES + so, &tmV, &full_bar[s], 0, g, off, pid, policy);
+          tma_load_4d_w(stage + so, &tmK, &full_bar[s], 0, g, off, pid, policy);
+          tma_load_4d_w(stage + C::HALF_BYTES + so, &tmV, &full_bar[s], 0, g, off, pid, policy);
         } else {
-          tma_load_4d(stage + so, &tmK, &full_bar[s], 0, g, off, pid, policy);
-          tma_load_4d(stage + C::HALF_BYTES + so, &tmK, &full_bar[s], 64, g, off, pid, policy);
-          tma_load_4d(stage + 2 * C::HALF_BYTES + so, &tmV, &full_bar[s], 0, g, off, pid, policy);
-          tma_load_4d(stage + 3 * C::HALF_BYTES + so, &tmV, &full_bar[s], 64, g, off, pid, policy);
+          tma_load_4d_w(stage + so, &tmK, &full_bar[s], 0, g, off, pid, policy);
+          tma_load_4d_w(stage + C::HALF_BYTES + so, &tmK, &full_bar[s], 64, g, off, pid, policy);
+          tma_load_4d_w(stage + 2 * C::HALF_BYTES + so, &tmV, &full_bar[s], 0, g, off, pid, policy);
+          tma_load_4d_w(stage + 3 * C::HALF_BYTES + so, &tmV, &full_bar[s], 64, g, off, pid, policy);
         }
       }
     }
   };
-  // Thread 0 fills the ring.  (A test delay moves the fill after the query
+  // Warp 0 fills the ring.  (A test delay moves the fill after the query
   // staging and spins first, so that the other warps' first waits run out.)
   auto fill_ring = [&]() {
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+    }
     policy = l2_policy_evict_first();
     for (int t = 0; t < C::NSTAGE && t < ntiles; ++t) {
       issue(t);
       ++issued;
     }
   };
-  if (threadIdx.x == 0 && p.producer_delay_ns == 0) fill_ring();
+  if (warp == 0 && p.producer_delay_ns == 0) fill_ring();
 
   // ---- raw query values (fp32 bit patterns), turned into MMA fragments below.
   uint32_t qraw[NPW][8][4];
@@ -382,7 +398,6 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   } else {
     load_q([&](int64_t o) { return uint32_t(reinterpret_cast<const uint16_t*>(p.q)[o]) << 16; });
   }
-  const float ks_g = C::Q8 ? p.k_scale[g] : 1.f;
 
   // ---- query fragments (B operand of S^T = K . Q^T): B[k = dim][n = head]
   // lane holds dims 2(lane%4)+{0,1} and +8 of head (lane/4) of each n-tile.
@@ -476,9 +491,9 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     limB[j] = len - TQ + min(rA + 1, R - 1) / G + 1;
   }
 
-  if (threadIdx.x == 0 && p.producer_delay_ns != 0) {
+  if (warp == 0 && p.producer_delay_ns != 0) {
     const uint64_t t0 = globaltimer_ns();
-    while (globaltimer_ns() - t0 < p.producer_delay_ns) {
+    while (__any_sync(0xffffffffu, globaltimer_ns() - t0 < p.producer_delay_ns)) {
     }
     fill_ring();
   }
@@ -692,10 +707,10 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[s]);
-    if (threadIdx.x == 0 && t >= 1 && issued < ntiles) {
+    if (warp == 0 && t >= 1 && issued < ntiles) {
       const int tp = t - 1;
-      if (mbar_wait_or_abort(&empty_bar[tp % C::NSTAGE], (tp / C::NSTAGE) & 1, abort_s,
-                             p.wait_limit_ns)) {
+      if (__all_sync(0xffffffffu, mbar_wait_or_abort(&empty_bar[tp % C::NSTAGE], (tp / C::NSTAGE) & 1,
+                                                     abort_s, p.wait_limit_ns))) {
         issue(issued);
         ++issued;
       }
@@ -714,7 +729,11 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   // Sum l over the 8 lanes that share each head, then merge the token
   // groups' (m, l, acc) through shared memory (the ring is free now).
   float* ML_s = reinterpret_cast<float*>(smem);              // [WT][GP][2]
-  float* ACC_s = ML_s + C::WT * C::GP * 2;                   // [WT][GP][D]
+  float* ACC_s = ML_s + C::WT * C::GP * 2;                   // [WT][GP][AS]
+  // Position of dim d in an accumulator row: the 8-bit fragments put the
+  // lanes' dims 16 apart, so bits 2..4 are swizzled with d / 16 (float4
+  // groups and even/odd pairs stay together).
+  auto acc_col = [](int d) { return C::Q8 ? (d ^ (((d >> 4) & 7) << 2)) : d; };
 #pragma unroll
   for (int j = 0; j < NPW; ++j) {
 #pragma unroll
@@ -734,20 +753,28 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       // Accumulator rows r = lane/4 and r + 8 of m-tile mt are dims
-      // mt*16 + r and + 8 (bf16), or 16r + 2mt and 16r + 2mt + 1 (8-bit).
-      const int d = C::Q8 ? 16 * (lane >> 2) + 2 * mt : mt * 16 + (lane >> 2);
-      const int d2 = C::Q8 ? d + 1 : d + 8;
-      ACC_s[(wt * C::GP + hA) * C::D + d] = acc[j][mt][0];
-      ACC_s[(wt * C::GP + hA + 1) * C::D + d] = acc[j][mt][1];
-      ACC_s[(wt * C::GP + hA) * C::D + d2] = acc[j][mt][2];
-      ACC_s[(wt * C::GP + hA + 1) * C::D + d2] = acc[j][mt][3];
+      // mt*16 + r and + 8 (bf16), or 16r + 2mt and 16r + 2mt + 1 (8-bit:
+      // one 8-byte store per row).
+      float* rowA = ACC_s + (wt * C::GP + hA) * C::AS;
+      float* rowB = rowA + C::AS;
+      if constexpr (C::Q8) {
+        const int d = acc_col(16 * (lane >> 2) + 2 * mt);
+        *reinterpret_cast<float2*>(rowA + d) = make_float2(acc[j][mt][0], acc[j][mt][2]);
+        *reinterpret_cast<float2*>(rowB + d) = make_float2(acc[j][mt][1], acc[j][mt][3]);
+      } else {
+        const int d = mt * 16 + (lane >> 2);
+        rowA[d] = acc[j][mt][0];
+        rowB[d] = acc[j][mt][1];
+        rowA[d + 8] = acc[j][mt][2];
+        rowB[d + 8] = acc[j][mt][3];
+      }
     }
   }
   __syncthreads();
   // Per head: the common max, each token group's weight 2^(m_w - M) / l_tot
   // (into SF_s) and the log-sum-exp; then every output element is a short
   // weighted sum over the token groups, four elements per thread at a time.
-  float* SF_s = ACC_s + C::WT * C::GP * C::D;                // [WT][GP]
+  float* SF_s = ACC_s + C::WT * C::GP * C::AS;               // [WT][GP]
   float* SB_s = SF_s + C::WT * C::GP;                         // [GP]
   for (int h = threadIdx.x; h < R; h += C::THREADS) {         // h: row (t * G + head)
     float M = kNegInf;
@@ -763,7 +790,7 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
     }
     // 8-bit caches: the kv head's V scale joins the normalisation; int8
     // subtracts the code bias (times the V scale) from the normalised sum.
-    const float vsc = C::Q8 ? p.v_scale[g] : 1.f;
+    const float vsc = vs_g;
     const float inv = lt > 0.f ? vsc / lt : 0.f;
 #pragma unroll
     for (int w = 0; w < C::WT; ++w) SF_s[w * C::GP + h] = f[w] * inv;
@@ -783,7 +810,7 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
 #pragma unroll
     for (int w = 0; w < C::WT; ++w) {
       const float sf = SF_s[w * C::GP + h];
-      const float4 a = *reinterpret_cast<const float4*>(ACC_s + (w * C::GP + h) * C::D + d);
+      const float4 a = *reinterpret_cast<const float4*>(ACC_s + (w * C::GP + h) * C::AS + acc_col(d));
       o.x = fmaf(sf, a.x, o.x);
       o.y = fmaf(sf, a.y, o.y);
       o.z = fmaf(sf, a.z, o.z);
