@@ -1148,55 +1148,51 @@ def run_fd(args, rank, world):
 
 def run_sweep(args):
     """--sweep-splits: per split count (and split-kernel variant, through
-    the library's FD_SPLIT_VARIANT knob), the device time per call of back-
-    to-back calls and the split kernel's event-timed launch; one JSON line
-    each.  A tuning aid, not the benchmark line."""
+    the library's FD_SPLIT_VARIANT knob), the device time per call of graph
+    steps over rotating copies (as the headline is timed) and of direct
+    calls, and the split kernel's event-timed launch; one JSON line each,
+    marking the library heuristic's own choice.  With --sweep-lengths, the
+    batch-1 layer at each of those lengths instead of --workload.  A tuning
+    aid, not the benchmark line."""
     import torch
     import decode_attention_20_b300 as fd
     from decode_attention_20_b300 import _lib
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     L = _lib.lib()
-    w = make_workload(args.workload, dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     stream = torch.cuda.Stream(device=dev)
     variants = args.sweep_variants.split(",") if args.sweep_variants else [""]
-    iters = max(10, min(args.steps, 200))
-    for var in variants:
-        if var:
-            os.environ["FD_SPLIT_VARIANT"] = var
-        else:
-            os.environ.pop("FD_SPLIT_VARIANT", None)
-        for ns in [int(x) for x in args.sweep_splits.split(",")]:
-            w.prepare(L, stream, ns)
-            with torch.cuda.stream(stream):
-                for i in range(3):
-                    w.call(i)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for i in range(iters):
-                    w.call(i)
-                e1.record(stream)
-            stream.synchronize()
-            call_us = e0.elapsed_time(e1) * 1e3 / iters
-            fd.profile_enable(True)
-            with torch.cuda.stream(stream):
-                for i in range(iters):
-                    w.call(i)
-            stream.synchronize()
-            kern = {}
-            for kind, label in [(FD_KERNEL_SPLIT, "split"), (FD_KERNEL_COMBINE, "combine"),
-                                (FD_KERNEL_BIF_CTX, "bif_ctx")]:
-                n, ms = fd.profile_read(kind)
-                if n:
-                    kern[label + "_us"] = round(ms * 1e3 / n, 3)
-            fd.profile_enable(False)
-            fd.check_device_error(stream)
-            row = {"workload": w.name, "variant": var or "default", "splits": ns,
-                   "call_us": round(call_us, 3), **kern}
-            if isinstance(w, DecodeWorkload):
-                row["split_gbs"] = round(w.dominant_units / (kern["split_us"] * 1e-6) / 1e9, 1)
-            print(json.dumps(row), flush=True)
+    shorts = ([f"b1_L{int(x)}" for x in args.sweep_lengths.split(",")] if args.sweep_lengths
+              else [args.workload])
+    for short in shorts:
+        w = make_workload(short, dev)
+        chosen = (fd.choose_num_splits(w.B, w.Hkv, w.Lcap, sms)
+                  if isinstance(w, DecodeWorkload) else 0)
+        for var in variants:
+            if var:
+                os.environ["FD_SPLIT_VARIANT"] = var
+            else:
+                os.environ.pop("FD_SPLIT_VARIANT", None)
+            for ns in [int(x) for x in args.sweep_splits.split(",")]:
+                w.prepare(L, stream, ns)
+                with torch.cuda.stream(stream):
+                    for i in range(max(3, w.nbuf)):
+                        w.call(i)
+                stream.synchronize()
+                t = time_steps(w, stream, 5, 2, args.window_ms / 1e3)
+                direct = time_direct(w, stream, max(32, min(400, w.nbuf * 2)))
+                kern, _ = kernel_times(w, stream, 64, direct)
+                fd.check_device_error(stream)
+                row = {"workload": w.name, "variant": var or "default", "splits": ns,
+                       "heuristic": ns == chosen, "call_us": round(t["us_per_call"], 3),
+                       "direct_us": round(direct, 3), **kern}
+                if isinstance(w, DecodeWorkload):
+                    row["call_gbs"] = round(w.required / (t["us_per_call"] * 1e-6) / 1e9, 1)
+                    row["split_gbs"] = round(w.dominant_units / (kern["split_us"] * 1e-6) / 1e9, 1)
+                print(json.dumps(row), flush=True)
+        del w
+        torch.cuda.empty_cache()
     return 0
 
 
@@ -1274,6 +1270,8 @@ def main(argv=None):
                     help="comma-separated split counts: print one timing line per count instead")
     ap.add_argument("--sweep-variants", default="",
                     help="with --sweep-splits: comma-separated FD_SPLIT_VARIANT values")
+    ap.add_argument("--sweep-lengths", default="",
+                    help="with --sweep-splits: comma-separated batch-1 layer lengths instead of --workload")
     ap.add_argument("--bif-sweep", action="store_true",
                     help="bifurcated vs replicated-context over n, Lc and kv heads instead")
     args = ap.parse_args(argv)

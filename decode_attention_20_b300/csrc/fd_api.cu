@@ -416,10 +416,11 @@ bool mma_group_ok(int64_t G) { return G == 4 || G == 8 || G == 16 || G == 32 || 
 // waves(ns) * (chunk(ns) + kSplitOverheadTokens), where chunk is the
 // fd_split_bounds chunk of a max_len history and waves counts rounds of two
 // CTAs per SM (the default split kernel's occupancy) over batch * kv_heads *
-// (non-empty splits) CTAs; ns is capped at ceil(max_len / 256) and
-// FD_MAX_SPLITS.
+// (non-empty splits) CTAs; ns is capped at ceil(max_len / 64) (chunks of
+// at least one 64-token tile: the split-count sweeps find the fastest call
+// there for histories of 512 to 2048 tokens) and FD_MAX_SPLITS.
 int32_t choose_splits_host(int64_t batch, int64_t kv_heads, int64_t max_len, int32_t num_sms) {
-  constexpr int64_t kMinChunk = 256;
+  constexpr int64_t kMinChunk = 64;
   constexpr int64_t kSplitOverheadTokens = 256;
   if (batch <= 0 || kv_heads <= 0 || max_len <= 0 || num_sms <= 0) return 1;
   const int64_t units = batch * kv_heads;

@@ -23,8 +23,10 @@ import numpy as np
 SPLIT_ALIGN = 64
 # Largest number of splits per (sequence, kv-head).
 MAX_SPLITS = 256
-# Shortest chunk the split heuristic will create (tokens).
-MIN_CHUNK = 256
+# Shortest chunk the split heuristic will create (tokens): one 64-token tile
+# of the split kernel (the split-count sweeps on B300 find the fastest call
+# at 64-token chunks for histories of 512 to 2048 tokens).
+MIN_CHUNK = 64
 # Fixed cost of one wave of split CTAs in the heuristic's makespan model, in
 # tokens of streaming (start-up latency of the first tiles plus the epilogue).
 SPLIT_OVERHEAD_TOKENS = 256

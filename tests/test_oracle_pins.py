@@ -226,9 +226,9 @@ def test_heuristic_properties():
             for L in [1, 64, 256, 512, 1024, 4096, 65536, 131072, 1 << 20]:
                 ns = oracle.choose_num_splits_ref(B, hkv, L, sms)
                 assert 1 <= ns <= oracle.MAX_SPLITS
-                assert ns <= max(1, -(-L // oracle.MIN_CHUNK))   # chunks of >= 256 tokens
-    # short history -> no splitting
-    assert oracle.choose_num_splits_ref(1, 8, 200, sms) == 1
+                assert ns <= max(1, -(-L // oracle.MIN_CHUNK))   # chunks of >= 64 tokens
+    # a history of one tile -> no splitting
+    assert oracle.choose_num_splits_ref(1, 8, 64, sms) == 1
     assert oracle.choose_num_splits_ref(0, 8, 65536, 148) == 1
 
 
@@ -257,6 +257,10 @@ def test_heuristic_workload_choices():
     assert oracle.choose_num_splits_ref(1, 8, 65536, 148) == 37
     assert oracle.choose_num_splits_ref(4, 8, 131072, 148) == 9
     assert oracle.choose_num_splits_ref(32, 8, 32768, 148) == 8
+    # short batch-1 histories: one 64-token tile per split where one wave
+    # holds them (the fastest calls of the sweeps at 512 .. 2048 tokens)
+    assert [oracle.choose_num_splits_ref(1, 8, L, 148) for L in (512, 1024, 2048, 4096, 8192)] == \
+        [8, 16, 32, 32, 32]
 
 
 def test_required_bytes_config_flash_decoding_64k():
