@@ -165,3 +165,40 @@ def test_decode_folded_into_context_kernel(cuda_device, monkeypatch, n, G, ld, d
     O_ref, L_ref = _ref(case)
     assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16,
                   f"fold n={n} G={G} ld={ld} ns={ctx_splits}")
+
+
+@pytest.mark.parametrize("lc,ctx_splits", [(1, 0), (57, 0), (57, 3), (127, 2)])
+def test_decode_folded_with_context_shorter_than_a_tile(cuda_device, monkeypatch, lc, ctx_splits):
+    """The folded decode part when the whole shared context is shorter than
+    one 128-token tile: the context run of every query tile is a single
+    partial tile (one token at the least), followed by the samples' decode
+    tiles; split counts that leave some runs with decode tiles only."""
+    monkeypatch.setenv("FD_BIF_CTX", "tc")
+    monkeypatch.setenv("FD_BIF_FOLD", "1")
+    case = inputs.bifurcated_case(9, 32, 1, 128, lc, 300, seed=lc + 5,
+                                  dec_lens=[300, 1, 0, 129, 128, 257, 64, 2, 299])
+    O, L = _run(case, ctx_splits)
+    O_ref, L_ref = _ref(case)
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16,
+                  f"short context lc={lc} ns={ctx_splits}")
+
+
+@pytest.mark.parametrize("ctx_splits", [0, 1, 5])
+def test_decode_folded_with_peaked_decode_keys(cuda_device, monkeypatch, ctx_splits):
+    """Decode keys scaled by 8 (exact in bf16) at a seeded 5% of each
+    sample's own positions: the running maximum jumps inside a sample's
+    decode tiles, after the context tiles of the same run, so the O
+    accumulator is rescaled mid-run for some rows and not for others."""
+    monkeypatch.setenv("FD_BIF_CTX", "tc")
+    monkeypatch.setenv("FD_BIF_FOLD", "1")
+    case = inputs.bifurcated_case(12, 32, 1, 128, 1000, 384, seed=91,
+                                  dec_lens=[384, 200, 0, 1, 383, 256, 129, 64, 300, 17, 128, 250])
+    gen = torch.Generator().manual_seed(92)
+    for i, n in enumerate(case.lens):
+        if n:
+            pos = torch.randperm(n, generator=gen)[:max(1, n // 20)]
+            case.k_dec[i, pos] = case.k_dec[i, pos] * 8
+    O, L = _run(case, ctx_splits)
+    O_ref, L_ref = _ref(case)
+    assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16,
+                  f"peaked decode keys ns={ctx_splits}")
