@@ -23,13 +23,6 @@
 namespace fd {
 cudaError_t read_and_clear_device_error(unsigned int* bits, cudaStream_t st);
 
-// Tokens per split of a len-token history cut into ns splits (the chunk of
-// fd_split_bounds).
-int split_chunk(int64_t len, int ns) {
-  if (ns < 1 || len <= 0) return 0;
-  const int64_t per = (len + ns - 1) / ns;
-  return (int)(((per + kSplitAlign - 1) / kSplitAlign) * kSplitAlign);
-}
 }
 
 using namespace fd;
@@ -377,14 +370,19 @@ bool tma_ok(const DecodeDesc& d, const void* kd, const void* vd, const int64_t (
 
 // Which split kernel variant to use.  Tuning and test knob, read on every
 // call: FD_SPLIT_VARIANT = "cuda" forces the CUDA-core kernel, "mma0" /
-// "mma1" / "mma2" pick a tensor-core tiling.  Unset: "mma2" (3-stage ring of
-// 64-token tiles, two CTAs per SM): in the split-count sweeps it matched the
-// 6-stage one-CTA-per-SM tiling at batch 1 and beat it by 5% on the ragged
-// batch, the second resident CTA covering the first one's start and tail.
-int split_variant(int64_t chunk_tokens) {
-  (void)chunk_tokens;
+// "mma1" / "mma2" pick a tensor-core tiling.  Unset, from the variant sweeps
+// on B300 (batch-1 64K layer, 32 and 37 splits):
+//  - bf16 caches: "mma2" (3-stage ring of 64-token tiles, two CTAs per SM):
+//    it matched the 6-stage one-CTA-per-SM tiling at batch 1 and beat it by
+//    5% on the ragged batch, the second resident CTA covering the first
+//    one's start and tail; paged caches 46.2 us against 53.2 and 71.3.
+//  - 8-bit caches: "mma1" (8 warps, 128-token tiles, 3 stages): e4m3 33.2 us
+//    against 36.2 (4 warps) and 38.8 (64-token tiles), the extra warps
+//    hiding the latency of the code conversions; int8 28.9 us, level with
+//    4 warps and 2 us ahead of 64-token tiles.
+int split_variant(int kv_kind) {
   const char* e = getenv("FD_SPLIT_VARIANT");
-  if (e == nullptr || e[0] == 0) return 2;
+  if (e == nullptr || e[0] == 0) return (kv_kind == kKvI8 || kv_kind == kKvE4m3) ? 1 : 2;
   if (!strcmp(e, "cuda")) return -1;
   if (!strcmp(e, "mma1")) return 1;
   if (!strcmp(e, "mma2")) return 2;
@@ -520,7 +518,7 @@ fd_status enqueue_split(const DecodeDesc& d, const fd_tensor* q, const fd_tensor
   const int64_t kv_batch = pg ? pg->num_pages : (kv_broadcast ? 1 : d.B);
   const int64_t map_len = pg ? pg->page_size : d.Lcap;
   const int64_t strides[6] = {p.k_sl, p.k_sh, p.v_sl, p.v_sh, p.k_sb, p.v_sb};
-  const int variant = split_variant(split_chunk(d.Lcap, ns));
+  const int variant = split_variant(p.kv_kind);
   // The tensor-core kernel takes bf16 queries over a bf16 cache, or bf16 /
   // f32 queries over an 8-bit cache (converted to f16 in the kernel).
   const int mtile = mma_tile_tokens(variant, p.kv_kind);

@@ -155,7 +155,5 @@ cudaError_t launch_bif_ctx(const BifCtxParams& p, const CUtensorMap& tmK, const 
 // Tile height (tokens) of the TMA split kernel; the tensor-map box uses it.
 constexpr int kSplitTileTokens = 64;
 
-// Host-side helpers (fd_api.cu).
-int split_chunk(int64_t len, int ns);
 
 }  // namespace fd

@@ -30,13 +30,15 @@ pytestmark = pytest.mark.gpu
 KINDS = ["int8", "e4m3"]
 
 
-@pytest.fixture(params=["mma", "cuda"])
+@pytest.fixture(params=["mma", "mma0", "mma2", "cuda"])
 def path(request, monkeypatch):
-    """Tensor-core split kernel (default) or the CUDA-core kernel."""
-    if request.param == "cuda":
-        monkeypatch.setenv("FD_SPLIT_VARIANT", "cuda")
-    else:
+    """Tensor-core split kernel: the default tiling (8 warps, 128-token
+    tiles for 8-bit caches), the 4-warp 128-token one (mma0), the 64-token
+    6-stage one (mma2); or the CUDA-core kernel."""
+    if request.param == "mma":
         monkeypatch.delenv("FD_SPLIT_VARIANT", raising=False)
+    else:
+        monkeypatch.setenv("FD_SPLIT_VARIANT", request.param)
     return request.param
 
 
