@@ -94,9 +94,13 @@ def rotation_copies(per_copy_bytes):
 # profiles/traffic.json is used only while their code (comments and
 # whitespace aside) hashes to the value it was captured with; otherwise the
 # kernel has changed and traffic is null.
+# The kernel's code and the host code that picks its instance (tiling,
+# split count): a capture stays valid only while both are unchanged.
 KERNEL_SOURCES = {
-    FD_KERNEL_SPLIT: ["fd_split_mma.cuh", "fd_split.cuh", "fd_device.cuh"],
-    FD_KERNEL_BIF_CTX: ["fd_bif_ctx.cuh", "fd_tcgen05.cuh", "fd_split.cuh", "fd_device.cuh"],
+    FD_KERNEL_SPLIT: ["fd_split_mma.cuh", "fd_split.cuh", "fd_device.cuh", "fd_kernels.cu",
+                      "fd_api.cu"],
+    FD_KERNEL_BIF_CTX: ["fd_bif_ctx.cuh", "fd_tcgen05.cuh", "fd_split.cuh", "fd_device.cuh",
+                        "fd_kernels.cu", "fd_api.cu"],
 }
 
 
