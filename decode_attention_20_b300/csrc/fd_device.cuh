@@ -178,59 +178,11 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 
 // ------------------------------------------------------- bulk stores
 
-// Asynchronous bulk copy shared -> global of `bytes` (a multiple of 16; both
-// addresses 16-byte aligned), tracked in this thread's bulk group.
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                   reinterpret_cast<uint64_t>(gdst)),
-               "r"(smem_u32(ssrc)), "r"(bytes)
-               : "memory");
-}
-// Commit this thread's bulk copies and wait until they have completed.
-__device__ __forceinline__ void bulk_store_commit_and_wait() {
-  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
-}
 // Commit this thread's bulk copies and wait until their shared-memory
 // sources have been read (the source may then be reused or released; the
 // global writes complete with the grid).
 __device__ __forceinline__ void bulk_store_commit_and_wait_read() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// ------------------------------------------------------- thread-block clusters
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Shared-memory address `saddr` of this CTA mapped to CTA `rank` of the
-// cluster (distributed shared memory).
-__device__ __forceinline__ uint32_t dsmem_map(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-__device__ __forceinline__ float2 dsmem_ld_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
-               : "memory");
-  return v;
-}
-// Every thread of every CTA of the cluster: writes before are visible to
-// reads after (release / acquire at cluster scope).
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------------- named barriers

@@ -83,59 +83,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
 
 // ------------------------------------------------------------ MMA
 
-// D[tmem] (+)= A[smem] * B[smem]^T (one CTA); accumulate = false overwrites.
-__device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T (one CTA): A is read from tensor memory,
-// row i of A in lane i, two consecutive 16-bit K elements per 32-bit column
-// (the lower K index in the low half); `a_tmem` addresses its first column.
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                            uint32_t idesc, bool accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
-      : "memory");
-}
-
-// The same two MMAs with the descriptors passed as 32-bit halves, the
-// accumulate flag a compile-time constant: the issuing thread then spends
-// one integer add per MMA on its descriptors (a descriptor rebuilt from an
-// address per MMA costs the issuer more than the 64 cycles a 128x128x16 MMA
-// takes on the tensor core, measured on B300).
-template <bool ACC>
-__device__ __forceinline__ void mma_bf16_ts_c(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
-                                              uint32_t b_hi, uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
-      "mov.b64 bd, {%2, %3};\n\t"
-      "setp.ne.b32 p, %5, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC ? 1 : 0)
-      : "memory");
-}
-template <bool ACC>
-__device__ __forceinline__ void mma_bf16_ss_c(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
-                                              uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t.reg .b64 ad, bd;\n\t"
-      "mov.b64 ad, {%1, %2};\n\t"
-      "mov.b64 bd, {%3, %4};\n\t"
-      "setp.ne.b32 p, %6, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %5, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC ? 1 : 0)
-      : "memory");
-}
-
+// D[tmem] (+)= A[tmem] * B[smem]^T (one CTA; ACC = false overwrites): A is
+// read from tensor memory, row i of A in lane i, two consecutive 16-bit K
+// elements per 32-bit column (the lower K index in the low half); `a_tmem`
+// addresses its first column.
 // Whole-warp forms.  Every lane of a converged warp executes the call with
 // the same (warp-uniform) operands and one elected lane issues the
 // instruction.  Issuing from warp-uniform code lets the operands live in
@@ -153,6 +104,8 @@ __device__ __forceinline__ void mma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, 
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(ACC ? 1 : 0)
       : "memory");
 }
+// Arrive once on `bar` when every tcgen05 operation the elected lane issued
+// so far has completed.
 __device__ __forceinline__ void commit_w(uint64_t* bar) {
   asm volatile(
       "{\n\t.reg .pred e;\n\t"
@@ -176,14 +129,6 @@ __device__ __forceinline__ void cp_128x256b_w(uint32_t taddr, uint64_t s_desc) {
       : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 operation this thread issued so far
-// has completed.
-__device__ __forceinline__ void commit(uint64_t* bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_u32(bar))
-      : "memory");
-}
 
 // ------------------------------------------------------------ TMEM <-> registers
 
