@@ -207,7 +207,6 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
                      const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
   using C = MmaCfg<KVQ, NT, WN, W, T, NSTAGE>;
-  if (!p.late_wait) pdl_wait_prerequisites();   // launched with PDL: no memory access before this
   constexpr int NPW = C::NPW;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -224,6 +223,21 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   const int wn = warp % WN;                    // n-tile group
   const int wt = warp / WN;                    // token group
 
+  // Set-up that reads no global memory (the ring's barriers, the tensor maps
+  // in parameter space) runs before the launch wait, so it overlaps the tail
+  // of the preceding kernel on the stream.
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NSTAGE; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], W);
+    }
+    *abort_s = 0;
+    fence_barrier_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (!p.late_wait) pdl_wait_prerequisites();   // launched with PDL: no global memory access before this
+
   const int len = resolve_len(p.seqlens, b, p.Lcap);
   int begin, end;
   split_range(len, p.ns, split, begin, end);
@@ -235,15 +249,6 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   if constexpr (C::Q8) {
     ks_g = p.k_scale[g];
     vs_g = p.v_scale[g];
-  }
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NSTAGE; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], W);
-    }
-    *abort_s = 0;
-    fence_barrier_init();
   }
 
   // Rows of the kv head: (query token t, head in group hl), row = t * G + hl
@@ -324,10 +329,6 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
   // Warp 0 fills the ring.  (A test delay moves the fill after the query
   // staging and spins first, so that the other warps' first waits run out.)
   auto fill_ring = [&]() {
-    if (lane == 0) {
-      prefetch_tensormap(&tmK);
-      prefetch_tensormap(&tmV);
-    }
     policy = l2_policy_evict_first();
     for (int t = 0; t < C::NSTAGE && t < ntiles; ++t) {
       issue(t);
