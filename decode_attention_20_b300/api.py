@@ -22,6 +22,13 @@ _DT = {torch.float32: _lib.FD_F32, torch.bfloat16: _lib.FD_BF16, torch.int32: _l
        torch.int8: _lib.FD_I8, torch.float8_e4m3fn: _lib.FD_E4M3}
 
 
+# Descriptors by value: (pointer, dtype, shape, strides) -> fd_tensor.  A
+# descriptor holds nothing but those values, so a cached one is the one that
+# would be built; a decode loop that reuses its buffers builds each once.
+_DESC_CACHE: dict = {}
+_DESC_CACHE_MAX = 512
+
+
 def _desc(t: Optional[torch.Tensor], name: str):
     if t is None:
         return None
@@ -29,19 +36,33 @@ def _desc(t: Optional[torch.Tensor], name: str):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    key = (t.data_ptr(), t.dtype, t.shape, t.stride())
+    d = _DESC_CACHE.get(key)
+    if d is not None:
+        return d
     if t.dtype not in _DT:
         raise TypeError(f"{name}: unsupported dtype {t.dtype}")
     if t.dim() > 4:
         raise ValueError(f"{name}: at most 4 dims")
-    return _lib.raw_descriptor(t.data_ptr(), _DT[t.dtype], list(t.shape), list(t.stride()))
+    d = _lib.raw_descriptor(key[0], _DT[t.dtype], list(key[2]), list(key[3]))
+    if len(_DESC_CACHE) >= _DESC_CACHE_MAX:
+        _DESC_CACHE.clear()
+    _DESC_CACHE[key] = d
+    return d
 
 
 def _ref(d):
     return ctypes.byref(d) if d is not None else None
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(stream):
     if stream is None:
+        if _raw_stream is not None:
+            # The current stream's handle without building a Stream object.
+            return ctypes.c_void_p(_raw_stream(torch.cuda.current_device()))
         return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     if isinstance(stream, torch.cuda.Stream):
         return ctypes.c_void_p(stream.cuda_stream)
