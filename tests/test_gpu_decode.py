@@ -297,3 +297,19 @@ def test_nan_padding_past_the_lengths_is_ignored(cuda_device, variant):
         O_ref, L_ref = oracle.decode_attention_ref(to_f64(case.q), to_f64(case.k), to_f64(case.v),
                                                    _lens_np(case), case.scale)
         assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, torch.bfloat16, f"{variant} nan pad ns={ns}")
+
+
+def test_descriptor_cache_is_by_value(cuda_device):
+    """The binding caches fd_tensor descriptors by (pointer, dtype, shape,
+    strides): the same values give the same descriptor, another view of the
+    same memory its own one, with that view's strides."""
+    from decode_attention_20_b300 import api
+    t = torch.zeros((2, 3, 4), device="cuda")
+    a = api._desc(t, "t")
+    assert api._desc(t.view(2, 3, 4), "t") is a
+    v = t.transpose(0, 1)
+    d = api._desc(v, "v")
+    assert d is not a
+    assert [d.shape[i] for i in range(3)] == list(v.shape)
+    assert [d.stride[i] for i in range(3)] == list(v.stride())
+    assert d.data == a.data == t.data_ptr()
