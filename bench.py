@@ -33,9 +33,11 @@ Prints ONE JSON line (rank 0):
                that together exceed L2 (C sized so that the steps span about
                --window-ms); CUDA events on the launching stream, a barrier
                and a synchronise on both sides.  ms_per_step is one step.
-  e2e          microseconds per step through the Python API: H2D from pinned
-               host memory of the step's new inputs (query, one new K/V row per
-               sequence), the call, D2H of out (+ lse), synchronised per step
+  e2e          microseconds per step through the Python API: one H2D from
+               pinned host memory of the step's new inputs (query, one new K/V
+               row per sequence, packed in one buffer), the rows written into
+               the cache, the call, one D2H of out + lse (one buffer),
+               synchronised per step
   roofline     the dominant kernel's algorithmic bytes (or FLOPs) per launch /
                its mean CUDA-event duration (launches queued back to back,
                without programmatic dependent launch), against the peak
@@ -247,6 +249,27 @@ def _rows(t, n):
     return t.view(n, -1)
 
 
+def _staging(device, specs):
+    """One pinned host buffer and one device buffer holding tensors of the
+    given (shape, dtype) specs at 256-byte aligned offsets, so that a step
+    moves all its inputs (or all its results) in one copy.  Returns (host
+    buffer, device buffer, host views, device views)."""
+    import numpy as np
+    import torch
+    sizes = [int(np.prod(shape)) * torch.empty((), dtype=dt).element_size() for shape, dt in specs]
+    offs, off = [], 0
+    for n in sizes:
+        offs.append(off)
+        off = (off + n + 255) // 256 * 256
+    h = torch.empty(off, dtype=torch.uint8).pin_memory()
+    d = torch.empty(off, dtype=torch.uint8, device=device)
+
+    def views(buf):
+        return [buf[o:o + n].view(dt).view(shape) for (shape, dt), o, n in zip(specs, offs, sizes)]
+
+    return h, d, views(h), views(d)
+
+
 def _host_loop_us(stream, steps, step, warmup=5):
     """Wall-clock microseconds per call of step(i) on `stream`, after
     `warmup` untimed calls (first-use costs: lazy kernel loading, pinned
@@ -319,50 +342,44 @@ class DecodeWorkload(Workload):
         if st:
             raise RuntimeError(self.L.fd_last_error().decode())
 
-    def api_call(self, q, k, v, stream):
+    def api_call(self, q, k, v, stream, out=None, lse=None):
         import decode_attention_20_b300 as fd
-        fd.decode_attention(q, k, v, self.seqlens_dev, self.ns, self.case.scale, out=self.out,
-                            lse=self.lse, stream=stream)
+        fd.decode_attention(q, k, v, self.seqlens_dev, self.ns, self.case.scale,
+                            out=self.out if out is None else out,
+                            lse=self.lse if lse is None else lse, stream=stream)
 
     def e2e(self, stream, steps):
-        """Per step: H2D of the new query and one new K/V row per sequence
-        (written at position len_b - 1), the call, D2H of out + lse."""
+        """Per step: one H2D of the new query and one new K/V row per
+        sequence (packed in one pinned buffer; the rows are then written at
+        position len_b - 1), the call, one D2H of out + lse (one buffer)."""
         import torch
-        import decode_attention_20_b300 as fd
         c = self.case
-        hq = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
-        hq.copy_(c.q.cpu())
+        dev = c.q.device
         # the Tq newest rows of every sequence (positions len_b - Tq .. len_b - 1)
         pos = [(b, j) for b, n in enumerate(self.lens) for j in range(max(0, n - self.Tq), max(n, 1))]
         nr = len(pos)
-        hk = torch.empty((nr, self.Hkv, self.D), dtype=c.k.dtype).pin_memory()
-        hv = torch.empty_like(hk).pin_memory()
+        row = (nr, self.Hkv * self.D)
+        h_in, d_in, (hq, hk, hv), (dq, dk, dv) = _staging(
+            dev, [(tuple(c.q.shape), c.q.dtype), (row, c.k.dtype), (row, c.k.dtype)])
+        hq.copy_(c.q.cpu())
         for i, (b, j) in enumerate(pos):
-            hk[i].copy_(c.k[b, j].cpu())
-            hv[i].copy_(c.v[b, j].cpu())
-        hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
-        hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
-        rows = torch.tensor([b * self.Lcap + j for b, j in pos], dtype=torch.int64,
-                            device=c.q.device)
-        dk = torch.empty((nr, self.Hkv * self.D), dtype=c.k.dtype, device=c.q.device)
-        dv = torch.empty_like(dk)
+            hk[i].copy_(c.k[b, j].reshape(-1).cpu())
+            hv[i].copy_(c.v[b, j].reshape(-1).cpu())
+        h_res, d_res, _, (dout, dlse) = _staging(
+            dev, [(tuple(self.out.shape), torch.float32), (tuple(self.lse.shape), torch.float32)])
+        rows = torch.tensor([b * self.Lcap + j for b, j in pos], dtype=torch.int64, device=dev)
 
         def step(i):
             kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
-            c.q.copy_(hq, non_blocking=True)
-            dk.copy_(hk.view(nr, -1), non_blocking=True)
-            dv.copy_(hv.view(nr, -1), non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
             _rows(kb, self.B * self.Lcap).index_copy_(0, rows, _rows(dk, nr))
             _rows(vb, self.B * self.Lcap).index_copy_(0, rows, _rows(dv, nr))
-            self.api_call(c.q, kb, vb, stream)
-            hout.copy_(self.out, non_blocking=True)
-            hlse.copy_(self.lse, non_blocking=True)
+            self.api_call(dq, kb, vb, stream, out=dout, lse=dlse)
+            h_res.copy_(d_res, non_blocking=True)
             stream.synchronize()
 
         us = _host_loop_us(stream, steps, step)
-        h2d = hq.numel() * hq.element_size() + hk.numel() * hk.element_size() * 2
-        d2h = hout.numel() * 4 + hlse.numel() * 4
-        return us, h2d, d2h
+        return us, h_in.numel(), h_res.numel()
 
     def _oracle_inputs(self, n0):
         c = self.case
@@ -476,44 +493,39 @@ class BifWorkload(Workload):
         return e0.elapsed_time(e1) * 1e3 / steps, kv
 
     def e2e(self, stream, steps):
-        """Per step: H2D of the queries and one new decode K/V row per sample,
-        the call, D2H of out + lse."""
+        """Per step: one H2D of the queries and one new decode K/V row per
+        sample (one pinned buffer; the rows are then written into the decode
+        caches), the call, one D2H of out + lse (one buffer)."""
         import torch
         import decode_attention_20_b300 as fd
         c = self.case
-        hq = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
+        dev = c.q.device
+        rshape = (self.n, self.Hkv * self.D)
+        h_in, d_in, (hq, hk, hv), (dq, dk, dv) = _staging(
+            dev, [(tuple(c.q.shape), c.q.dtype), (rshape, c.k_dec.dtype), (rshape, c.k_dec.dtype)])
         hq.copy_(c.q.cpu())
-        hk = torch.empty((self.n, self.Hkv, self.D), dtype=c.k_dec.dtype).pin_memory()
-        hv = torch.empty_like(hk).pin_memory()
         pos = [max(0, x - 1) for x in c.lens]
         for b in range(self.n):
-            hk[b].copy_(c.k_dec[b, pos[b]].cpu())
-            hv[b].copy_(c.v_dec[b, pos[b]].cpu())
-        hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
-        hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+            hk[b].copy_(c.k_dec[b, pos[b]].reshape(-1).cpu())
+            hv[b].copy_(c.v_dec[b, pos[b]].reshape(-1).cpu())
+        h_res, d_res, _, (dout, dlse) = _staging(
+            dev, [(tuple(self.out.shape), torch.float32), (tuple(self.lse.shape), torch.float32)])
         rows = torch.tensor([b * self.Ld + pos[b] for b in range(self.n)], dtype=torch.int64,
-                            device=c.q.device)
-        dk = torch.empty((self.n, self.Hkv * self.D), dtype=c.k_dec.dtype, device=c.q.device)
-        dv = torch.empty_like(dk)
+                            device=dev)
 
         def step(i):
-            q, kc, vc, kd, vd = self.bufs[i % self.nbuf]
-            q.copy_(hq, non_blocking=True)
-            dk.copy_(hk.view(self.n, -1), non_blocking=True)
-            dv.copy_(hv.view(self.n, -1), non_blocking=True)
+            _, kc, vc, kd, vd = self.bufs[i % self.nbuf]
+            d_in.copy_(h_in, non_blocking=True)
             kd.view(self.n * self.Ld, -1).index_copy_(0, rows, dk)
             vd.view(self.n * self.Ld, -1).index_copy_(0, rows, dv)
-            fd.bifurcated_attention(q, kc, vc, kd, vd, self.dec_dev, c.scale, out=self.out,
-                                    lse=self.lse, ctx_splits=self.ns, return_lse=True,
+            fd.bifurcated_attention(dq, kc, vc, kd, vd, self.dec_dev, c.scale, out=dout,
+                                    lse=dlse, ctx_splits=self.ns, return_lse=True,
                                     stream=stream)
-            hout.copy_(self.out, non_blocking=True)
-            hlse.copy_(self.lse, non_blocking=True)
+            h_res.copy_(d_res, non_blocking=True)
             stream.synchronize()
 
         us = _host_loop_us(stream, steps, step)
-        h2d = hq.numel() * 2 + hk.numel() * 2 * 2
-        d2h = hout.numel() * 4 + hlse.numel() * 4
-        return us, h2d, d2h
+        return us, h_in.numel(), h_res.numel()
 
     def oracle_sample(self):
         """Time the oracle once on a fixed sample: sample 0 over the whole
@@ -594,36 +606,37 @@ class PagedWorkload(DecodeWorkload):
             raise RuntimeError(self.L.fd_last_error().decode())
 
     def e2e(self, stream, steps):
-        """Per step: H2D of the new query and of the newest token's K/V row
-        into its page, the paged call, D2H of out + lse."""
+        """Per step: one H2D of the new query and the newest token's K/V row
+        (one pinned buffer; the row is then written into its page), the paged
+        call, one D2H of out + lse (one buffer)."""
         import torch
         import decode_attention_20_b300 as fd
         c = self.pcase
-        hq = torch.empty(c.q.shape, dtype=c.q.dtype).pin_memory()
-        hq.copy_(c.q.cpu())
+        dev = c.q.device
         last = self.Lcap - 1
         pid = int(c.block_table[0, last // self.page_size])
         row = pid * self.page_size + last % self.page_size
-        hk = torch.empty((1, self.Hkv * self.D), dtype=c.k_pages.dtype).pin_memory()
-        hv = torch.empty_like(hk).pin_memory()
+        rshape = (1, self.Hkv * self.D)
+        h_in, d_in, (hq, hk, hv), (dq, dk, dv) = _staging(
+            dev, [(tuple(c.q.shape), c.q.dtype), (rshape, c.k_pages.dtype), (rshape, c.k_pages.dtype)])
+        hq.copy_(c.q.cpu())
         hk.copy_(c.k_pages.view(-1, self.Hkv * self.D)[row:row + 1].cpu())
         hv.copy_(c.v_pages.view(-1, self.Hkv * self.D)[row:row + 1].cpu())
-        hout = torch.empty(self.out.shape, dtype=torch.float32).pin_memory()
-        hlse = torch.empty(self.lse.shape, dtype=torch.float32).pin_memory()
+        h_res, d_res, _, (dout, dlse) = _staging(
+            dev, [(tuple(self.out.shape), torch.float32), (tuple(self.lse.shape), torch.float32)])
 
         def step(i):
             kb, vb = self.ks[i % self.nbuf], self.vs[i % self.nbuf]
-            c.q.copy_(hq, non_blocking=True)
-            kb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(hk, non_blocking=True)
-            vb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(hv, non_blocking=True)
-            fd.decode_attention_paged(c.q, kb, vb, self.bt_dev, None, self.ns, c.scale,
-                                      out=self.out, lse=self.lse, stream=stream)
-            hout.copy_(self.out, non_blocking=True)
-            hlse.copy_(self.lse, non_blocking=True)
+            d_in.copy_(h_in, non_blocking=True)
+            kb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(dk, non_blocking=True)
+            vb.view(-1, self.Hkv * self.D)[row:row + 1].copy_(dv, non_blocking=True)
+            fd.decode_attention_paged(dq, kb, vb, self.bt_dev, None, self.ns, c.scale,
+                                      out=dout, lse=dlse, stream=stream)
+            h_res.copy_(d_res, non_blocking=True)
             stream.synchronize()
 
         us = _host_loop_us(stream, steps, step)
-        return us, hq.numel() * 2 + hk.numel() * 2 * 2, hout.numel() * 4 + hlse.numel() * 4
+        return us, h_in.numel(), h_res.numel()
 
 
 class MultiWorkload(DecodeWorkload):
@@ -650,10 +663,11 @@ class MultiWorkload(DecodeWorkload):
         if st:
             raise RuntimeError(self.L.fd_last_error().decode())
 
-    def api_call(self, q, k, v, stream):
+    def api_call(self, q, k, v, stream, out=None, lse=None):
         import decode_attention_20_b300 as fd
         fd.decode_attention_multi(q, k, v, self.seqlens_dev, self.ns, self.case.scale,
-                                  out=self.out, lse=self.lse, stream=stream)
+                                  out=self.out if out is None else out,
+                                  lse=self.lse if lse is None else lse, stream=stream)
 
     def _oracle_call(self, q, k, v, T):
         import oracle
@@ -694,11 +708,12 @@ class QuantWorkload(DecodeWorkload):
         if st:
             raise RuntimeError(self.L.fd_last_error().decode())
 
-    def api_call(self, q, k, v, stream):
+    def api_call(self, q, k, v, stream, out=None, lse=None):
         import decode_attention_20_b300 as fd
         c = self.case
         fd.decode_attention_quant(q, k, v, c.k_scale, c.v_scale, self.seqlens_dev, self.ns,
-                                  c.scale, out=self.out, lse=self.lse, stream=stream)
+                                  c.scale, out=self.out if out is None else out,
+                                  lse=self.lse if lse is None else lse, stream=stream)
 
     def _oracle_inputs(self, n0):
         import torch
