@@ -808,6 +808,29 @@ def cpu_baseline(w, budget_s=3.0, min_reps=3, max_reps=20):
             "sample": f"{sample}; best of {reps}"}
 
 
+def cpu_baseline_ref_arm(w, short):
+    """The reference arm's own measurement of this workload, run as a
+    separate process (`bench.py --impl reference`), so that the GPU line's
+    cpu_baseline and the reference line come from the same code under the
+    same process conditions (a host-memory-bound fp64 oracle is sensitive to
+    what else the process did before).  Steps: 20 for a sample under 0.2 s,
+    5 under 1.5 s, else 3.  Falls back to timing in this process."""
+    one = cpu_baseline(w, budget_s=0.0, min_reps=1, max_reps=1)
+    per_s = one["value"] * 1e-6
+    steps = 20 if per_s < 0.2 else 5 if per_s < 1.5 else 3
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", short,
+           "--steps", str(steps), "--warmup", "1"]
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env)
+        line = next(json.loads(l) for l in r.stdout.splitlines() if l.startswith("{"))
+        cb = dict(line["cpu_baseline"])
+        cb["sample"] += "; measured by the reference arm in a separate process"
+        return cb
+    except Exception:                                   # noqa: BLE001 (fall back to this process)
+        return cpu_baseline(w)
+
+
 # ------------------------------------------------------------------ reference arm
 
 def run_reference(args, rank, world):
@@ -1167,7 +1190,7 @@ def run_fd(args, rank, world):
     if configs:
         line["configs"] = configs
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline_ref_arm(w, args.workload)
     print(json.dumps(line), flush=True)
     return 0
 
