@@ -38,6 +38,8 @@
 // PV product as one f16 value (11 significant bits), one MMA.
 #pragma once
 
+#include <type_traits>
+
 #include "fd_split.cuh"
 
 namespace fd {
@@ -133,10 +135,14 @@ __device__ __forceinline__ void q8_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t
     lo = __byte_perm(x, 0x64646464u, 0x5140);
     hi = __byte_perm(x, 0x64646464u, 0x7362);
   } else {
-    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(x & 0xffffu), __NV_E4M3);
-    const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(x >> 16), __NV_E4M3);
-    lo = uint32_t(a.x) | (uint32_t(a.y) << 16);
-    hi = uint32_t(b.x) | (uint32_t(b.y) << 16);
+    // Each half of the word is one e4m3 pair; the conversion writes the
+    // f16 pair straight into a 32-bit register (element order kept).
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
   }
 }
 
@@ -686,23 +692,32 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
           const uint4 vB = lds128_q8<KVQ>(vbase + swz128(vr + 1, ch));
           const uint4 vC = lds128_q8<KVQ>(vbase + swz128(vr + 8, ch));
           const uint4 vD = lds128_q8<KVQ>(vbase + swz128(vr + 9, ch));
+          // e4m3 codes past the split may be NaN: the last, partial tile of
+          // a range clears them after the conversion (a tile-uniform
+          // branch, so full tiles spend nothing on it).
+          auto pv = [&](auto clear) {
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-            const uint32_t iAB = __byte_perm(u4_word(vA, mt >> 1), u4_word(vB, mt >> 1), sel);
-            const uint32_t iCD = __byte_perm(u4_word(vC, mt >> 1), u4_word(vD, mt >> 1), sel);
-            uint32_t a0, a1, a2, a3;
-            q8_to_f16x2x2<KVQ>(iAB, a0, a1);
-            q8_to_f16x2x2<KVQ>(iCD, a2, a3);
-            if constexpr (KVQ == 2) {      // e4m3 codes past the split may be NaN
-              a0 &= keep01;
-              a1 &= keep01;
-              a2 &= keep23;
-              a3 &= keep23;
+            for (int mt = 0; mt < 8; ++mt) {
+              const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+              const uint32_t iAB = __byte_perm(u4_word(vA, mt >> 1), u4_word(vB, mt >> 1), sel);
+              const uint32_t iCD = __byte_perm(u4_word(vC, mt >> 1), u4_word(vD, mt >> 1), sel);
+              uint32_t a0, a1, a2, a3;
+              q8_to_f16x2x2<KVQ>(iAB, a0, a1);
+              q8_to_f16x2x2<KVQ>(iCD, a2, a3);
+              if constexpr (decltype(clear)::value) {
+                a0 &= keep01;
+                a1 &= keep01;
+                a2 &= keep23;
+                a3 &= keep23;
+              }
+#pragma unroll
+              for (int j = 0; j < NPW; ++j) mma_f16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
             }
-#pragma unroll
-            for (int j = 0; j < NPW; ++j) mma_f16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
-          }
+          };
+          if (KVQ == 2 && nvalid < C::T)
+            pv(std::integral_constant<bool, KVQ == 2>{});
+          else
+            pv(std::integral_constant<bool, false>{});
         }
       }
     }
