@@ -20,15 +20,15 @@
 //   S^T[16 tok x 8 heads]  = K[16 x 128] . Q^T[128 x 8]    8 mma (k = 16 dims)
 //   online softmax on the accumulator fragment (each lane: 2 tokens x 2
 //   heads; per-head block max over the 8 lanes sharing lane % 4)
-//   P^T -> bf16 hi + lo, transposed in registers (movmatrix) into B operands
+//   P^T -> bf16, transposed in registers (movmatrix) into B operands
 //   O^T[128 dims x 8 heads] += V^T[128 x 16 tok] . P^T[16 tok x 8 heads]
-//                                                   2 x 8 mma (k = 16 tokens)
+//                                                   8 mma (k = 16 tokens)
 // K and V tiles arrive by TMA with the 128-byte swizzle (two 64-column boxes
 // per tile), so every ldmatrix is bank-conflict free.
 //
-// With a bf16 cache the probabilities enter the PV product as a hi + lo pair
-// of bf16 values (two MMAs), which keeps ~16 mantissa bits; the running sum
-// l stays in fp32.
+// With a bf16 cache the probabilities enter the PV product as bf16 (8
+// significant bits, one MMA); the running sum l stays in fp32, so the
+// log-sum-exp carries no rounding of P.
 //
 // 8-bit caches (int8 or e4m3 codes with one scale per kv head for K and for
 // V): one 128-byte box per row, codes turned into exact f16 values in
@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
       const bool vA = tokA < nvalid;
       const bool vB = tokA + 8 < nvalid;
       const int absA = begin + t * C::T + tokA;                  // absolute token index
-      uint32_t pb[NPW][2], pbl[NPW][2];
+      uint32_t pb[NPW][2];
       bool moved = false;
       float alpha[NPW][2];
 #pragma unroll
@@ -601,9 +601,9 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
         const float pB0 = (mn0 == kNegInf) ? 0.f : fast_exp2(sB0 - mn0);
         const float pA1 = (mn1 == kNegInf) ? 0.f : fast_exp2(sA1 - mn1);
         const float pB1 = (mn1 == kNegInf) ? 0.f : fast_exp2(sB1 - mn1);
-        // Probabilities as hi + lo bf16 pairs (hi = RNE(p), lo = RNE(p - hi)):
-        // two PV products carry ~16 mantissa bits, so the bf16 operand adds
-        // no visible error; the running sum keeps the fp32 values.
+        // Probabilities enter the PV product as bf16 (round to nearest even,
+        // at most 2^-9 relative per p) and the running sum keeps the fp32
+        // values, so the log-sum-exp carries no rounding of P.
         if constexpr (KVQ == 1) {
           // The normaliser sums the f16 probabilities the PV product uses,
           // so that the epilogue's bias removal is exact.
@@ -622,14 +622,8 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
         if constexpr (!C::Q8) {
           const uint32_t XA = pack_bf16x2(pA0, pA1);      // token tA, heads hA hB
           const uint32_t XB = pack_bf16x2(pB0, pB1);      // token tB
-          const uint32_t XAl = pack_bf16x2(pA0 - __uint_as_float(XA << 16),
-                                           pA1 - __uint_as_float(XA & 0xffff0000u));
-          const uint32_t XBl = pack_bf16x2(pB0 - __uint_as_float(XB << 16),
-                                           pB1 - __uint_as_float(XB & 0xffff0000u));
           pb[j][0] = movmatrix_trans(XA);                 // B[k = tokens 0-7][n = head]
           pb[j][1] = movmatrix_trans(XB);                 // B[k = tokens 8-15][n = head]
-          pbl[j][0] = movmatrix_trans(XAl);
-          pbl[j][1] = movmatrix_trans(XBl);
         } else if constexpr (KVQ == 2) {
           // f16 keeps 11 significant bits of p (<= 256 under the lazy
           // rescale): one PV product suffices.
@@ -676,7 +670,6 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
 #pragma unroll
             for (int j = 0; j < NPW; ++j) {
               mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
-              mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pbl[j][0], pbl[j][1]);
             }
           }
         } else {
