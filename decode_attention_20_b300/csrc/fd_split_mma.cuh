@@ -656,22 +656,30 @@ __global__ void __launch_bounds__(W * 32, (KVQ != 0 && W == 8) ? 2 : 1)
         }
         if constexpr (!C::Q8) {
           const int vrow = row0 + r8 + (lane >> 4) * 8;
+          // Only the last, partial tile of a range clears its V elements (a
+          // tile-uniform branch; full tiles spend nothing on it).
+          auto pv = [&](auto clear) {
 #pragma unroll
-          for (int mt = 0; mt < 8; ++mt) {
-            const int col = mt * 16 + ((lane >> 3) & 1) * 8;
-            const uint32_t addr =
-                vbase + (col >> 6) * C::HALF_BYTES + swz128(vrow, (col & 63) >> 3);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(addr, a0, a1, a2, a3);
-            a0 &= keep01;
-            a1 &= keep01;
-            a2 &= keep23;
-            a3 &= keep23;
+            for (int mt = 0; mt < 8; ++mt) {
+              const int col = mt * 16 + ((lane >> 3) & 1) * 8;
+              const uint32_t addr =
+                  vbase + (col >> 6) * C::HALF_BYTES + swz128(vrow, (col & 63) >> 3);
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_trans(addr, a0, a1, a2, a3);
+              if constexpr (decltype(clear)::value) {
+                a0 &= keep01;
+                a1 &= keep01;
+                a2 &= keep23;
+                a3 &= keep23;
+              }
 #pragma unroll
-            for (int j = 0; j < NPW; ++j) {
-              mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
+              for (int j = 0; j < NPW; ++j) mma_bf16_16816(acc[j][mt], a0, a1, a2, a3, pb[j][0], pb[j][1]);
             }
-          }
+          };
+          if (nvalid < C::T)
+            pv(std::integral_constant<bool, true>{});
+          else
+            pv(std::integral_constant<bool, false>{});
         } else {
           // A = V^T with the dims reordered so that a lane reads whole
           // 16-byte chunks: lane (r = lane/4, t = lane%4) reads chunk r of
