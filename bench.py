@@ -37,7 +37,8 @@ Prints ONE JSON line (rank 0):
                pinned host memory of the step's new inputs (query, one new K/V
                row per sequence, packed in one buffer), the rows written into
                the cache, the call, one D2H of out + lse (one buffer),
-               synchronised per step
+               synchronised per step; host wall clock, the median of five
+               equal blocks of steps
   roofline     the dominant kernel's algorithmic bytes (or FLOPs) per launch /
                its mean CUDA-event duration (launches queued back to back,
                without programmatic dependent launch), against the peak
@@ -270,20 +271,28 @@ def _staging(device, specs):
     return h, d, views(h), views(d)
 
 
-def _host_loop_us(stream, steps, step, warmup=5):
+def _host_loop_us(stream, steps, step, warmup=5, blocks=5):
     """Wall-clock microseconds per call of step(i) on `stream`, after
     `warmup` untimed calls (first-use costs: lazy kernel loading, pinned
-    staging, pool growth)."""
+    staging, pool growth): the steps run as `blocks` equal blocks, each
+    timed on its own, and the median block gives the value, so that one
+    stall of the shared host cores does not set it."""
     import torch
     with torch.cuda.stream(stream):
         for i in range(warmup):
             step(i)
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
+    per = max(1, steps // blocks)
+    times = []
+    i = 0
     with torch.cuda.stream(stream):
-        for i in range(steps):
-            step(i)
-    return (time.perf_counter() - t0) * 1e6 / steps
+        for _ in range(blocks):
+            t0 = time.perf_counter()
+            for _ in range(per):
+                step(i)
+                i += 1
+            times.append((time.perf_counter() - t0) * 1e6 / per)
+    return statistics.median(times)
 
 
 class DecodeWorkload(Workload):
