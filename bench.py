@@ -837,7 +837,9 @@ def cpu_baseline_ref_arm(w, short):
         cb["sample"] += "; measured by the reference arm in a separate process"
         return cb
     except Exception:                                   # noqa: BLE001 (fall back to this process)
-        return cpu_baseline(w)
+        cb = cpu_baseline(w)
+        cb["sample"] += "; timed in this process (the reference arm subprocess gave no line)"
+        return cb
 
 
 # ------------------------------------------------------------------ reference arm
@@ -1019,7 +1021,7 @@ def dominant_roofline(w, dom_us, peaks):
 
 
 def measure_config(short, dev, stream, L, peaks, window_s=0.15, ns=0):
-    """One BASELINE workload measured the way the headline is (graph steps
+    """One of the other workloads measured the way the headline is (graph steps
     over rotating copies, direct calls, per-kernel events), as a compact
     record for the line's `configs` object."""
     import torch
@@ -1147,7 +1149,7 @@ def run_fd(args, rank, world):
     vals = max_over_ranks(vals, world)
     us_per_call, e2e_us, dom_us = [float(x) for x in vals.tolist()]
 
-    # The other BASELINE workloads and the batch-1 length sweep, measured the
+    # The other workloads and the batch-1 length sweep, measured the
     # same way (rank 0 of a single-GPU run, default workload only).
     configs = {}
     if world == 1 and args.workload == "b1_64k" and not args.no_configs:
@@ -1317,11 +1319,11 @@ def main(argv=None):
     ap.add_argument("--window-ms", type=float, default=400.0,
                     help="device time the timed steps should span (sets the calls per step)")
     ap.add_argument("--no-configs", action="store_true",
-                    help="skip the other BASELINE workloads and the length sweep in the line")
+                    help="skip the other workloads and the length sweep in the line")
     ap.add_argument("--impl", choices=["fd", "reference"], default="fd")
     ap.add_argument("--workload", default="b1_64k",
-                    choices=["b1_64k", "ragged_b32", "long_b4", "bif_mqa", "paged_b1_64k",
-                             "int8_b1_64k", "e4m3_b1_64k", "verify4_b1_64k"])
+                    choices=["b1_64k", "tiny_fp32", "ragged_b32", "long_b4", "bif_mqa",
+                             "paged_b1_64k", "int8_b1_64k", "e4m3_b1_64k", "verify4_b1_64k"])
     ap.add_argument("--num-splits", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep-splits", default="",
