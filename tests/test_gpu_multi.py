@@ -101,3 +101,15 @@ def test_full_size_verification_b1(cuda_device, tq):
     O, L = _run(c, 0)
     O_ref, L_ref = oracle.multi_token_decode_ref(to_f64(c.q), to_f64(c.k), to_f64(c.v), None, c.scale)
     assert_parity(to_f64(O), to_f64(L), O_ref, L_ref, c.k.dtype, f"verify tq={tq}")
+
+
+def test_nan_padding_past_the_lengths_is_ignored(cuda_device, path):
+    """Cache rows at or past a sequence's length may hold anything, NaN
+    included: the partial last tile of a split clears them before the PV
+    product, and the causal limits keep them out of the scores."""
+    c = inputs.multi_token_case(2, 4, 16, 2, 128, 700, seed=77, seqlens=[333, 70])
+    for b, n in enumerate([333, 70]):
+        c.k[b, n:] = float("nan")
+        c.v[b, n:] = float("nan")
+    for ns in (1, 3, 0):
+        _check(c, ns, f"{path} nan past lengths ns={ns}")

@@ -108,3 +108,19 @@ def test_paged_bad_page_id_is_reported(cuda_device):
             assert ei.value.status == 9
         finally:
             del os.environ["FD_SPLIT_VARIANT"]
+
+
+def test_nan_past_the_lengths_is_ignored(cuda_device, variant):
+    """Page rows at or past a sequence's length may hold anything, NaN
+    included: the tail of its last page and every later page of its table."""
+    ps, pages, lens = 64, 8, [333, 70]
+    case = inputs.paged_case(2, 16, 2, 128, ps, pages, seed=21, seqlens=lens)
+    for b, n in enumerate(lens):
+        for p in range(pages):
+            first = max(0, n - p * ps)
+            if first < ps:
+                page = int(case.block_table[b, p])
+                case.k_pages[page, first:] = float("nan")
+                case.v_pages[page, first:] = float("nan")
+    for ns in [0, 1, 3]:
+        _check(case, ns, f"{variant} nan past lengths ns={ns}")
