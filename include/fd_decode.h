@@ -44,6 +44,14 @@
  *  - Workspace: calls that need scratch memory for partial results allocate
  *    it stream-ordered (cudaMallocAsync / cudaFreeAsync on `stream`), so
  *    calls on different streams or threads never share scratch.
+ *  - Arithmetic: no step of the method is approximated; sums and the online
+ *    softmax are fp32 and the partial results fp32.  With bf16 caches the
+ *    tensor-core kernels round each softmax probability to bf16 (relative
+ *    error at most 2^-9) before the P.V product, while the normaliser and
+ *    the LSE use the fp32 probabilities; with 8-bit caches the probability
+ *    is rounded to f16 (2^-11) and the codes become exact f16 values; fp32
+ *    caches run in fp32 throughout.  Exponentials use the hardware ex2
+ *    approximation.
  */
 #ifndef FD_DECODE_H
 #define FD_DECODE_H
